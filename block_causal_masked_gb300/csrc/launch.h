@@ -1,0 +1,106 @@
+// launch.h -- internal host-side interface between the C ABI (api.cu) and the
+// kernels (attn.cu, vocab.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace bd {
+
+constexpr int kAttnBM = 128;        // packed query rows per CTA (tcgen05 M)
+constexpr int kAttnBN = 128;        // keys per K/V tile
+constexpr int kAttnMaxTiles = 512;  // K/V tiles a CTA may list before its split
+constexpr int kAttnMaxSplits = 64;
+
+// Everything the attention kernels need, in the fork's terms: plain attention is
+// the fork with N = 1, the prefix = rows [0, C) of K/V and the private rows =
+// the active rows [C, C + n_q) (priv_len = 0).
+struct AttnParams {
+  const void* q;          // bf16 [N, n_q, Hq, D]
+  void* o;                // bf16 [N, n_q, Hq, D]
+  float* lse;             // fp32 [N, Hq, n_q] or null
+  float* part_o;          // fp32 [splits, N*n_q*Hq, D]       (splits > 1)
+  float* part_lse;        // fp32 [splits, N*n_q*Hq]          (splits > 1)
+  const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
+  const int32_t* k_pos;        // [C] or null
+  int32_t* dev_status;
+  int N, n_q, Hq, Hkv, G, D, C, priv_len, n_blocks, block_size, num_splits;
+  int rows_per_head;      // N * n_q * G
+  int n_prefix_tiles;     // ceil(C / BN)
+  float scale_log2;       // sm_scale * log2(e)
+  int rope;
+  int delta;
+  unsigned long long rope_turns[64];  // theta^(-2d/D) / (2*pi) as a 0.64 fixed-point fraction
+};
+
+struct AttnMaps {
+  CUtensorMap pk, pv;     // prefix K/V: 3D (D, C, Hkv)
+  CUtensorMap rk, rv;     // private K/V: 4D (D, priv_len + n_q, Hkv, N)
+};
+
+int attn_smem_bytes(int D);
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream);
+
+// ---------------------------------------------------------------- vocab reductions
+
+struct UnmaskParams {
+  const void* logits;
+  int dtype;              // 0 f32, 1 bf16
+  long long ld;
+  int R, V;
+  const int32_t* logit_row;
+  int n_pos;
+  const int32_t* block_start;
+  int n_blocks;
+  uint8_t* state;
+  int32_t* tokens;
+  float tau_full, tau_half;
+  int min_num, min_den, k_fixed, add_num, add_den, act_num, act_den;
+  uint8_t* commit;
+  int32_t* n_committed;
+  int32_t* status;
+  int32_t* pred;
+  float* conf;
+  float* lse;
+  int32_t* dev_status;
+  // workspace carve-up
+  float4* chunk_part;         // [n_pos, chunks]: (max, sum, argmax bits, -)
+  float4* row_result;         // [n_pos]: (conf, lse, pred bits, candidate flag)
+  unsigned int* row_ticket;   // [n_pos]
+  unsigned int* grid_ticket;  // [1]
+  int chunks;                 // CTAs per logits row
+  int chunk_elems;            // elements per chunk (multiple of 8)
+};
+
+struct VerifyParams {
+  int n_seq, L;
+  int32_t* tokens;
+  uint8_t* state;
+  const void* logits;
+  int dtype;
+  long long ld;
+  int n_rows, V;
+  const float* noise;
+  float inv_temp;
+  int32_t* accepted_len;
+  int32_t* bonus;
+  int32_t* bonus_pos;
+  int32_t* dev_status;
+  float4* chunk_part;         // [n_seq * n_rows, chunks]: (score, argmax bits, -, -)
+  int32_t* row_argmax;        // [n_seq * n_rows]
+  unsigned int* row_ticket;   // [n_seq * n_rows]
+  unsigned int* seq_ticket;   // [n_seq]
+  int chunks;
+  int chunk_elems;
+};
+
+size_t unmask_workspace_bytes(int n_pos, int chunks);
+size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks);
+void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems);
+cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
+
+}  // namespace bd

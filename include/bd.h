@@ -1,0 +1,337 @@
+/*
+ * bd.h -- C ABI of libbd: the hot path of block-causal masked-diffusion decoding
+ * on one GB300 (sm_103a).
+ *
+ * One denoising step over the active blocks of a block-causal masked-diffusion
+ * decoder is made of four calls:
+ *
+ *   bd_block_causal_attn   attention of the active blocks over the cached prefix
+ *   bd_unmask_step         argmax / confidence over the vocabulary and the commit rule
+ *   bd_spec_verify         scaffold-speculative verification of a drafted block
+ *   bd_fork_rollouts       attention of N rollouts that share one prefix KV cache
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Ownership: every data pointer is a caller-owned DEVICE buffer (for example a
+ *   torch tensor's data_ptr()).  The library never allocates, frees or keeps a
+ *   pointer past the call; all work is enqueued asynchronously on `stream`
+ *   (a cudaStream_t, NULL = legacy default stream).
+ * - Layout: tensors are dense, row-major in the order their shape is written,
+ *   and start on a 16-byte boundary.
+ * - Workspace: calls that need scratch memory take a caller-owned device buffer
+ *   of at least bd_*_workspace_size(args) bytes.  It must be zero-filled before
+ *   its first use; every call that completes leaves its counter words at zero
+ *   again, so the buffer can be reused by later calls on the same stream without
+ *   clearing.  Calls that share a workspace must not overlap in time.
+ * - Errors: argument errors are found on the host before anything is enqueued
+ *   and returned as a bd_status; nothing is launched in that case.  Errors the
+ *   device finds (a bounded wait that expired, an inconsistent block partition)
+ *   are OR-ed into the optional `dev_status` word (device int32, may be NULL);
+ *   bd_check() reads and maps it.
+ * - The kernels are built for sm_103a only; on any other device the calls
+ *   return BD_ERR_UNSUPPORTED.
+ *
+ * Position states, block states and dtypes are the integer constants below.
+ */
+#ifndef BD_H
+#define BD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bd_status {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes        */
+  BD_ERR_UNSUPPORTED = 2,   /* head dim, GQA ratio, alignment or device not supported  */
+  BD_ERR_WORKSPACE = 3,     /* workspace missing or smaller than bd_*_workspace_size   */
+  BD_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                       */
+  BD_ERR_TIMEOUT = 5,       /* (bd_check) a device-side bounded wait expired           */
+  BD_ERR_DEVICE_INPUT = 6   /* (bd_check) the device found an inconsistent input       */
+} bd_status;
+
+/* bits OR-ed into *dev_status by the kernels */
+#define BD_DEV_TIMEOUT 0x1
+#define BD_DEV_BAD_INPUT 0x2
+
+/* per-position state (uint8) */
+#define BD_MASKED 0
+#define BD_COMMITTED 1
+#define BD_SCAFFOLD 2
+
+/* per-block activation status (int32), see bd_unmask_step */
+#define BD_INACTIVE 0
+#define BD_HALF 1
+#define BD_FULL 2
+#define BD_DONE 3
+
+/* logits element types */
+#define BD_F32 0
+#define BD_BF16 1
+
+/* -----------------------------------------------------------------------------
+ * RoPE applied inside the attention operator to pre-RoPE cached keys.
+ *
+ * FlashDrive tutorial (agifrontier.github.io), section "流式推理": cached keys are
+ * kept without position encoding and RoPE is injected in the operator at the
+ * re-based position p - Δ after the window slides.
+ *
+ * With enabled != 0, cached prefix key s is rotated at position k_pos[s] - delta
+ * before Q·Kᵀ, rotate-half over the pairs (d, d + D/2) with frequency
+ * theta^(-2d/D).  The rotated key enters the bf16 product as bf16.  Queries and
+ * the active positions' own keys must already be rotated by the caller.
+ *   k_pos  device int32 [C], or NULL for k_pos[s] = s
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_rope {
+  int32_t enabled;
+  const int32_t* k_pos;
+  int32_t delta;
+  float theta;
+} bd_rope;
+
+/* -----------------------------------------------------------------------------
+ * bd_block_causal_attn
+ *
+ * Fast-dVLA paper notes (papernotes.org), "关键设计 1. 分块因果注意力"; Fast-dDrive
+ * method summary (e.mffb.com.cn) §3.1; WAM-Diff2 write-up (163.com) §2.1: the
+ * output is cut into blocks; a block attends to the whole cached prefix, to every
+ * earlier block and bidirectionally to itself, never to a later block.  Block
+ * size 1 is ordinary causal attention.
+ *
+ * For active position i in block b(i), query head h (KV head h / (Hq/Hkv)):
+ *   key j is visible  <=>  j < C  or  block(j - C) <= b(i)
+ *   o[i, h]   = softmax_j(q[i,h]·k[h',j] · sm_scale) · v[h', j]   (bf16 out)
+ *   lse[h, i] = ln Σ_visible exp(q[i,h]·k[h',j] · sm_scale)       (fp32)
+ *
+ *   q            bf16 [n_q, Hq, D]
+ *   k, v         bf16 [Hkv, kv_stride, D]; rows [0, C) cached prefix, rows
+ *                [C, C + n_q) the active positions (already rotated); rows past
+ *                C + n_q are never read
+ *   o            bf16 [n_q, Hq, D]
+ *   lse          fp32 [Hq, n_q] natural log, or NULL
+ *   block_start  device int32 [n_blocks + 1]: 0 = block_start[0] < ... <
+ *                block_start[n_blocks] = n_q; or NULL for uniform blocks of
+ *                block_size positions (the last one ragged)
+ *   sm_scale     0 -> D^-1/2
+ *   num_splits   KV splits across CTAs; 0 -> chosen by the library
+ * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= n_q; 0 <= C; kv_stride >= C + n_q.
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_attn_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const int32_t* block_start;
+  int32_t n_blocks;
+  int32_t block_size;
+  int32_t C;
+  int32_t n_q;
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t D;
+  int32_t kv_stride;
+  float sm_scale;
+  bd_rope rope;
+  int32_t num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+} bd_attn_args;
+
+bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream);
+size_t bd_attn_workspace_size(const bd_attn_args* a);
+
+/* -----------------------------------------------------------------------------
+ * bd_fork_rollouts
+ *
+ * Fast-dDrive method summary (e.mffb.com.cn) §3.3 "共享前缀多轨迹Rollout": the
+ * first sections are decoded once; their KV cache is shared by N trajectory
+ * rollouts, which are forked from it and differ only in their trajectory part.
+ *
+ * Rollout r's active query i (block b(i)) attends to the whole shared prefix
+ * (never copied), to its own private rows [0, priv_len) (its earlier trajectory
+ * blocks) and block-causally to its active rows [priv_len, priv_len + n_q).
+ *
+ *   q                 bf16 [N, n_q, Hq, D]
+ *   prefix_k/v        bf16 [Hkv, prefix_stride, D], rows [0, C) used; read only
+ *   priv_k/v          bf16 [N, Hkv, priv_stride, D], rows [0, priv_len + n_q) used
+ *   o                 bf16 [N, n_q, Hq, D]
+ *   lse               fp32 [N, Hq, n_q] or NULL
+ *   block_start, n_blocks, block_size, sm_scale, rope, num_splits: as in
+ *   bd_attn_args (rope applies to the shared prefix keys only)
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_fork_args {
+  int32_t N;
+  const void* q;
+  const void* prefix_k;
+  const void* prefix_v;
+  int32_t prefix_stride;
+  const void* priv_k;
+  const void* priv_v;
+  int32_t priv_stride;
+  int32_t priv_len;
+  void* o;
+  float* lse;
+  const int32_t* block_start;
+  int32_t n_blocks;
+  int32_t block_size;
+  int32_t C;
+  int32_t n_q;
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t D;
+  float sm_scale;
+  bd_rope rope;
+  int32_t num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+} bd_fork_args;
+
+bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream);
+size_t bd_fork_workspace_size(const bd_fork_args* a);
+
+/* -----------------------------------------------------------------------------
+ * bd_unmask_step
+ *
+ * Fast-dDrive method summary (e.mffb.com.cn) §3.1 (masked positions predicted
+ * by the reverse process), §3.2 mode 2 step 1 (scaffold auto-accepted);
+ * Fast-dVLA paper notes, "关键设计 2" (unmasked tokens stay fixed) and "关键设计
+ * 4. 流水线并行解码" (half / full activation by the predecessor's completion
+ * ratio; confidence threshold; at least a fraction of the remaining tokens).
+ *
+ * For every candidate position p (state[p] == BD_MASKED and logit_row[p] >= 0):
+ *   pred[p] = argmax_v logits[row, v]           (lowest index on ties)
+ *   conf[p] = max softmax probability = 1 / Σ_v exp(l_v - max)
+ *   lse[p]  = max + ln Σ_v exp(l_v - max)
+ * Block status, from the state at call time:
+ *   BD_DONE if the block has no masked position; else block 0 is BD_FULL (its
+ *   predecessor lies in the cache); else, with r = non-masked positions of the
+ *   previous block (scaffold included) over its size:
+ *   r >= act_num/act_den -> BD_FULL, r >= add_num/add_den -> BD_HALF, else
+ *   BD_INACTIVE (exact integer comparison).
+ * Commits (rem = candidates of the block):
+ *   BD_FULL:  {conf >= tau_full} ∪ {the n_min most confident candidates},
+ *             n_min = min(rem, max(k_fixed, ceil(rem * min_num / min_den))),
+ *             equal confidences ranked by lower position;
+ *   BD_HALF:  {conf >= tau_half};  BD_INACTIVE / BD_DONE: nothing.
+ * A committed position gets tokens[p] = pred[p], state[p] = BD_COMMITTED,
+ * commit[p] = 1.  Scaffold and committed positions never change.
+ *
+ *   logits        [R, V] of logits_dtype (BD_F32 | BD_BF16), row stride logits_ld
+ *                 elements (multiple of 8)
+ *   logit_row     int32 [n_pos]: logits row of each position, or -1
+ *   block_start   int32 [n_blocks + 1] over the n_pos positions (device)
+ *   state         uint8 [n_pos] in/out;  tokens int32 [n_pos] in/out
+ *   commit        uint8 [n_pos] out;  n_committed, status int32 [n_blocks] out
+ *   pred, conf, lse   int32/fp32/fp32 [n_pos] out, or NULL; non-candidates
+ *                 get -1 / 0 / 0
+ * Supported: n_pos <= 4096 and every block <= 1024 positions.
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_unmask_args {
+  const void* logits;
+  int32_t logits_dtype;
+  int64_t logits_ld;
+  int32_t R;
+  int32_t V;
+  const int32_t* logit_row;
+  int32_t n_pos;
+  const int32_t* block_start;
+  int32_t n_blocks;
+  uint8_t* state;
+  int32_t* tokens;
+  float tau_full;
+  float tau_half;
+  int32_t min_num, min_den;
+  int32_t k_fixed;
+  int32_t add_num, add_den;
+  int32_t act_num, act_den;
+  uint8_t* commit;
+  int32_t* n_committed;
+  int32_t* status;
+  int32_t* pred;
+  float* conf;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+} bd_unmask_args;
+
+bd_status bd_unmask_step(const bd_unmask_args* a, void* stream);
+size_t bd_unmask_workspace_size(const bd_unmask_args* a);
+
+/* -----------------------------------------------------------------------------
+ * bd_spec_verify
+ *
+ * Fast-dDrive method summary (e.mffb.com.cn) §3.2 "模式二：Scaffold Speculative
+ * Decoding": scaffold accepted as is; the MDM draft of the block's editable
+ * positions is compared left to right with the AR argmax; matches are accepted;
+ * at the first mismatch the AR token is taken, later drafts are dropped, and a
+ * bonus token is accepted.  Fast-dDrive abstract / §1: for test-time scaling the
+ * AR verifier of the trajectory section is sampled.
+ *
+ * For each sequence s of n_seq (independent rollouts), with E = number of
+ * non-scaffold slots of its block and e the editable ordinal of a slot:
+ *   t_e = argmax_v ar[s, e, v]                       (greedy, noise == NULL)
+ *   t_e = argmax_v (ar[s,e,v] / temperature - ln(-ln u[s,e,v]))   (sampled)
+ * Going over the masked editable slots in order (committed slots are skipped):
+ * a slot whose draft equals t_e is committed; the first one that differs takes
+ * t_e, is committed and is the bonus; masked slots after it return to masked
+ * with token -1.  If none differs, the bonus is t_E (row E), which belongs to
+ * the position after the block (bonus_pos = L).
+ *
+ *   tokens        int32 [n_seq, L] in/out (masked slots hold the draft)
+ *   state         uint8 [n_seq, L] in/out
+ *   ar_logits     [n_seq, n_rows, V] of logits_dtype, row stride logits_ld;
+ *                 n_rows must equal E + 1 for every sequence
+ *   noise         fp32 [n_seq, n_rows, V] uniforms in (0, 1), row stride
+ *                 logits_ld, or NULL for greedy
+ *   accepted_len  int32 [n_seq] out: slots committed this round, bonus included
+ *   bonus, bonus_pos  int32 [n_seq] out
+ * Supported: L <= 1024.
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_verify_args {
+  int32_t n_seq;
+  int32_t L;
+  int32_t* tokens;
+  uint8_t* state;
+  const void* ar_logits;
+  int32_t logits_dtype;
+  int64_t logits_ld;
+  int32_t n_rows;
+  int32_t V;
+  const float* noise;
+  float temperature;
+  int32_t* accepted_len;
+  int32_t* bonus;
+  int32_t* bonus_pos;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+} bd_verify_args;
+
+bd_status bd_spec_verify(const bd_verify_args* a, void* stream);
+size_t bd_verify_workspace_size(const bd_verify_args* a);
+
+/* -----------------------------------------------------------------------------
+ * Helpers
+ * ---------------------------------------------------------------------------*/
+const char* bd_status_string(bd_status s);
+
+/* Synchronises `stream`, reads *dev_status and maps its bits: BD_DEV_TIMEOUT ->
+ * BD_ERR_TIMEOUT, BD_DEV_BAD_INPUT -> BD_ERR_DEVICE_INPUT, 0 -> BD_OK.  The word
+ * is left as it is (clear it with cudaMemsetAsync to reuse it). */
+bd_status bd_check(const int32_t* dev_status, void* stream);
+
+/* Library version, "major.minor.patch". */
+const char* bd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_H */
