@@ -1,0 +1,304 @@
+"""Python binding of libbd, the C-ABI library of the block-causal masked-diffusion
+decode step on GB300 (sm_103a).
+
+Argument marshalling only: every function here fills the C struct declared in
+``include/bd.h`` from torch tensors (device memory and the current stream) and
+calls the library entry point of the same name.  All arithmetic runs in the
+library's CUDA kernels; there is no fallback.  If the library cannot be loaded
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_spec_verify", "bd_check",
+           "bd_status_string", "lib", "BdError", "Workspace", "MASKED", "COMMITTED", "SCAFFOLD",
+           "INACTIVE", "HALF", "FULL", "DONE"]
+
+MASKED, COMMITTED, SCAFFOLD = 0, 1, 2
+INACTIVE, HALF, FULL, DONE = 0, 1, 2, 3
+BD_F32, BD_BF16 = 0, 1
+
+
+class BdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({bd_status_string(status)})")
+        self.status = status
+
+
+class bd_rope(ct.Structure):
+    _fields_ = [("enabled", ct.c_int32), ("k_pos", ct.c_void_p), ("delta", ct.c_int32), ("theta", ct.c_float)]
+
+
+class bd_attn_args(ct.Structure):
+    _fields_ = [("q", ct.c_void_p), ("k", ct.c_void_p), ("v", ct.c_void_p), ("o", ct.c_void_p), ("lse", ct.c_void_p),
+                ("block_start", ct.c_void_p), ("n_blocks", ct.c_int32), ("block_size", ct.c_int32),
+                ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
+                ("kv_stride", ct.c_int32), ("sm_scale", ct.c_float), ("rope", bd_rope),
+                ("num_splits", ct.c_int32), ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t),
+                ("dev_status", ct.c_void_p)]
+
+
+class bd_fork_args(ct.Structure):
+    _fields_ = [("N", ct.c_int32), ("q", ct.c_void_p), ("prefix_k", ct.c_void_p), ("prefix_v", ct.c_void_p),
+                ("prefix_stride", ct.c_int32), ("priv_k", ct.c_void_p), ("priv_v", ct.c_void_p),
+                ("priv_stride", ct.c_int32), ("priv_len", ct.c_int32), ("o", ct.c_void_p), ("lse", ct.c_void_p),
+                ("block_start", ct.c_void_p), ("n_blocks", ct.c_int32), ("block_size", ct.c_int32),
+                ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
+                ("sm_scale", ct.c_float), ("rope", bd_rope), ("num_splits", ct.c_int32),
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+
+
+class bd_unmask_args(ct.Structure):
+    _fields_ = [("logits", ct.c_void_p), ("logits_dtype", ct.c_int32), ("logits_ld", ct.c_int64),
+                ("R", ct.c_int32), ("V", ct.c_int32), ("logit_row", ct.c_void_p), ("n_pos", ct.c_int32),
+                ("block_start", ct.c_void_p), ("n_blocks", ct.c_int32), ("state", ct.c_void_p),
+                ("tokens", ct.c_void_p), ("tau_full", ct.c_float), ("tau_half", ct.c_float),
+                ("min_num", ct.c_int32), ("min_den", ct.c_int32), ("k_fixed", ct.c_int32),
+                ("add_num", ct.c_int32), ("add_den", ct.c_int32), ("act_num", ct.c_int32), ("act_den", ct.c_int32),
+                ("commit", ct.c_void_p), ("n_committed", ct.c_void_p), ("status", ct.c_void_p),
+                ("pred", ct.c_void_p), ("conf", ct.c_void_p), ("lse", ct.c_void_p),
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+
+
+class bd_verify_args(ct.Structure):
+    _fields_ = [("n_seq", ct.c_int32), ("L", ct.c_int32), ("tokens", ct.c_void_p), ("state", ct.c_void_p),
+                ("ar_logits", ct.c_void_p), ("logits_dtype", ct.c_int32), ("logits_ld", ct.c_int64),
+                ("n_rows", ct.c_int32), ("V", ct.c_int32), ("noise", ct.c_void_p), ("temperature", ct.c_float),
+                ("accepted_len", ct.c_void_p), ("bonus", ct.c_void_p), ("bonus_pos", ct.c_void_p),
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ct.CDLL:
+    """The loaded libbd.so (built in-tree on first use when nvcc is present)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ct.CDLL(path)
+            for name, argt in (("bd_block_causal_attn", bd_attn_args), ("bd_fork_rollouts", bd_fork_args),
+                               ("bd_unmask_step", bd_unmask_args), ("bd_spec_verify", bd_verify_args)):
+                fn = getattr(L, name)
+                fn.argtypes = [ct.POINTER(argt), ct.c_void_p]
+                fn.restype = ct.c_int
+            for name, argt in (("bd_attn_workspace_size", bd_attn_args), ("bd_fork_workspace_size", bd_fork_args),
+                               ("bd_unmask_workspace_size", bd_unmask_args),
+                               ("bd_verify_workspace_size", bd_verify_args)):
+                fn = getattr(L, name)
+                fn.argtypes = [ct.POINTER(argt)]
+                fn.restype = ct.c_size_t
+            L.bd_status_string.argtypes = [ct.c_int]
+            L.bd_status_string.restype = ct.c_char_p
+            L.bd_check.argtypes = [ct.c_void_p, ct.c_void_p]
+            L.bd_check.restype = ct.c_int
+            L.bd_version.restype = ct.c_char_p
+            _lib = L
+    return _lib
+
+
+def bd_status_string(status: int) -> str:
+    return lib().bd_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ct.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ct.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise BdError(fn, st)
+
+
+class Workspace:
+    """Zero-filled device scratch grown on demand (one per device and purpose).
+
+    The library leaves its counters at zero after every completed call, so the
+    buffer is cleared only when it is (re)allocated."""
+
+    def __init__(self):
+        self._buf = {}
+
+    def get(self, nbytes: int, device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        key = torch.device(device).index
+        buf = self._buf.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+            self._buf[key] = buf
+        return buf
+
+
+_WS = {"attn": Workspace(), "unmask": Workspace(), "verify": Workspace()}
+
+
+def _rope(rope) -> bd_rope:
+    r = bd_rope()
+    if rope:
+        r.enabled = 1
+        kp = rope.get("k_pos")
+        r.k_pos = None if kp is None else kp.data_ptr()
+        r.delta = int(rope.get("delta", 0))
+        r.theta = float(rope.get("theta", 10000.0))
+    return r
+
+
+def _bs(block_start):
+    if block_start is None:
+        return None, 0
+    assert block_start.dtype == torch.int32 and block_start.is_cuda
+    return block_start.data_ptr(), block_start.numel() - 1
+
+
+def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0, o=None, lse=None,
+                         sm_scale: float = 0.0, rope=None, num_splits: int = 0, workspace=None,
+                         dev_status=None, stream=None):
+    """Block-causal attention of the active positions.  q [n_q, Hq, D] bf16;
+    k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after).
+    Returns (o [n_q, Hq, D] bf16, lse [Hq, n_q] fp32)."""
+    n_q, Hq, D = q.shape
+    Hkv, kv_stride, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, n_q), dtype=torch.float32, device=q.device)
+    a = bd_attn_args()
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+    a.block_start, a.n_blocks = _bs(block_start)
+    a.block_size = int(block_size)
+    a.C, a.n_q, a.Hq, a.Hkv, a.D, a.kv_stride = int(C), n_q, Hq, Hkv, D, kv_stride
+    a.sm_scale = float(sm_scale)
+    a.rope = _rope(rope)
+    a.num_splits = int(num_splits)
+    need = lib().bd_attn_workspace_size(a)
+    ws = workspace if workspace is not None else _WS["attn"].get(need, q.device)
+    a.workspace = None if ws is None else ws.data_ptr()
+    a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    _check("bd_block_causal_attn", lib().bd_block_causal_attn(a, _stream(stream)))
+    return o, lse
+
+
+def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: int, block_start=None,
+                     block_size: int = 0, o=None, lse=None, sm_scale: float = 0.0, rope=None, num_splits: int = 0,
+                     workspace=None, dev_status=None, stream=None):
+    """N rollouts over one shared prefix.  q [N, n_q, Hq, D]; prefix_k/v [Hkv, prefix_stride, D];
+    priv_k/v [N, Hkv, priv_stride, D].  Returns (o [N, n_q, Hq, D], lse [N, Hq, n_q])."""
+    N, n_q, Hq, D = q.shape
+    Hkv, prefix_stride, _ = prefix_k.shape
+    priv_stride = priv_k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((N, Hq, n_q), dtype=torch.float32, device=q.device)
+    a = bd_fork_args()
+    a.N, a.q = N, q.data_ptr()
+    a.prefix_k, a.prefix_v, a.prefix_stride = prefix_k.data_ptr(), prefix_v.data_ptr(), prefix_stride
+    a.priv_k, a.priv_v, a.priv_stride, a.priv_len = priv_k.data_ptr(), priv_v.data_ptr(), priv_stride, int(priv_len)
+    a.o, a.lse = o.data_ptr(), lse.data_ptr()
+    a.block_start, a.n_blocks = _bs(block_start)
+    a.block_size = int(block_size)
+    a.C, a.n_q, a.Hq, a.Hkv, a.D = int(C), n_q, Hq, Hkv, D
+    a.sm_scale = float(sm_scale)
+    a.rope = _rope(rope)
+    a.num_splits = int(num_splits)
+    need = lib().bd_fork_workspace_size(a)
+    ws = workspace if workspace is not None else _WS["attn"].get(need, q.device)
+    a.workspace = None if ws is None else ws.data_ptr()
+    a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    _check("bd_fork_rollouts", lib().bd_fork_rollouts(a, _stream(stream)))
+    return o, lse
+
+
+def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: float, tau_half: float,
+                   min_frac=(1, 4), k_fixed: int = 0, add_thr=(1, 2), act_thr=(17, 20), commit=None,
+                   n_committed=None, status=None, pred=None, conf=None, lse=None, workspace=None,
+                   dev_status=None, stream=None):
+    """One unmask/commit step; updates ``state`` and ``tokens`` in place.
+    Returns dict(commit, n_committed, status, pred, conf, lse)."""
+    R, V = logits.shape
+    n_pos = state.numel()
+    n_blocks = block_start.numel() - 1
+    dev = logits.device
+    commit = torch.empty(n_pos, dtype=torch.uint8, device=dev) if commit is None else commit
+    n_committed = torch.empty(n_blocks, dtype=torch.int32, device=dev) if n_committed is None else n_committed
+    status = torch.empty(n_blocks, dtype=torch.int32, device=dev) if status is None else status
+    pred = torch.empty(n_pos, dtype=torch.int32, device=dev) if pred is None else pred
+    conf = torch.empty(n_pos, dtype=torch.float32, device=dev) if conf is None else conf
+    lse = torch.empty(n_pos, dtype=torch.float32, device=dev) if lse is None else lse
+    a = bd_unmask_args()
+    a.logits = logits.data_ptr()
+    a.logits_dtype = BD_BF16 if logits.dtype == torch.bfloat16 else BD_F32
+    a.logits_ld = logits.stride(0)
+    a.R, a.V = R, V
+    a.logit_row, a.n_pos = logit_row.data_ptr(), n_pos
+    a.block_start, a.n_blocks = block_start.data_ptr(), n_blocks
+    a.state, a.tokens = state.data_ptr(), tokens.data_ptr()
+    a.tau_full, a.tau_half = float(tau_full), float(tau_half)
+    a.min_num, a.min_den = int(min_frac[0]), int(min_frac[1])
+    a.k_fixed = int(k_fixed)
+    a.add_num, a.add_den = int(add_thr[0]), int(add_thr[1])
+    a.act_num, a.act_den = int(act_thr[0]), int(act_thr[1])
+    a.commit, a.n_committed, a.status = commit.data_ptr(), n_committed.data_ptr(), status.data_ptr()
+    a.pred, a.conf, a.lse = pred.data_ptr(), conf.data_ptr(), lse.data_ptr()
+    need = lib().bd_unmask_workspace_size(a)
+    ws = workspace if workspace is not None else _WS["unmask"].get(need, dev)
+    a.workspace = None if ws is None else ws.data_ptr()
+    a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    _check("bd_unmask_step", lib().bd_unmask_step(a, _stream(stream)))
+    return dict(commit=commit, n_committed=n_committed, status=status, pred=pred, conf=conf, lse=lse)
+
+
+def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.0, accepted_len=None, bonus=None,
+                   bonus_pos=None, workspace=None, dev_status=None, stream=None):
+    """Scaffold-speculative verify; updates ``tokens``/``state`` [n_seq, L] in place.
+    ar_logits [n_seq, n_rows, V]; noise fp32 of the same shape or None.
+    Returns (accepted_len, bonus, bonus_pos), int32 [n_seq] each."""
+    n_seq, L = tokens.shape
+    _, n_rows, V = ar_logits.shape
+    dev = tokens.device
+    accepted_len = torch.empty(n_seq, dtype=torch.int32, device=dev) if accepted_len is None else accepted_len
+    bonus = torch.empty(n_seq, dtype=torch.int32, device=dev) if bonus is None else bonus
+    bonus_pos = torch.empty(n_seq, dtype=torch.int32, device=dev) if bonus_pos is None else bonus_pos
+    assert ar_logits.stride(0) == n_rows * ar_logits.stride(1)
+    if noise is not None:
+        assert noise.stride(1) == ar_logits.stride(1) and noise.stride(0) == ar_logits.stride(0)
+    a = bd_verify_args()
+    a.n_seq, a.L = n_seq, L
+    a.tokens, a.state = tokens.data_ptr(), state.data_ptr()
+    a.ar_logits = ar_logits.data_ptr()
+    a.logits_dtype = BD_BF16 if ar_logits.dtype == torch.bfloat16 else BD_F32
+    a.logits_ld = ar_logits.stride(1)
+    a.n_rows, a.V = n_rows, V
+    a.noise = None if noise is None else noise.data_ptr()
+    a.temperature = float(temperature)
+    a.accepted_len, a.bonus, a.bonus_pos = accepted_len.data_ptr(), bonus.data_ptr(), bonus_pos.data_ptr()
+    need = lib().bd_verify_workspace_size(a)
+    ws = workspace if workspace is not None else _WS["verify"].get(need, dev)
+    a.workspace = None if ws is None else ws.data_ptr()
+    a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    _check("bd_spec_verify", lib().bd_spec_verify(a, _stream(stream)))
+    return accepted_len, bonus, bonus_pos
+
+
+def bd_check(dev_status, stream=None) -> int:
+    """Synchronises the stream and maps the device status word (0 = ok)."""
+    return lib().bd_check(dev_status.data_ptr(), _stream(stream))

@@ -1,0 +1,473 @@
+// api.cu -- the extern "C" entry points of libbd (declared in include/bd.h):
+// argument validation on the host, workspace sizing and carving, TMA tensor
+// maps (cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda), and the kernel launches of attn.cu / vocab.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/bd.h"
+#include "launch.h"
+
+namespace {
+
+using namespace bd;
+
+// Work is planned for the 152 SMs of a GB300 so that workspace sizes are plain
+// host arithmetic that does not depend on which device is current.
+constexpr int kPlanSms = 152;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// ------------------------------------------------------------------ device checks
+
+std::mutex g_mu;
+int g_dev_cc[64];  // 0 unknown, else major*10+minor
+
+bd_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev_cc[dev] == 0) {
+    int ma = 0, mi = 0;
+    if (cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return BD_ERR_CUDA;
+    g_dev_cc[dev] = ma * 10 + mi;
+  }
+  return g_dev_cc[dev] == 103 ? BD_OK : BD_ERR_UNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// bf16 K/V tensor map with a {64, 128, 1, ...} box and 128-byte swizzle.
+bd_status make_kv_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides) {
+  auto fn = encode_fn();
+  if (!fn) return BD_ERR_CUDA;
+  cuuint64_t gdim[4];
+  cuuint64_t gstr[3];
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kAttnBN), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) gstr[i] = strides[i];
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstr, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ attention (plain and fork)
+
+struct AttnDesc {
+  int N;
+  const void* q;
+  const void* pk;
+  const void* pv;
+  long long prefix_stride;
+  const void* rk;
+  const void* rv;
+  long long priv_stride;
+  int priv_len;
+  void* o;
+  float* lse;
+  const int32_t* block_start;
+  int n_blocks, block_size, C, n_q, Hq, Hkv, D;
+  float sm_scale;
+  bd_rope rope;
+  int num_splits;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* ds;
+};
+
+struct AttnPlan {
+  int G, rows_per_head, m_tiles, n_prefix_tiles, splits;
+  size_t ws_bytes;
+};
+
+bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
+  if (d.N < 1 || d.n_q < 1 || d.C < 0 || d.Hq < 1 || d.Hkv < 1 || d.priv_len < 0) return BD_ERR_INVALID_ARG;
+  if (d.D != 64 && d.D != 128) return BD_ERR_UNSUPPORTED;
+  if (d.Hq % d.Hkv != 0) return BD_ERR_UNSUPPORTED;
+  if (d.block_start == nullptr) {
+    if (d.block_size < 1) return BD_ERR_INVALID_ARG;
+  } else if (d.n_blocks < 1 || d.n_blocks > d.n_q) {
+    return BD_ERR_INVALID_ARG;
+  }
+  if (d.num_splits < 0 || d.num_splits > kAttnMaxSplits) return BD_ERR_INVALID_ARG;
+  if (d.rope.enabled && !(d.rope.theta > 0.f)) return BD_ERR_INVALID_ARG;
+  const long long G = d.Hq / d.Hkv;
+  const long long per_roll = static_cast<long long>(d.n_q) * G;
+  const long long rows = per_roll * d.N;
+  if (rows > (1ll << 30)) return BD_ERR_UNSUPPORTED;
+  pl->G = static_cast<int>(G);
+  pl->rows_per_head = static_cast<int>(rows);
+  pl->m_tiles = static_cast<int>((rows + kAttnBM - 1) / kAttnBM);
+  pl->n_prefix_tiles = (d.C + kAttnBN - 1) / kAttnBN;
+  const long long priv_tiles = (d.priv_len + d.n_q + kAttnBN - 1) / kAttnBN;
+  const long long rolls_per_tile = (kAttnBM - 1) / per_roll + 2 < d.N ? (kAttnBM - 1) / per_roll + 2 : d.N;
+  const long long max_tiles = pl->n_prefix_tiles + rolls_per_tile * priv_tiles;
+  if (max_tiles > kAttnMaxTiles) return BD_ERR_UNSUPPORTED;
+  int splits = d.num_splits;
+  if (splits == 0) {
+    // spread the KV range of every (row tile, KV head) over the SMs, keeping at
+    // least two tiles per split so that the ring stays busy
+    const long long base = static_cast<long long>(pl->m_tiles) * d.Hkv;
+    long long s = kPlanSms / base;
+    const long long by_tiles = max_tiles / 2;
+    if (s > by_tiles) s = by_tiles;
+    if (s > 32) s = 32;
+    splits = s < 1 ? 1 : static_cast<int>(s);
+  }
+  pl->splits = splits;
+  const size_t total = static_cast<size_t>(rows) / G * d.Hq;  // N * n_q * Hq output rows
+  pl->ws_bytes = splits > 1 ? align256(sizeof(float) * splits * total * d.D) + align256(sizeof(float) * splits * total)
+                            : 0;
+  return BD_OK;
+}
+
+bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
+  AttnPlan pl;
+  bd_status st = plan_attention(d, &pl);
+  if (st != BD_OK) return st;
+  if (!d.q || !d.pv || !d.pk || !d.rk || !d.rv || !d.o) return BD_ERR_INVALID_ARG;
+  if (!aligned(d.q, 16) || !aligned(d.o, 16) || !aligned(d.pk, 16) || !aligned(d.pv, 16) || !aligned(d.rk, 16) ||
+      !aligned(d.rv, 16) || (d.lse && !aligned(d.lse, 4)))
+    return BD_ERR_UNSUPPORTED;
+  if (pl.ws_bytes > 0 && (d.ws == nullptr || d.ws_bytes < pl.ws_bytes || !aligned(d.ws, 256)))
+    return BD_ERR_WORKSPACE;
+  if ((st = check_device()) != BD_OK) return st;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = d.q;
+  p.o = d.o;
+  p.lse = d.lse;
+  const size_t total = static_cast<size_t>(d.N) * d.n_q * d.Hq;
+  if (pl.splits > 1) {
+    p.part_o = static_cast<float*>(d.ws);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(d.ws) + align256(sizeof(float) * pl.splits * total * d.D));
+  }
+  p.block_start = d.block_start;
+  p.k_pos = d.rope.enabled ? d.rope.k_pos : nullptr;
+  p.dev_status = d.ds;
+  p.N = d.N;
+  p.n_q = d.n_q;
+  p.Hq = d.Hq;
+  p.Hkv = d.Hkv;
+  p.G = pl.G;
+  p.D = d.D;
+  p.C = d.C;
+  p.priv_len = d.priv_len;
+  p.n_blocks = d.n_blocks;
+  p.block_size = d.block_size;
+  p.num_splits = pl.splits;
+  p.rows_per_head = pl.rows_per_head;
+  p.n_prefix_tiles = pl.n_prefix_tiles;
+  const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.rope = d.rope.enabled ? 1 : 0;
+  p.delta = d.rope.delta;
+  if (p.rope) {
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < d.D / 2; ++i) {
+      const double f = std::pow(static_cast<double>(d.rope.theta), -2.0 * i / d.D);
+      double x = f / two_pi;
+      x -= std::floor(x);
+      p.rope_turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
+    }
+  }
+
+  AttnMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const uint64_t row_b = static_cast<uint64_t>(d.D) * 2;
+  if (d.C > 0) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.C), static_cast<uint64_t>(d.Hkv)};
+    const uint64_t strides[2] = {row_b, static_cast<uint64_t>(d.prefix_stride) * row_b};
+    if ((st = make_kv_map(&maps.pk, d.pk, 3, dims, strides)) != BD_OK) return st;
+    if ((st = make_kv_map(&maps.pv, d.pv, 3, dims, strides)) != BD_OK) return st;
+  }
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.priv_len + d.n_q),
+                              static_cast<uint64_t>(d.Hkv), static_cast<uint64_t>(d.N)};
+    const uint64_t strides[3] = {row_b, static_cast<uint64_t>(d.priv_stride) * row_b,
+                                 static_cast<uint64_t>(d.priv_stride) * row_b * d.Hkv};
+    if ((st = make_kv_map(&maps.rk, d.rk, 4, dims, strides)) != BD_OK) return st;
+    if ((st = make_kv_map(&maps.rv, d.rv, 4, dims, strides)) != BD_OK) return st;
+  }
+  return launch_attention(p, maps, pl.m_tiles, stream) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+AttnDesc desc_of(const bd_attn_args* a) {
+  AttnDesc d;
+  std::memset(&d, 0, sizeof(d));
+  d.N = 1;
+  d.q = a->q;
+  d.pk = a->k;
+  d.pv = a->v;
+  d.prefix_stride = a->kv_stride;
+  const size_t off = static_cast<size_t>(a->C > 0 ? a->C : 0) * (a->D > 0 ? a->D : 0) * 2;
+  d.rk = a->k ? static_cast<const char*>(a->k) + off : nullptr;
+  d.rv = a->v ? static_cast<const char*>(a->v) + off : nullptr;
+  d.priv_stride = a->kv_stride;
+  d.priv_len = 0;
+  d.o = a->o;
+  d.lse = a->lse;
+  d.block_start = a->block_start;
+  d.n_blocks = a->n_blocks;
+  d.block_size = a->block_size;
+  d.C = a->C;
+  d.n_q = a->n_q;
+  d.Hq = a->Hq;
+  d.Hkv = a->Hkv;
+  d.D = a->D;
+  d.sm_scale = a->sm_scale;
+  d.rope = a->rope;
+  d.num_splits = a->num_splits;
+  d.ws = a->workspace;
+  d.ws_bytes = a->workspace_bytes;
+  d.ds = a->dev_status;
+  return d;
+}
+
+AttnDesc desc_of(const bd_fork_args* a) {
+  AttnDesc d;
+  std::memset(&d, 0, sizeof(d));
+  d.N = a->N;
+  d.q = a->q;
+  d.pk = a->prefix_k;
+  d.pv = a->prefix_v;
+  d.prefix_stride = a->prefix_stride;
+  d.rk = a->priv_k;
+  d.rv = a->priv_v;
+  d.priv_stride = a->priv_stride;
+  d.priv_len = a->priv_len;
+  d.o = a->o;
+  d.lse = a->lse;
+  d.block_start = a->block_start;
+  d.n_blocks = a->n_blocks;
+  d.block_size = a->block_size;
+  d.C = a->C;
+  d.n_q = a->n_q;
+  d.Hq = a->Hq;
+  d.Hkv = a->Hkv;
+  d.D = a->D;
+  d.sm_scale = a->sm_scale;
+  d.rope = a->rope;
+  d.num_splits = a->num_splits;
+  d.ws = a->workspace;
+  d.ws_bytes = a->workspace_bytes;
+  d.ds = a->dev_status;
+  return d;
+}
+
+// ------------------------------------------------------------------ unmask / verify
+
+bd_status plan_unmask(const bd_unmask_args* a, int* chunks, int* elems, size_t* ws) {
+  if (!a) return BD_ERR_INVALID_ARG;
+  if (a->R < 1 || a->V < 1 || a->n_pos < 1 || a->n_blocks < 1 || a->n_blocks > a->n_pos) return BD_ERR_INVALID_ARG;
+  if (a->n_pos > 2048) return BD_ERR_UNSUPPORTED;
+  if (a->logits_dtype != BD_F32 && a->logits_dtype != BD_BF16) return BD_ERR_INVALID_ARG;
+  if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
+  if (a->min_den < 1 || a->add_den < 1 || a->act_den < 1 || a->min_num < 0 || a->add_num < 0 || a->act_num < 0 ||
+      a->k_fixed < 0)
+    return BD_ERR_INVALID_ARG;
+  const int rows = a->R < a->n_pos ? a->R : a->n_pos;
+  vocab_split(rows, a->V, kPlanSms, chunks, elems);
+  *ws = unmask_workspace_bytes(a->n_pos, *chunks);
+  return BD_OK;
+}
+
+bd_status plan_verify(const bd_verify_args* a, int* chunks, int* elems, size_t* ws) {
+  if (!a) return BD_ERR_INVALID_ARG;
+  if (a->n_seq < 1 || a->L < 1 || a->n_rows < 1 || a->n_rows > a->L + 1 || a->V < 1) return BD_ERR_INVALID_ARG;
+  if (a->L > 1024) return BD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->n_seq) * a->n_rows > 65535) return BD_ERR_UNSUPPORTED;
+  if (a->logits_dtype != BD_F32 && a->logits_dtype != BD_BF16) return BD_ERR_INVALID_ARG;
+  if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
+  if (a->noise && !(a->temperature > 0.f)) return BD_ERR_INVALID_ARG;
+  vocab_split(a->n_seq * a->n_rows, a->V, kPlanSms, chunks, elems);
+  *ws = verify_workspace_bytes(a->n_seq, a->n_rows, *chunks);
+  return BD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bd_attn_workspace_size(const bd_attn_args* a) {
+  if (!a) return 0;
+  AttnPlan pl;
+  return plan_attention(desc_of(a), &pl) == BD_OK ? pl.ws_bytes : 0;
+}
+
+size_t bd_fork_workspace_size(const bd_fork_args* a) {
+  if (!a) return 0;
+  AttnPlan pl;
+  return plan_attention(desc_of(a), &pl) == BD_OK ? pl.ws_bytes : 0;
+}
+
+bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream) {
+  if (!a || !a->q || !a->k || !a->v || !a->o) return BD_ERR_INVALID_ARG;
+  if (a->kv_stride < static_cast<long long>(a->C) + a->n_q) return BD_ERR_INVALID_ARG;
+  return run_attention(desc_of(a), static_cast<cudaStream_t>(stream));
+}
+
+bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream) {
+  if (!a || !a->q || !a->prefix_k || !a->prefix_v || !a->priv_k || !a->priv_v || !a->o) return BD_ERR_INVALID_ARG;
+  if (a->C > 0 && a->prefix_stride < a->C) return BD_ERR_INVALID_ARG;
+  if (a->priv_stride < static_cast<long long>(a->priv_len) + a->n_q) return BD_ERR_INVALID_ARG;
+  return run_attention(desc_of(a), static_cast<cudaStream_t>(stream));
+}
+
+size_t bd_unmask_workspace_size(const bd_unmask_args* a) {
+  int c, e;
+  size_t ws = 0;
+  return plan_unmask(a, &c, &e, &ws) == BD_OK ? ws : 0;
+}
+
+bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
+  int chunks, elems;
+  size_t ws;
+  bd_status st = plan_unmask(a, &chunks, &elems, &ws);
+  if (st != BD_OK) return st;
+  if (!a->logits || !a->logit_row || !a->block_start || !a->state || !a->tokens || !a->commit || !a->n_committed ||
+      !a->status)
+    return BD_ERR_INVALID_ARG;
+  if (!aligned(a->logits, 16)) return BD_ERR_UNSUPPORTED;
+  if (!a->workspace || a->workspace_bytes < ws || !aligned(a->workspace, 256)) return BD_ERR_WORKSPACE;
+  if ((st = check_device()) != BD_OK) return st;
+  UnmaskParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.logits = a->logits;
+  p.dtype = a->logits_dtype;
+  p.ld = a->logits_ld;
+  p.R = a->R;
+  p.V = a->V;
+  p.logit_row = a->logit_row;
+  p.n_pos = a->n_pos;
+  p.block_start = a->block_start;
+  p.n_blocks = a->n_blocks;
+  p.state = a->state;
+  p.tokens = a->tokens;
+  p.tau_full = a->tau_full;
+  p.tau_half = a->tau_half;
+  p.min_num = a->min_num;
+  p.min_den = a->min_den;
+  p.k_fixed = a->k_fixed;
+  p.add_num = a->add_num;
+  p.add_den = a->add_den;
+  p.act_num = a->act_num;
+  p.act_den = a->act_den;
+  p.commit = a->commit;
+  p.n_committed = a->n_committed;
+  p.status = a->status;
+  p.pred = a->pred;
+  p.conf = a->conf;
+  p.lse = a->lse;
+  p.dev_status = a->dev_status;
+  char* w = static_cast<char*>(a->workspace);
+  p.chunk_part = reinterpret_cast<float4*>(w);
+  w += align256(sizeof(float4) * static_cast<size_t>(a->n_pos) * chunks);
+  p.row_result = reinterpret_cast<float4*>(w);
+  w += align256(sizeof(float4) * a->n_pos);
+  p.row_ticket = reinterpret_cast<unsigned*>(w);
+  w += align256(sizeof(unsigned) * a->n_pos);
+  p.grid_ticket = reinterpret_cast<unsigned*>(w);
+  p.chunks = chunks;
+  p.chunk_elems = elems;
+  return launch_unmask(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+size_t bd_verify_workspace_size(const bd_verify_args* a) {
+  int c, e;
+  size_t ws = 0;
+  return plan_verify(a, &c, &e, &ws) == BD_OK ? ws : 0;
+}
+
+bd_status bd_spec_verify(const bd_verify_args* a, void* stream) {
+  int chunks, elems;
+  size_t ws;
+  bd_status st = plan_verify(a, &chunks, &elems, &ws);
+  if (st != BD_OK) return st;
+  if (!a->tokens || !a->state || !a->ar_logits || !a->accepted_len || !a->bonus || !a->bonus_pos)
+    return BD_ERR_INVALID_ARG;
+  if (!aligned(a->ar_logits, 16) || (a->noise && !aligned(a->noise, 16))) return BD_ERR_UNSUPPORTED;
+  if (!a->workspace || a->workspace_bytes < ws || !aligned(a->workspace, 256)) return BD_ERR_WORKSPACE;
+  if ((st = check_device()) != BD_OK) return st;
+  VerifyParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_seq = a->n_seq;
+  p.L = a->L;
+  p.tokens = a->tokens;
+  p.state = a->state;
+  p.logits = a->ar_logits;
+  p.dtype = a->logits_dtype;
+  p.ld = a->logits_ld;
+  p.n_rows = a->n_rows;
+  p.V = a->V;
+  p.noise = a->noise;
+  p.inv_temp = a->noise ? 1.0f / a->temperature : 1.0f;
+  p.accepted_len = a->accepted_len;
+  p.bonus = a->bonus;
+  p.bonus_pos = a->bonus_pos;
+  p.dev_status = a->dev_status;
+  const size_t rows = static_cast<size_t>(a->n_seq) * a->n_rows;
+  char* w = static_cast<char*>(a->workspace);
+  p.chunk_part = reinterpret_cast<float4*>(w);
+  w += align256(sizeof(float4) * rows * chunks);
+  p.row_argmax = reinterpret_cast<int32_t*>(w);
+  w += align256(sizeof(int32_t) * rows);
+  p.row_ticket = reinterpret_cast<unsigned*>(w);
+  w += align256(sizeof(unsigned) * rows);
+  p.seq_ticket = reinterpret_cast<unsigned*>(w);
+  p.chunks = chunks;
+  p.chunk_elems = elems;
+  return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+const char* bd_status_string(bd_status s) {
+  switch (s) {
+    case BD_OK: return "ok";
+    case BD_ERR_INVALID_ARG: return "invalid argument";
+    case BD_ERR_UNSUPPORTED: return "unsupported shape, alignment or device";
+    case BD_ERR_WORKSPACE: return "workspace missing or too small";
+    case BD_ERR_CUDA: return "CUDA call failed";
+    case BD_ERR_TIMEOUT: return "a device-side bounded wait expired";
+    case BD_ERR_DEVICE_INPUT: return "the device found an inconsistent input";
+  }
+  return "unknown status";
+}
+
+bd_status bd_check(const int32_t* dev_status, void* stream) {
+  if (!dev_status) return BD_ERR_INVALID_ARG;
+  int32_t h = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BD_ERR_CUDA;
+  if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return BD_ERR_CUDA;
+  if (h & BD_DEV_TIMEOUT) return BD_ERR_TIMEOUT;
+  if (h & BD_DEV_BAD_INPUT) return BD_ERR_DEVICE_INPUT;
+  return BD_OK;
+}
+
+const char* bd_version(void) { return "0.1.0"; }
+
+}  // extern "C"

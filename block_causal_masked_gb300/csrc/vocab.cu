@@ -1,0 +1,434 @@
+// vocab.cu -- vocabulary-wide reductions of the decode step on sm_103a:
+//   unmask_kernel  argmax / max-softmax-probability / LSE of every masked
+//                  position's logits row, then the per-block commit rule;
+//   verify_kernel  argmax (greedy or Gumbel-max) of every AR row, then the
+//                  left-to-right speculative match of each sequence.
+//
+// Both are HBM streams: a grid of (chunk, row) CTAs reads each row once with
+// 16-byte loads, keeps a running (max, first argmax, Σexp) per thread and
+// merges it with warp shuffles.  The last CTA to finish a row (atomic ticket,
+// no spinning) merges the row's chunk partials; the last row to finish runs the
+// small per-block / per-sequence decision in the same launch.  Counters are
+// returned to zero, so the workspace needs clearing only once.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace bd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxPos = 2048;     // positions of one unmask window
+constexpr int kMaxBlock = 1024;   // positions of one block
+constexpr int kMaxVerifyL = 1024; // slots of one verified block
+
+// Running (max, sum of exp(x - max), first index of max).
+struct Acc {
+  float m;
+  float s;
+  int idx;
+};
+
+__device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
+  if (b.m == -INFINITY) return;
+  if (a.m == -INFINITY) {
+    a = b;
+    return;
+  }
+  const float M = fmaxf(a.m, b.m);
+  const float s = a.s * exp2f((a.m - M) * kLog2e) + b.s * exp2f((b.m - M) * kLog2e);
+  a.idx = a.m > b.m ? a.idx : (b.m > a.m ? b.idx : min(a.idx, b.idx));
+  a.m = M;
+  a.s = s;
+}
+
+// Folds a vector of n values starting at index i0 into the accumulator.
+template <int N>
+__device__ __forceinline__ void acc_vec(Acc& a, const float (&x)[N], int i0, bool need_sum) {
+  float vm = x[0];
+  int vi = 0;
+#pragma unroll
+  for (int k = 1; k < N; ++k)
+    if (x[k] > vm) { vm = x[k]; vi = k; }
+  if (vm > a.m) {
+    if (need_sum) a.s = (a.m == -INFINITY) ? 0.f : a.s * exp2f((a.m - vm) * kLog2e);
+    a.m = vm;
+    a.idx = i0 + vi;
+  }
+  if (need_sum) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) a.s += exp2f((x[k] - a.m) * kLog2e);
+  }
+}
+
+__device__ __forceinline__ void load_vec8(const void* base, int dtype, long long off, float (&x)[8]) {
+  if (dtype == BD_BF16) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(ws[k] << 16);
+      x[2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
+    }
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    const float4 a = __ldg(f), b = __ldg(f + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ float load_one(const void* base, int dtype, long long off) {
+  if (dtype == BD_BF16) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + off);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  return __ldg(static_cast<const float*>(base) + off);
+}
+
+// Gumbel-perturbed score x / T - ln(-ln u); the inner logarithm is taken with
+// full precision because u close to 1 decides the largest perturbations.
+__device__ __forceinline__ float gumbel_score(float x, float u, float inv_temp) {
+  return fmaf(x, inv_temp, -__logf(-logf(u)));
+}
+
+// Block-wide merge of the per-thread accumulators; the result is valid in thread 0.
+__device__ Acc block_reduce(Acc a, Acc* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Acc b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    acc_merge(a, b);
+  }
+  if (lane == 0) sh[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) acc_merge(a, sh[w]);
+  }
+  return a;
+}
+
+// Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed scores).
+__device__ Acc reduce_chunk(const void* logits, int dtype, long long row_off, const float* noise, long long noise_off,
+                            float inv_temp, int lo, int hi, bool need_sum) {
+  Acc a{-INFINITY, 0.f, 0x7fffffff};
+  const int vlo = lo / 8, vhi = hi / 8;  // whole 8-element vectors (lo is a multiple of 8)
+  int v = vlo + threadIdx.x;
+  // four vectors in flight per thread
+  for (; v + 3 * kThreads < vhi; v += 4 * kThreads) {
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load_vec8(logits, dtype, row_off + 8ll * (v + u * kThreads), x[u]);
+    if (noise) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4* np4 = reinterpret_cast<const float4*>(noise + noise_off + 8ll * (v + u * kThreads));
+        const float4 n0 = __ldg(np4), n1 = __ldg(np4 + 1);
+        const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[u][k] = gumbel_score(x[u][k], nn[k], inv_temp);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc_vec<8>(a, x[u], 8 * (v + u * kThreads), need_sum);
+  }
+  for (; v < vhi; v += kThreads) {
+    float x[8];
+    load_vec8(logits, dtype, row_off + 8ll * v, x);
+    if (noise) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = gumbel_score(x[k], __ldg(noise + noise_off + 8ll * v + k), inv_temp);
+    }
+    acc_vec<8>(a, x, 8 * v, need_sum);
+  }
+  // ragged tail of the row (only when the row length is not a multiple of 8)
+  for (int i = vhi * 8 + threadIdx.x; i < hi; i += kThreads) {
+    float x[1] = {load_one(logits, dtype, row_off + i)};
+    if (noise) x[0] = gumbel_score(x[0], __ldg(noise + noise_off + i), inv_temp);
+    acc_vec<1>(a, x, i, need_sum);
+  }
+  return a;
+}
+
+// ======================================================================= unmask
+
+__device__ void unmask_select(const UnmaskParams& p) {
+  __shared__ uint8_t st0[kMaxPos];
+  __shared__ float conf_s[kMaxPos];
+  __shared__ int pred_s[kMaxPos];
+  __shared__ int cnt[4];
+  const int tid = threadIdx.x;
+  int ok_local = 1;
+  for (int b = tid; b < p.n_blocks; b += kThreads) {
+    const int lo = __ldg(p.block_start + b), hi = __ldg(p.block_start + b + 1);
+    ok_local &= lo < hi && hi - lo <= kMaxBlock;
+  }
+  if (tid == 0) ok_local &= __ldg(p.block_start) == 0 && __ldg(p.block_start + p.n_blocks) == p.n_pos;
+  for (int j = tid; j < p.n_pos; j += kThreads) {
+    st0[j] = p.state[j];
+    const float4 rr = __ldcg(p.row_result + j);
+    const int pr = __float_as_int(rr.z);
+    conf_s[j] = rr.x;
+    pred_s[j] = pr;
+    if (p.pred) p.pred[j] = pr;
+    if (p.conf) p.conf[j] = pr >= 0 ? rr.x : 0.f;
+    if (p.lse) p.lse[j] = pr >= 0 ? rr.y : 0.f;
+    p.commit[j] = 0;
+  }
+  if (!__syncthreads_and(ok_local)) {
+    if (tid == 0 && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
+    return;
+  }
+  for (int b = 0; b < p.n_blocks; ++b) {
+    const int lo = __ldg(p.block_start + b), hi = __ldg(p.block_start + b + 1);
+    if (tid < 4) cnt[tid] = 0;
+    __syncthreads();
+    int masked = 0, cand = 0, prev_done = 0;
+    for (int j = lo + tid; j < hi; j += kThreads) {
+      masked += st0[j] == BD_MASKED;
+      cand += pred_s[j] >= 0;
+    }
+    if (b > 0) {
+      const int plo = __ldg(p.block_start + b - 1);
+      for (int j = plo + tid; j < lo; j += kThreads) prev_done += st0[j] != BD_MASKED;
+    }
+    if (masked) atomicAdd(&cnt[0], masked);
+    if (cand) atomicAdd(&cnt[1], cand);
+    if (prev_done) atomicAdd(&cnt[2], prev_done);
+    __syncthreads();
+    int status;
+    if (cnt[0] == 0) {
+      status = BD_DONE;
+    } else if (b == 0) {
+      status = BD_FULL;
+    } else {
+      const long long psize = lo - __ldg(p.block_start + b - 1);
+      const long long done = cnt[2];
+      status = done * p.act_den >= static_cast<long long>(p.act_num) * psize   ? BD_FULL
+               : done * p.add_den >= static_cast<long long>(p.add_num) * psize ? BD_HALF
+                                                                               : BD_INACTIVE;
+    }
+    const int rem = cnt[1];
+    const int frac = static_cast<int>((static_cast<long long>(rem) * p.min_num + p.min_den - 1) / p.min_den);
+    const int n_min = min(rem, max(p.k_fixed, frac));
+    int ncom = 0;
+    if (status == BD_FULL || status == BD_HALF) {
+      for (int j = lo + tid; j < hi; j += kThreads) {
+        if (pred_s[j] < 0) continue;
+        const float c = conf_s[j];
+        bool take;
+        if (status == BD_HALF) {
+          take = c >= p.tau_half;
+        } else {
+          take = c >= p.tau_full;
+          if (!take) {
+            int rank = 0;
+            for (int k = lo; k < hi && rank < n_min; ++k)
+              if (pred_s[k] >= 0 && (conf_s[k] > c || (conf_s[k] == c && k < j))) ++rank;
+            take = rank < n_min;
+          }
+        }
+        if (take) {
+          p.commit[j] = 1;
+          p.tokens[j] = pred_s[j];
+          p.state[j] = BD_COMMITTED;
+          ++ncom;
+        }
+      }
+    }
+    if (ncom) atomicAdd(&cnt[3], ncom);
+    __syncthreads();
+    if (tid == 0) {
+      p.n_committed[b] = cnt[3];
+      p.status[b] = status;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
+  __shared__ Acc red[kThreads / 32];
+  __shared__ int last_row, last_grid;
+  const int pos = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const int row = __ldg(p.logit_row + pos);
+  const bool cand = p.state[pos] == BD_MASKED && row >= 0 && row < p.R;
+  if (cand) {
+    const int lo = chunk * p.chunk_elems;
+    const int hi = min(p.V, lo + p.chunk_elems);
+    Acc a{-INFINITY, 0.f, 0x7fffffff};
+    if (lo < hi) a = reduce_chunk(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
+    a = block_reduce(a, red);
+    if (threadIdx.x == 0) p.chunk_part[static_cast<size_t>(pos) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last_row = atomicAdd(p.row_ticket + pos, 1u) == static_cast<unsigned>(p.chunks - 1);
+  }
+  __syncthreads();
+  if (!last_row) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    float4 res = make_float4(0.f, 0.f, __int_as_float(-1), 0.f);
+    if (cand) {
+      Acc a{-INFINITY, 0.f, 0x7fffffff};
+      for (int c = 0; c < p.chunks; ++c) {
+        const float4 q = __ldcg(p.chunk_part + static_cast<size_t>(pos) * p.chunks + c);
+        acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
+      }
+      res = make_float4(1.f / a.s, a.m + logf(a.s), __int_as_float(a.idx), 1.f);
+    }
+    p.row_result[pos] = res;
+    p.row_ticket[pos] = 0u;
+    __threadfence();
+    last_grid = atomicAdd(p.grid_ticket, 1u) == static_cast<unsigned>(p.n_pos - 1);
+  }
+  __syncthreads();
+  if (!last_grid) return;
+  __threadfence();
+  unmask_select(p);
+  if (threadIdx.x == 0) *p.grid_ticket = 0u;
+}
+
+// ======================================================================= verify
+
+__device__ void verify_match(const VerifyParams& p, int s) {
+  __shared__ uint8_t st[kMaxVerifyL];
+  __shared__ int tok[kMaxVerifyL];
+  __shared__ int arg[kMaxVerifyL + 1];
+  const int L = p.L;
+  for (int j = threadIdx.x; j < L; j += kThreads) {
+    st[j] = p.state[static_cast<size_t>(s) * L + j];
+    tok[j] = p.tokens[static_cast<size_t>(s) * L + j];
+  }
+  for (int e = threadIdx.x; e < p.n_rows; e += kThreads) arg[e] = __ldcg(p.row_argmax + static_cast<size_t>(s) * p.n_rows + e);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int e = 0, n_acc = 0, bonus = -1, bonus_pos = -1;
+    bool mismatch = false;
+    for (int j = 0; j < L; ++j) {
+      if (st[j] == BD_SCAFFOLD) continue;
+      if (st[j] == BD_MASKED) {
+        if (!mismatch) {
+          const int t = e < p.n_rows ? arg[e] : -1;
+          if (t == tok[j]) {
+            st[j] = BD_COMMITTED;
+            ++n_acc;
+          } else {
+            tok[j] = t;
+            st[j] = BD_COMMITTED;
+            bonus = t;
+            bonus_pos = j;
+            mismatch = true;
+          }
+        } else {
+          tok[j] = -1;
+        }
+      }
+      ++e;
+    }
+    if (e + 1 != p.n_rows && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
+    if (!mismatch) {
+      bonus = e < p.n_rows ? arg[e] : -1;
+      bonus_pos = L;
+    }
+    p.accepted_len[s] = n_acc + 1;
+    p.bonus[s] = bonus;
+    p.bonus_pos[s] = bonus_pos;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < L; j += kThreads) {
+    p.state[static_cast<size_t>(s) * L + j] = st[j];
+    p.tokens[static_cast<size_t>(s) * L + j] = tok[j];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
+  __shared__ Acc red[kThreads / 32];
+  __shared__ int last_row, last_seq;
+  const int row = blockIdx.y;  // sequence * n_rows + e
+  const int chunk = blockIdx.x;
+  const int s = row / p.n_rows;
+  const int lo = chunk * p.chunk_elems;
+  const int hi = min(p.V, lo + p.chunk_elems);
+  Acc a{-INFINITY, 0.f, 0x7fffffff};
+  if (lo < hi)
+    a = reduce_chunk(p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise, static_cast<long long>(row) * p.ld,
+                     p.inv_temp, lo, hi, false);
+  a = block_reduce(a, red);
+  if (threadIdx.x == 0) {
+    p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, 0.f, __int_as_float(a.idx), 0.f);
+    __threadfence();
+    last_row = atomicAdd(p.row_ticket + row, 1u) == static_cast<unsigned>(p.chunks - 1);
+  }
+  __syncthreads();
+  if (!last_row) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    Acc m{-INFINITY, 0.f, 0x7fffffff};
+    for (int c = 0; c < p.chunks; ++c) {
+      const float4 q = __ldcg(p.chunk_part + static_cast<size_t>(row) * p.chunks + c);
+      const Acc b{q.x, 0.f, __float_as_int(q.z)};
+      if (b.m > m.m || (b.m == m.m && b.idx < m.idx)) m = b;
+    }
+    p.row_argmax[row] = m.idx == 0x7fffffff ? -1 : m.idx;
+    p.row_ticket[row] = 0u;
+    __threadfence();
+    last_seq = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.n_rows - 1);
+  }
+  __syncthreads();
+  if (!last_seq) return;
+  __threadfence();
+  verify_match(p, s);
+  if (threadIdx.x == 0) p.seq_ticket[s] = 0u;
+}
+
+}  // namespace
+
+void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems) {
+  // about two CTAs per SM over the whole grid, chunks of at least 2048 elements
+  const int target = 2 * num_sms;
+  int c = (target + rows - 1) / rows;
+  const int max_c = (V + 2047) / 2048;
+  if (c > max_c) c = max_c;
+  if (c < 1) c = 1;
+  int e = (V + c - 1) / c;
+  e = (e + 7) / 8 * 8;
+  c = (V + e - 1) / e;
+  *chunks = c;
+  *chunk_elems = e;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t unmask_workspace_bytes(int n_pos, int chunks) {
+  return align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks) + align256(sizeof(float4) * n_pos) +
+         align256(sizeof(unsigned) * n_pos) + 256;
+}
+
+size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
+  const size_t rows = static_cast<size_t>(n_seq) * n_rows;
+  return align256(sizeof(float4) * rows * chunks) + align256(sizeof(int32_t) * rows) +
+         align256(sizeof(unsigned) * rows) + align256(sizeof(unsigned) * n_seq);
+}
+
+cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
+  const dim3 grid(p.chunks, p.n_pos);
+  unmask_kernel<<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
+  const dim3 grid(p.chunks, p.n_seq * p.n_rows);
+  verify_kernel<<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bd
