@@ -1,0 +1,54 @@
+"""Shared helpers of the GPU parity tests: moving seeded inputs to the device and
+the tolerances the workload fixes.
+
+Attention: |o - o_ref| <= 1e-2 + 1e-2 |o_ref| element-wise, LSE within 1e-5
+relative.  Integer and index outputs: bit-exact.  Confidences: 2e-6 relative
+(fp32 accumulation over the vocabulary against float64); the commit decisions
+taken from them are exact because every input is drawn with decision margins
+that the tests assert (see the ``margins`` returned by the oracle).
+"""
+import numpy as np
+import torch
+
+DEV = "cuda:0"
+O_ATOL, O_RTOL = 1e-2, 1e-2
+LSE_RTOL = 1e-5
+CONF_RTOL = 2e-6
+
+
+def bf16(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV).to(torch.bfloat16)
+
+
+def f32(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+
+
+def i32(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(DEV)
+
+
+def u8(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).to(DEV)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def assert_attn_close(o, lse, o_ref, lse_ref, what=""):
+    o = host(o).astype(np.float64)
+    lse = host(lse).astype(np.float64)
+    err = np.abs(o - o_ref)
+    bound = O_ATOL + O_RTOL * np.abs(o_ref)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outputs off; worst {np.max(err - bound):.3g} over bound"
+    lerr = np.abs(lse - lse_ref)
+    lb = LSE_RTOL * np.abs(lse_ref) + 1e-6
+    assert not (lerr > lb).any(), f"{what}: lse off by up to {np.max(lerr / np.maximum(np.abs(lse_ref), 1e-30)):.3g} relative"
+
+
+def status_word() -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=DEV)

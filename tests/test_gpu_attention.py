@@ -1,0 +1,170 @@
+"""GPU parity of bd_block_causal_attn and bd_fork_rollouts against the float64
+oracle, through the C ABI, on seeded inputs spanning several K/V tiles, ragged
+tails, every block layout the method has (uniform, ragged, block size 1 = causal,
+one block = bidirectional), head dims 64/128, GQA ratios 1/2/8, KV splits, and
+in-kernel RoPE."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import block_causal_masked_gb300 as bd
+import oracle
+import synth
+from helpers import DEV, assert_attn_close, bf16, host, i32, status_word
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (name, C, block_start, Hq, Hkv, D, splits)
+    ("tiny_cfg", 256, [0, 8, 16], 4, 2, 64, 0),
+    ("no_prefix", 0, [0, 5, 9], 8, 8, 128, 0),
+    ("ragged_prefix_129", 129, [0, 3, 11, 12], 16, 2, 128, 1),
+    ("ragged_prefix_127", 127, [0, 20, 40], 16, 2, 128, 3),
+    ("causal_b1", 700, list(range(8)), 16, 8, 128, 0),
+    ("one_block", 390, [0, 33], 16, 2, 128, 2),
+    ("many_rows", 1000, [0, 33, 66, 92], 16, 2, 128, 0),     # 92 * 8 = 736 packed rows, 6 row tiles
+    ("single_key_prefix", 1, [0, 1, 2], 2, 1, 64, 0),
+    ("long_prefix", 3092, [0, 33], 16, 2, 128, 0),
+]
+
+
+def _run(case, splits, rope=None, block_start=True):
+    bs = torch.tensor(case.block_start, dtype=torch.int32, device=DEV) if block_start else None
+    ds = status_word()
+    o, lse = bd.bd_block_causal_attn(bf16(case.q), bf16(case.k), bf16(case.v), case.C, block_start=bs,
+                                     block_size=0 if block_start else 1, num_splits=splits, rope=rope,
+                                     dev_status=ds)
+    assert bd.bd_check(ds) == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("name,C,bs,Hq,Hkv,D,splits", CASES, ids=[c[0] for c in CASES])
+def test_attention_matches_oracle(name, C, bs, Hq, Hkv, D, splits):
+    case = synth.attn_case(10, zlib.crc32(name.encode()) % 1000, C=C, block_start=bs, Hq=Hq, Hkv=Hkv, D=D, kv_pad=5,
+                           text_from=max(0, C - 40))
+    o, lse = _run(case, splits)
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, C, bs)
+    assert_attn_close(o, lse, o_ref, lse_ref, name)
+
+
+def test_uniform_blocks_without_partition_array():
+    """block_start = NULL with a block size: the last block ragged (n_q = 13, B = 4)."""
+    case = synth.attn_case(11, 0, C=200, block_start=[0, 4, 8, 12, 13], Hq=8, Hkv=2, D=128)
+    ds = status_word()
+    o, lse = bd.bd_block_causal_attn(bf16(case.q), bf16(case.k), bf16(case.v), case.C, block_size=4, dev_status=ds)
+    assert bd.bd_check(ds) == 0
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, case.C, [0, 4, 8, 12, 13])
+    assert_attn_close(o, lse, o_ref, lse_ref)
+
+
+def test_split_count_does_not_change_the_result():
+    case = synth.attn_case(12, 0, C=2000, block_start=[0, 16, 33], Hq=16, Hkv=2, D=128)
+    res = [_run(case, s) for s in (1, 2, 7, 16)]
+    for o, lse in res[1:]:
+        assert np.allclose(host(lse), host(res[0][1]), rtol=1e-6, atol=1e-6)
+        assert np.allclose(host(o), host(res[0][0]), rtol=8e-3, atol=1e-4)  # one bf16 rounding apart
+
+
+def test_later_blocks_do_not_leak_on_gpu():
+    """Perturbing the last block's queries, keys and values leaves the earlier
+    blocks' outputs bitwise unchanged on the GPU as well."""
+    bs = [0, 7, 14, 21]
+    case = synth.attn_case(13, 0, C=600, block_start=bs, Hq=16, Hkv=2, D=128)
+    o1, l1 = _run(case, 1)
+    case.q[14:] += 50.0
+    case.k[:, 600 + 14:] -= 50.0
+    case.v[:, 600 + 14:] += 50.0
+    o2, l2 = _run(case, 1)
+    assert torch.equal(o1[:14], o2[:14]) and torch.equal(l1[:, :14], l2[:, :14])
+    assert not torch.equal(o1[14:], o2[14:])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_in_kernel_rope_matches_oracle(D):
+    C = 600
+    case = synth.attn_case(14, D, C=C, block_start=[0, 12, 20], Hq=16, Hkv=2, D=D)
+    k_pos = (np.arange(C) * 3 + 256).astype(np.int32)
+    rope = dict(k_pos=i32(k_pos), delta=256, theta=10000.0)
+    o, lse = _run(case, 0, rope=rope)
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, C, case.block_start, k_pos=k_pos,
+                                                   delta=256, theta=10000.0, rope=True)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"rope D={D}")
+
+
+def test_in_kernel_rope_equals_prerotated_keys():
+    """RoPE inside the operator gives the no-RoPE result on keys rotated
+    beforehand (rotated in float64 and rounded to bf16 on the host)."""
+    C = 4096 + 210
+    case = synth.attn_case(15, 0, C=C, block_start=[0, 39], Hq=16, Hkv=2, D=128)
+    k_pos = synth.streaming_prefix_positions()
+    o, lse = _run(case, 0, rope=dict(k_pos=i32(k_pos), delta=256, theta=1e4))
+    k2 = case.k.copy()
+    k2[:, :C] = oracle.round_bf16(oracle.rope_rotate(case.k[:, :C], k_pos.astype(np.int64) - 256, 1e4))
+    case2 = synth.AttnCase(case.q, k2, case.v, C, case.block_start)
+    o2, lse2 = _run(case2, 0)
+    assert np.allclose(host(lse), host(lse2), rtol=2e-6, atol=1e-6)
+    assert np.allclose(host(o), host(o2), rtol=1e-2, atol=1e-2)
+
+
+# ---------------------------------------------------------------------------------------- fork
+
+def _fork(seed, N, C, n_q, priv_len, bs, D=128, rope=False):
+    k_pos = synth.streaming_prefix_positions(sections=C - 4096) if rope and C > 4096 else None
+    if rope and k_pos is None:
+        k_pos = (np.arange(C) + 256).astype(np.int32)
+    return synth.fork_case(seed, 0, N=N, C=C, n_q=n_q, priv_len=priv_len, block_start=bs, Hq=16, Hkv=2, D=D,
+                           k_pos=k_pos, delta=256 if rope else 0, theta=1e4)
+
+
+def _run_fork(f, splits=0, rope=False):
+    ds = status_word()
+    r = dict(k_pos=i32(f.k_pos), delta=f.delta, theta=f.theta) if rope else None
+    o, lse = bd.bd_fork_rollouts(bf16(f.q), bf16(f.prefix_k), bf16(f.prefix_v), bf16(f.priv_k), bf16(f.priv_v),
+                                 f.priv_len, f.C, block_start=i32(f.block_start), num_splits=splits, rope=r,
+                                 dev_status=ds)
+    assert bd.bd_check(ds) == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("N,C,n_q,priv_len,bs,splits", [
+    (1, 300, 12, 0, [0, 12], 0),
+    (3, 500, 39, 41, [0, 39], 0),
+    (8, 1000, 12, 78, [0, 12], 2),
+    (5, 129, 20, 130, [0, 10, 20], 1),
+])
+def test_fork_matches_oracle(N, C, n_q, priv_len, bs, splits):
+    f = _fork(20 + N, N, C, n_q, priv_len, bs)
+    o, lse = _run_fork(f, splits)
+    o_ref, lse_ref = oracle.fork_attention(f.q, f.prefix_k, f.prefix_v, f.priv_k, f.priv_v, priv_len, bs)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"fork N={N}")
+
+
+def test_fork_single_rollout_equals_plain_attention():
+    f = _fork(30, 1, 700, 33, 40, [0, 33])
+    o, lse = _run_fork(f)
+    k = np.concatenate([f.prefix_k, f.priv_k[0]], axis=1)
+    v = np.concatenate([f.prefix_v, f.priv_v[0]], axis=1)
+    case = synth.AttnCase(f.q[0], k, v, 700 + 40, f.block_start)
+    o2, lse2 = _run(case, 0)
+    assert np.allclose(host(o[0]), host(o2), rtol=8e-3, atol=1e-4)
+    assert np.allclose(host(lse[0]), host(lse2), rtol=1e-6, atol=1e-6)
+
+
+def test_fork_reads_the_prefix_without_writing_it():
+    f = _fork(31, 4, 800, 12, 39, [0, 12])
+    pk, pv = bf16(f.prefix_k), bf16(f.prefix_v)
+    pk0, pv0 = pk.clone(), pv.clone()
+    bd.bd_fork_rollouts(bf16(f.q), pk, pv, bf16(f.priv_k), bf16(f.priv_v), f.priv_len, f.C,
+                        block_start=i32(f.block_start))
+    torch.cuda.synchronize()
+    assert torch.equal(pk, pk0) and torch.equal(pv, pv0)
+
+
+def test_fork_with_rope_matches_oracle():
+    f = _fork(32, 4, 4096 + 210, 39, 41, [0, 39], rope=True)
+    o, lse = _run_fork(f, rope=True)
+    o_ref, lse_ref = oracle.fork_attention(f.q, f.prefix_k, f.prefix_v, f.priv_k, f.priv_v, f.priv_len,
+                                           f.block_start, k_pos=f.k_pos, delta=f.delta, theta=f.theta, rope=True)
+    assert_attn_close(o, lse, o_ref, lse_ref, "fork rope")
