@@ -63,7 +63,7 @@ class bd_unmask_args(ct.Structure):
                 ("min_num", ct.c_int32), ("min_den", ct.c_int32), ("k_fixed", ct.c_int32),
                 ("add_num", ct.c_int32), ("add_den", ct.c_int32), ("act_num", ct.c_int32), ("act_den", ct.c_int32),
                 ("commit", ct.c_void_p), ("n_committed", ct.c_void_p), ("status", ct.c_void_p),
-                ("pred", ct.c_void_p), ("conf", ct.c_void_p), ("lse", ct.c_void_p),
+                ("pred", ct.c_void_p), ("conf", ct.c_void_p), ("lse", ct.c_void_p), ("write_draft", ct.c_int32),
                 ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
 
 
@@ -227,7 +227,8 @@ def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: in
 
 
 def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: float, tau_half: float,
-                   min_frac=(1, 4), k_fixed: int = 0, add_thr=(1, 2), act_thr=(17, 20), commit=None,
+                   min_frac=(1, 4), k_fixed: int = 0, add_thr=(1, 2), act_thr=(17, 20), write_draft=False,
+                   commit=None,
                    n_committed=None, status=None, pred=None, conf=None, lse=None, workspace=None,
                    dev_status=None, stream=None):
     """One unmask/commit step; updates ``state`` and ``tokens`` in place.
@@ -245,7 +246,7 @@ def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: f
     a = bd_unmask_args()
     a.logits = logits.data_ptr()
     a.logits_dtype = BD_BF16 if logits.dtype == torch.bfloat16 else BD_F32
-    a.logits_ld = logits.stride(0)
+    a.logits_ld = logits.stride(0) if R > 1 else (V + 7) // 8 * 8
     a.R, a.V = R, V
     a.logit_row, a.n_pos = logit_row.data_ptr(), n_pos
     a.block_start, a.n_blocks = block_start.data_ptr(), n_blocks
@@ -257,6 +258,7 @@ def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: f
     a.act_num, a.act_den = int(act_thr[0]), int(act_thr[1])
     a.commit, a.n_committed, a.status = commit.data_ptr(), n_committed.data_ptr(), status.data_ptr()
     a.pred, a.conf, a.lse = pred.data_ptr(), conf.data_ptr(), lse.data_ptr()
+    a.write_draft = 1 if write_draft else 0
     need = lib().bd_unmask_workspace_size(a)
     ws = workspace if workspace is not None else _WS["unmask"].get(need, dev)
     a.workspace = None if ws is None else ws.data_ptr()
@@ -277,15 +279,18 @@ def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.
     accepted_len = torch.empty(n_seq, dtype=torch.int32, device=dev) if accepted_len is None else accepted_len
     bonus = torch.empty(n_seq, dtype=torch.int32, device=dev) if bonus is None else bonus
     bonus_pos = torch.empty(n_seq, dtype=torch.int32, device=dev) if bonus_pos is None else bonus_pos
-    assert ar_logits.stride(0) == n_rows * ar_logits.stride(1)
-    if noise is not None:
-        assert noise.stride(1) == ar_logits.stride(1) and noise.stride(0) == ar_logits.stride(0)
+    ld = ar_logits.stride(1) if n_rows > 1 else (V + 7) // 8 * 8
+    if n_seq > 1 and ar_logits.stride(0) != n_rows * ld:
+        raise ValueError("ar_logits: sequences must follow each other at n_rows * row stride")
+    if noise is not None and ((n_rows > 1 and noise.stride(1) != ld) or
+                              (n_seq > 1 and noise.stride(0) != ar_logits.stride(0))):
+        raise ValueError("noise must have the layout of ar_logits")
     a = bd_verify_args()
     a.n_seq, a.L = n_seq, L
     a.tokens, a.state = tokens.data_ptr(), state.data_ptr()
     a.ar_logits = ar_logits.data_ptr()
     a.logits_dtype = BD_BF16 if ar_logits.dtype == torch.bfloat16 else BD_F32
-    a.logits_ld = ar_logits.stride(1)
+    a.logits_ld = ld
     a.n_rows, a.V = n_rows, V
     a.noise = None if noise is None else noise.data_ptr()
     a.temperature = float(temperature)

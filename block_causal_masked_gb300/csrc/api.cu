@@ -285,7 +285,7 @@ AttnDesc desc_of(const bd_fork_args* a) {
 bd_status plan_unmask(const bd_unmask_args* a, int* chunks, int* elems, size_t* ws) {
   if (!a) return BD_ERR_INVALID_ARG;
   if (a->R < 1 || a->V < 1 || a->n_pos < 1 || a->n_blocks < 1 || a->n_blocks > a->n_pos) return BD_ERR_INVALID_ARG;
-  if (a->n_pos > 2048) return BD_ERR_UNSUPPORTED;
+  if (a->n_pos > kMaxPos) return BD_ERR_UNSUPPORTED;
   if (a->logits_dtype != BD_F32 && a->logits_dtype != BD_BF16) return BD_ERR_INVALID_ARG;
   if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
   if (a->min_den < 1 || a->add_den < 1 || a->act_den < 1 || a->min_num < 0 || a->add_num < 0 || a->act_num < 0 ||
@@ -301,7 +301,8 @@ bd_status plan_verify(const bd_verify_args* a, int* chunks, int* elems, size_t* 
   if (!a) return BD_ERR_INVALID_ARG;
   if (a->n_seq < 1 || a->L < 1 || a->n_rows < 1 || a->n_rows > a->L + 1 || a->V < 1) return BD_ERR_INVALID_ARG;
   if (a->L > 1024) return BD_ERR_UNSUPPORTED;
-  if (static_cast<long long>(a->n_seq) * a->n_rows > 65535) return BD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->n_seq) * a->n_rows > kMaxVerifyRows || a->n_seq > kMaxVerifySeqs)
+    return BD_ERR_UNSUPPORTED;
   if (a->logits_dtype != BD_F32 && a->logits_dtype != BD_BF16) return BD_ERR_INVALID_ARG;
   if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
   if (a->noise && !(a->temperature > 0.f)) return BD_ERR_INVALID_ARG;
@@ -384,15 +385,15 @@ bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
   p.pred = a->pred;
   p.conf = a->conf;
   p.lse = a->lse;
+  p.write_draft = a->write_draft;
   p.dev_status = a->dev_status;
   char* w = static_cast<char*>(a->workspace);
+  p.grid_ticket = reinterpret_cast<unsigned*>(w);
+  p.row_ticket = reinterpret_cast<unsigned*>(w) + 1;
+  w += unmask_counter_bytes();
   p.chunk_part = reinterpret_cast<float4*>(w);
   w += align256(sizeof(float4) * static_cast<size_t>(a->n_pos) * chunks);
   p.row_result = reinterpret_cast<float4*>(w);
-  w += align256(sizeof(float4) * a->n_pos);
-  p.row_ticket = reinterpret_cast<unsigned*>(w);
-  w += align256(sizeof(unsigned) * a->n_pos);
-  p.grid_ticket = reinterpret_cast<unsigned*>(w);
   p.chunks = chunks;
   p.chunk_elems = elems;
   return launch_unmask(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
@@ -433,13 +434,12 @@ bd_status bd_spec_verify(const bd_verify_args* a, void* stream) {
   p.dev_status = a->dev_status;
   const size_t rows = static_cast<size_t>(a->n_seq) * a->n_rows;
   char* w = static_cast<char*>(a->workspace);
+  p.row_ticket = reinterpret_cast<unsigned*>(w);
+  p.seq_ticket = reinterpret_cast<unsigned*>(w + align256(sizeof(unsigned) * kMaxVerifyRows));
+  w += verify_counter_bytes();
   p.chunk_part = reinterpret_cast<float4*>(w);
   w += align256(sizeof(float4) * rows * chunks);
   p.row_argmax = reinterpret_cast<int32_t*>(w);
-  w += align256(sizeof(int32_t) * rows);
-  p.row_ticket = reinterpret_cast<unsigned*>(w);
-  w += align256(sizeof(unsigned) * rows);
-  p.seq_ticket = reinterpret_cast<unsigned*>(w);
   p.chunks = chunks;
   p.chunk_elems = elems;
   return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;

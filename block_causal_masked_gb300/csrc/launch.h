@@ -65,6 +65,7 @@ struct UnmaskParams {
   int32_t* pred;
   float* conf;
   float* lse;
+  int write_draft;
   int32_t* dev_status;
   // workspace carve-up
   float4* chunk_part;         // [n_pos, chunks]: (max, sum, argmax bits, -)
@@ -97,6 +98,12 @@ struct VerifyParams {
   int chunk_elems;
 };
 
+constexpr int kMaxPos = 2048;          // positions of one unmask window
+constexpr int kMaxVerifyRows = 16384;  // n_seq * n_rows of one verify call
+constexpr int kMaxVerifySeqs = 1024;   // sequences of one verify call
+
+size_t unmask_counter_bytes();
+size_t verify_counter_bytes();
 size_t unmask_workspace_bytes(int n_pos, int chunks);
 size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks);
 void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems);

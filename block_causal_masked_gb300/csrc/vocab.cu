@@ -22,7 +22,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxPos = 2048;     // positions of one unmask window
 constexpr int kMaxBlock = 1024;   // positions of one block
 constexpr int kMaxVerifyL = 1024; // slots of one verified block
 
@@ -240,8 +239,13 @@ __device__ void unmask_select(const UnmaskParams& p) {
           p.tokens[j] = pred_s[j];
           p.state[j] = BD_COMMITTED;
           ++ncom;
+        } else if (p.write_draft) {
+          p.tokens[j] = pred_s[j];
         }
       }
+    } else if (p.write_draft) {
+      for (int j = lo + tid; j < hi; j += kThreads)
+        if (pred_s[j] >= 0) p.tokens[j] = pred_s[j];
     }
     if (ncom) atomicAdd(&cnt[3], ncom);
     __syncthreads();
@@ -408,15 +412,22 @@ void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems) {
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Counter words sit in a fixed-size region at the start of the workspace, so a
+// buffer reused for calls of other shapes finds them where the previous call
+// left them: at zero.
+size_t unmask_counter_bytes() { return align256(sizeof(unsigned) * (kMaxPos + 1)); }
+size_t verify_counter_bytes() {
+  return align256(sizeof(unsigned) * kMaxVerifyRows) + align256(sizeof(unsigned) * kMaxVerifySeqs);
+}
+
 size_t unmask_workspace_bytes(int n_pos, int chunks) {
-  return align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks) + align256(sizeof(float4) * n_pos) +
-         align256(sizeof(unsigned) * n_pos) + 256;
+  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks) +
+         align256(sizeof(float4) * n_pos);
 }
 
 size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
   const size_t rows = static_cast<size_t>(n_seq) * n_rows;
-  return align256(sizeof(float4) * rows * chunks) + align256(sizeof(int32_t) * rows) +
-         align256(sizeof(unsigned) * rows) + align256(sizeof(unsigned) * n_seq);
+  return verify_counter_bytes() + align256(sizeof(float4) * rows * chunks) + align256(sizeof(int32_t) * rows);
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {

@@ -20,9 +20,10 @@
  *   and start on a 16-byte boundary.
  * - Workspace: calls that need scratch memory take a caller-owned device buffer
  *   of at least bd_*_workspace_size(args) bytes.  It must be zero-filled before
- *   its first use; every call that completes leaves its counter words at zero
- *   again, so the buffer can be reused by later calls on the same stream without
- *   clearing.  Calls that share a workspace must not overlap in time.
+ *   its first use; the counter words sit at fixed offsets at its start and every
+ *   call that completes leaves them at zero again, so the buffer can be reused
+ *   by later calls of any shape on the same stream without clearing.  Calls that
+ *   share a workspace must not overlap in time.
  * - Errors: argument errors are found on the host before anything is enqueued
  *   and returned as a bd_status; nothing is launched in that case.  Errors the
  *   device finds (a bounded wait that expired, an inconsistent block partition)
@@ -221,6 +222,10 @@ size_t bd_fork_workspace_size(const bd_fork_args* a);
  *   BD_HALF:  {conf >= tau_half};  BD_INACTIVE / BD_DONE: nothing.
  * A committed position gets tokens[p] = pred[p], state[p] = BD_COMMITTED,
  * commit[p] = 1.  Scaffold and committed positions never change.
+ * With write_draft != 0 every other candidate also gets tokens[p] = pred[p]
+ * while it stays BD_MASKED: the MDM draft of the scaffold-speculative round
+ * (method summary §3.2 mode 2, step 2: one MDM forward drafts every editable
+ * position), ready for bd_spec_verify.
  *
  *   logits        [R, V] of logits_dtype (BD_F32 | BD_BF16), row stride logits_ld
  *                 elements (multiple of 8)
@@ -230,7 +235,7 @@ size_t bd_fork_workspace_size(const bd_fork_args* a);
  *   commit        uint8 [n_pos] out;  n_committed, status int32 [n_blocks] out
  *   pred, conf, lse   int32/fp32/fp32 [n_pos] out, or NULL; non-candidates
  *                 get -1 / 0 / 0
- * Supported: n_pos <= 4096 and every block <= 1024 positions.
+ * Supported: n_pos <= 2048 and every block <= 1024 positions.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_unmask_args {
   const void* logits;
@@ -256,6 +261,7 @@ typedef struct bd_unmask_args {
   int32_t* pred;
   float* conf;
   float* lse;
+  int32_t write_draft;
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
@@ -292,7 +298,7 @@ size_t bd_unmask_workspace_size(const bd_unmask_args* a);
  *                 logits_ld, or NULL for greedy
  *   accepted_len  int32 [n_seq] out: slots committed this round, bonus included
  *   bonus, bonus_pos  int32 [n_seq] out
- * Supported: L <= 1024.
+ * Supported: L <= 1024, n_seq <= 1024, n_seq * n_rows <= 16384.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_verify_args {
   int32_t n_seq;

@@ -72,7 +72,7 @@ def block_status(state, block_start, add_thr: Fraction, act_thr: Fraction) -> li
 
 def unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: float,
                 tau_half: float, min_frac: Fraction, k_fixed: int, add_thr: Fraction,
-                act_thr: Fraction) -> dict:
+                act_thr: Fraction, write_draft: bool = False) -> dict:
     """One unmask/commit step over the active window.
 
     logits: [R, V]; logit_row[p]: row of position p or -1; state/tokens: [n_pos].
@@ -81,6 +81,10 @@ def unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: floa
     ``margins``: the smallest distances of this step's decisions from their
     thresholds (|conf - tau| over the candidates of half/full blocks, and the
     relative confidence gap at each full block's top-n_min cut).
+
+    With ``write_draft`` every candidate left masked also receives its argmax as
+    token: the MDM draft of a scaffold-speculative round (Fast-dDrive method
+    summary §3.2 "模式二", step 2: one MDM forward drafts all editable positions).
     """
     state = np.array(state, dtype=np.int64)
     tokens = np.array(tokens, dtype=np.int64)
@@ -118,6 +122,10 @@ def unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: floa
             tokens[p] = pred[p]
             state[p] = COMMITTED
         n_committed.append(len(chosen))
+        if write_draft:
+            for p in ps:
+                if p not in chosen:
+                    tokens[p] = pred[p]
     return dict(state=state, tokens=tokens, commit=commit, n_committed=np.array(n_committed),
                 status=np.array(status), pred=pred, conf=conf, lse=lse,
                 margins=dict(tau=tau_margin, rank=rank_margin))

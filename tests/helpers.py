@@ -17,19 +17,19 @@ CONF_RTOL = 2e-6
 
 
 def bf16(x) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV).to(torch.bfloat16)
+    return torch.from_numpy(np.array(x, dtype=np.float32, order='C', copy=True)).to(DEV).to(torch.bfloat16)
 
 
 def f32(x) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+    return torch.from_numpy(np.array(x, dtype=np.float32, order='C', copy=True)).to(DEV)
 
 
 def i32(x) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(DEV)
+    return torch.from_numpy(np.array(x, dtype=np.int32, order='C', copy=True)).to(DEV)
 
 
 def u8(x) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).to(DEV)
+    return torch.from_numpy(np.array(x, dtype=np.uint8, order='C', copy=True)).to(DEV)
 
 
 def host(t: torch.Tensor) -> np.ndarray:

@@ -300,3 +300,25 @@ def test_verify_sampled_rollouts(N):
     assert o["margins"]["gumbel"] >= 1e-3
     gg = _gpu_verify(drafts, state, ar, True, u, 1.0)
     _compare_verify(gg, o)
+
+
+def test_unmask_draft_mode_matches_oracle():
+    """Draft mode of the speculative round: tau = 0.9 commits, every other
+    editable position receives its argmax and stays masked."""
+    lay = synth.section_layout(1)
+    lo, hi = lay.block_start[2], lay.block_start[3]
+    scaf = lay.scaffold[lo:hi]
+    n = hi - lo
+    state = np.where(scaf == 1, synth.SCAFFOLD, synth.MASKED)
+    logit_row = np.full(n, -1)
+    logit_row[scaf == 0] = np.arange(int((scaf == 0).sum()))
+    kw = dict(tau_full=0.9, tau_half=0.9, min_frac=Fraction(0, 1), k_fixed=0, add_thr=Fraction(1, 2),
+              act_thr=Fraction(17, 20))
+    x = _conditioned_planted(7, int((scaf == 0).sum()), V, kw, state, logit_row, [0, n])
+    o = oracle.unmask_step(x, logit_row, [0, n], state, np.full(n, -1), write_draft=True, **kw)
+    st, tk = u8(state), i32(np.full(n, -1))
+    r = bd.bd_unmask_step(bf16(x), i32(logit_row), i32([0, n]), st, tk, tau_full=0.9, tau_half=0.9, min_frac=(0, 1),
+                          k_fixed=0, write_draft=True)
+    g = {k: host(v) for k, v in r.items()} | dict(state=host(st), tokens=host(tk))
+    _compare_unmask(g, o)
+    assert (g["state"] == synth.MASKED).any() and (g["tokens"][scaf == 0] >= 0).all()

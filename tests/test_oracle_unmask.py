@@ -197,3 +197,24 @@ def test_section_table_block_counts_and_scaffold_share():
         assert ed == d or last
     share = lay.scaffold.mean()
     assert abs(share - gold["scaffold_fraction_about"]) < 0.02
+
+
+def test_write_draft_fills_every_masked_candidate_with_its_argmax():
+    """Draft mode: committed positions as usual; every other masked position with
+    a row gets its argmax as token and stays masked; scaffold untouched."""
+    n = 12
+    logits = synth.normal_logits(17, 0, n, V=300, sigma=3.0, bf16=False)
+    state = np.zeros(n, int)
+    state[[2, 9]] = S
+    lr = np.arange(n)
+    lr[5] = -1
+    r = oracle.unmask_step(logits, lr, [0, 6, n], state, np.full(n, -1), tau_full=2.0, tau_half=2.0,
+                           min_frac=Fraction(1, 4), k_fixed=0, add_thr=Fraction(1, 2),
+                           act_thr=Fraction(17, 20), write_draft=True)
+    for p in range(n):
+        if state[p] == S or lr[p] < 0:
+            assert r["tokens"][p] == -1 and r["state"][p] == state[p]
+        else:
+            assert r["tokens"][p] == int(np.argmax(logits[p]))
+            assert r["state"][p] == (C_ if r["commit"][p] else M)
+    assert r["commit"].sum() >= 1 and (r["state"] == M).sum() >= 1
