@@ -226,7 +226,7 @@ class Clocks:
                  "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -246,7 +246,7 @@ class Clocks:
         sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 3 + i and "Active" in r[3 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 3 + i and r[3 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
 
@@ -332,12 +332,12 @@ def run_gpu(args, rank, world, local_rank):
     inp = make_inputs(W.seed + 100 * rank)
     rd = GpuRound(inp, device)
     rd.capture()
+    clocks = Clocks(local_rank)
     for _ in range(args.warmup):
         rd.timed_step()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = Clocks(local_rank)
     steps_ms, attn_ms, unmask_ms = [], [], []
     committed = 0
     for _ in range(args.steps):

@@ -23,7 +23,6 @@ using namespace bd;
 constexpr int kPlanSms = 152;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // ------------------------------------------------------------------ device checks
 
@@ -129,19 +128,16 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   if (max_tiles > kAttnMaxTiles) return BD_ERR_UNSUPPORTED;
   int splits = d.num_splits;
   if (splits == 0) {
-    // spread the KV range of every (row tile, KV head) over the SMs, keeping at
-    // least two tiles per split so that the ring stays busy
+    // spread the KV range of every (row tile, KV head) over the SMs as a cluster
+    // of up to 16 CTAs, at least one tile each
     const long long base = static_cast<long long>(pl->m_tiles) * d.Hkv;
     long long s = kPlanSms / base;
-    const long long by_tiles = max_tiles / 2;
-    if (s > by_tiles) s = by_tiles;
-    if (s > 32) s = 32;
+    if (s > max_tiles) s = max_tiles;
+    if (s > kAttnMaxSplits) s = kAttnMaxSplits;
     splits = s < 1 ? 1 : static_cast<int>(s);
   }
   pl->splits = splits;
-  const size_t total = static_cast<size_t>(rows) / G * d.Hq;  // N * n_q * Hq output rows
-  pl->ws_bytes = splits > 1 ? align256(sizeof(float) * splits * total * d.D) + align256(sizeof(float) * splits * total)
-                            : 0;
+  pl->ws_bytes = 0;  // splits are merged on chip, in the cluster
   return BD_OK;
 }
 
@@ -162,11 +158,6 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.q = d.q;
   p.o = d.o;
   p.lse = d.lse;
-  const size_t total = static_cast<size_t>(d.N) * d.n_q * d.Hq;
-  if (pl.splits > 1) {
-    p.part_o = static_cast<float*>(d.ws);
-    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(d.ws) + align256(sizeof(float) * pl.splits * total * d.D));
-  }
   p.block_start = d.block_start;
   p.k_pos = d.rope.enabled ? d.rope.k_pos : nullptr;
   p.dev_status = d.ds;
@@ -389,11 +380,7 @@ bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
   p.dev_status = a->dev_status;
   char* w = static_cast<char*>(a->workspace);
   p.grid_ticket = reinterpret_cast<unsigned*>(w);
-  p.row_ticket = reinterpret_cast<unsigned*>(w) + 1;
-  w += unmask_counter_bytes();
-  p.chunk_part = reinterpret_cast<float4*>(w);
-  w += align256(sizeof(float4) * static_cast<size_t>(a->n_pos) * chunks);
-  p.row_result = reinterpret_cast<float4*>(w);
+  p.chunk_part = reinterpret_cast<float4*>(w + unmask_counter_bytes());
   p.chunks = chunks;
   p.chunk_elems = elems;
   return launch_unmask(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
@@ -432,14 +419,9 @@ bd_status bd_spec_verify(const bd_verify_args* a, void* stream) {
   p.bonus = a->bonus;
   p.bonus_pos = a->bonus_pos;
   p.dev_status = a->dev_status;
-  const size_t rows = static_cast<size_t>(a->n_seq) * a->n_rows;
   char* w = static_cast<char*>(a->workspace);
-  p.row_ticket = reinterpret_cast<unsigned*>(w);
-  p.seq_ticket = reinterpret_cast<unsigned*>(w + align256(sizeof(unsigned) * kMaxVerifyRows));
-  w += verify_counter_bytes();
-  p.chunk_part = reinterpret_cast<float4*>(w);
-  w += align256(sizeof(float4) * rows * chunks);
-  p.row_argmax = reinterpret_cast<int32_t*>(w);
+  p.seq_ticket = reinterpret_cast<unsigned*>(w);
+  p.chunk_part = reinterpret_cast<float4*>(w + verify_counter_bytes());
   p.chunks = chunks;
   p.chunk_elems = elems;
   return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;

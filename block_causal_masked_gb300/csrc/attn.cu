@@ -22,9 +22,15 @@
 //   * with RoPE, warps 6-9 rotate each staged prefix K tile in shared memory at
 //     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
 //     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
-//   * KV splits write normalised fp32 partials and an LSE per row; a second
-//     kernel merges them with LSE weights.
-// Every wait is bounded (ptx.cuh); there is no wait on another CTA.
+//   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
+//     the end each CTA stages its rows' (max, sum) and scaled O in shared
+//     memory and the cluster merges them through distributed shared memory,
+//     each CTA reducing and storing a slice of the rows -- no partials in
+//     global memory and no second kernel.
+// Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
+// hardware cluster barriers, which every CTA of the cluster reaches on every
+// path.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -38,14 +44,15 @@ namespace {
 constexpr int BM = kAttnBM;
 constexpr int BN = kAttnBN;
 constexpr int kStages = 2;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
 
 struct TileEntry {
-  int32_t rollout;  // -1: shared prefix tile
-  int32_t key0;     // first key of the tile within its segment
+  int rollout;  // -1: shared prefix tile
+  int key0;     // first key of the tile within its segment
 };
+
+namespace cg = cooperative_groups;
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
@@ -62,9 +69,12 @@ struct Layout {
   static constexpr int kV = kK + kStages * kKVBytes;
   static constexpr int kP = kV + kStages * kKVBytes;
   static constexpr int kBar = kP + kPBytes;
-  static constexpr int kTiles = kBar + NUM_BARS * 8;
-  static constexpr int kMisc = kTiles + kAttnMaxTiles * 8;
-  static constexpr int kEnd = kMisc + 64;
+  static constexpr int kMisc = kBar + NUM_BARS * 8;
+  static constexpr int kML = kMisc + 64;       // [BM] (running max, sum) of each row, for the cluster merge
+  static constexpr int kLse = kML + BM * 8;    // [BM] merged LSE of each row
+  static constexpr int kEnd = kLse + BM * 4;
+  // the merge stages O (BM x D fp32) over the K stages, idle by then
+  static_assert(BM * D * 4 <= kStages * kKVBytes, "O staging must fit in the K ring");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
@@ -125,34 +135,124 @@ __device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long turns, 
   __sincosf(ang, &s, &c);
 }
 
-// Builds this CTA's list of K/V tiles (prefix tiles, then the private tiles of
-// every rollout its rows belong to, up to the furthest key any of them sees)
-// and keeps the contiguous share of split `split`.  Returns the count.
-__device__ int build_tiles(const AttnParams& p, int m0, int split, TileEntry* tiles) {
-  if (p.block_start != nullptr) {
-    bool ok = __ldg(p.block_start) == 0 && __ldg(p.block_start + p.n_blocks) == p.n_q;
-    for (int b = 0; ok && b < p.n_blocks; ++b) ok = __ldg(p.block_start + b) < __ldg(p.block_start + b + 1);
-    if (!ok) {
-      if (p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
-      return 0;
-    }
-  }
+// The K/V tiles of one CTA: the shared prefix tiles, then the private tiles of
+// every rollout its packed rows belong to.  Pure arithmetic, identical in every
+// thread; split `split` of `num_splits` takes a contiguous share of the list.
+struct TileRange {
+  int lo, hi;       // [lo, hi) in the CTA's list
+  int r_first;      // first rollout of the CTA's rows
+  int n_priv;       // private tiles per rollout
+};
+
+__device__ __forceinline__ TileRange tile_range(const AttnParams& p, int m0, int split) {
   const int per_roll = p.n_q * p.G;
   const int row_end = min(m0 + BM, p.rows_per_head);
-  const int r_first = m0 / per_roll;
+  TileRange tr;
+  tr.r_first = m0 / per_roll;
   const int r_last = (row_end - 1) / per_roll;
-  int total = 0;
-  for (int j = 0; j < p.n_prefix_tiles && total < kAttnMaxTiles; ++j) tiles[total++] = {-1, j * BN};
-  for (int r = r_first; r <= r_last; ++r) {
-    const int row_hi = min(row_end, (r + 1) * per_roll) - 1;
-    const int i_hi = (row_hi - r * per_roll) / p.G;
-    const int lim = p.priv_len + block_end_of(p, i_hi);
-    for (int k0 = 0; k0 < lim && total < kAttnMaxTiles; k0 += BN) tiles[total++] = {r, k0};
+  tr.n_priv = (p.priv_len + p.n_q + BN - 1) / BN;
+  const int total = p.n_prefix_tiles + (r_last - tr.r_first + 1) * tr.n_priv;
+  tr.lo = static_cast<int>(static_cast<long long>(split) * total / p.num_splits);
+  tr.hi = static_cast<int>(static_cast<long long>(split + 1) * total / p.num_splits);
+  return tr;
+}
+
+__device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRange& tr, int t) {
+  const int j = tr.lo + t;
+  if (j < p.n_prefix_tiles) return {-1, j * BN};
+  const int k = j - p.n_prefix_tiles;
+  return {tr.r_first + k / tr.n_priv, (k % tr.n_priv) * BN};
+}
+
+// Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
+// every thread of every CTA of the cluster; the softmax threads do the work:
+//   1. each row's (max, sum) of every split is read through distributed shared
+//      memory -> merged max M, sum L, and this split's weight 2^(m - M) / L;
+//   2. each CTA stages its weighted O rows (fp32) in its own shared memory;
+//   3. CTA `rank` sums a 1/S slice of the rows over the S CTAs and stores them.
+template <int D>
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
+                              float l_run) {
+  using L = Layout<D>;
+  constexpr int kChunks = D / 4;  // float4 chunks per staged row
+  cg::cluster_group cluster = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_sm = warp >= 2 && warp < 6;
+  const int quad = warp & 3;
+  const int rl = quad * 32 + lane;
+  const int S = p.num_splits;
+  float2* ml = reinterpret_cast<float2*>(smem + L::kML);
+  float* lse_s = reinterpret_cast<float*>(smem + L::kLse);
+  float* ost = reinterpret_cast<float*>(smem + L::kK);
+  cluster.sync();  // every split's (max, sum) is staged
+  if (is_sm) {
+    float M = -INFINITY;
+    for (int r = 0; r < S; ++r) {
+      const float2 x = *cluster.map_shared_rank(ml + rl, r);
+      if (x.y > 0.f) M = fmaxf(M, x.x);
+    }
+    float Ls = 0.f;
+    for (int r = 0; r < S; ++r) {
+      const float2 x = *cluster.map_shared_rank(ml + rl, r);
+      if (x.y > 0.f) Ls += x.y * exp2f(x.x - M);
+    }
+    const float w = (l_run > 0.f && Ls > 0.f) ? exp2f(m_run - M) / Ls : 0.f;
+    lse_s[rl] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    const bool warp_active = __any_sync(0xffffffffu, m0 + rl < p.rows_per_head);
+    if (warp_active) {
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      float v[32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        if (have_o) {
+          tmem_ld32(lane_base + 2 * BN + c * 32, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int pos = (c * 8 + q4) ^ (rl & (kChunks - 1));
+          *reinterpret_cast<float4*>(ost + rl * D + pos * 4) =
+              make_float4(v[4 * q4] * w, v[4 * q4 + 1] * w, v[4 * q4 + 2] * w, v[4 * q4 + 3] * w);
+        }
+      }
+    }
   }
-  const int lo = static_cast<int>(static_cast<long long>(split) * total / p.num_splits);
-  const int hi = static_cast<int>(static_cast<long long>(split + 1) * total / p.num_splits);
-  for (int t = lo; t < hi; ++t) tiles[t - lo] = tiles[t];
-  return hi - lo;
+  cluster.sync();  // every split's weighted O is staged
+  if (is_sm) {
+    const int t = threadIdx.x - 64;
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int rpc = (BM + S - 1) / S;
+    const int r0 = rank * rpc;
+    const int r1 = min(BM, r0 + rpc);
+    const int per_roll = p.n_q * p.G;
+    const int kvh = blockIdx.z;
+    for (int it = t; it < (r1 - r0) * kChunks; it += 128) {
+      const int row_l = r0 + it / kChunks;
+      const int ch = it % kChunks;
+      const int grow = m0 + row_l;
+      if (grow >= p.rows_per_head) continue;
+      const int pos = ch ^ (row_l & (kChunks - 1));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < S; ++r) {
+        const float4 x = *cluster.map_shared_rank(reinterpret_cast<float4*>(ost + row_l * D + pos * 4), r);
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      const int r_row = grow / per_roll;
+      const int rem = grow - r_row * per_roll;
+      const int i_row = rem / p.G;
+      const int qhead = kvh * p.G + (rem - i_row * p.G);
+      const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_s[row_l];
+    }
+  }
+  cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
 template <int D, bool ROPE>
@@ -162,8 +262,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  TileEntry* tiles = reinterpret_cast<TileEntry*>(smem + L::kTiles);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);  // [0] tmem base, [1] abort, [2] tiles
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);  // [0] tmem base, [1] abort
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -191,7 +290,6 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     mbar_init(&bars[KREADY + 1], 128);
     mbar_init(&bars[DRAIN], 1);
     misc[1] = 0;
-    misc[2] = static_cast<uint32_t>(build_tiles(p, m0, split, tiles));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -202,7 +300,12 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int nt = static_cast<int>(misc[2]);
+  const TileRange tr = tile_range(p, m0, split);
+  const int nt = tr.hi - tr.lo;
+  // softmax state of this thread's packed row (softmax warps), kept for the merge
+  float m_run = -INFINITY;  // running max, log2-scaled
+  float l_run = 0.f;
+  bool have_o = false;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -214,7 +317,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
       for (int t = 0; t < nt; ++t) {
         const int s = t & 1;
         if (t >= 2 && !mbar_wait(&bars[KVEMPTY + s], ((t >> 1) - 1) & 1, abort_flag, ds)) break;
-        const TileEntry te = tiles[t];
+        const TileEntry te = tile_at(p, tr, t);
         uint8_t* kdst = smem + L::kK + s * L::kKVBytes;
         uint8_t* vdst = smem + L::kV + s * L::kKVBytes;
         mbar_arrive_expect_tx(&bars[KFULL + s], L::kKVBytes);
@@ -319,8 +422,6 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     const int lim_priv = valid ? p.priv_len + block_end_of(p, i_row) : 0;
     const bool warp_active = __any_sync(0xffffffffu, valid);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    float m_run = -INFINITY;  // running max, log2-scaled
-    float l_run = 0.f;
     bool ok = true;
     float v[32];
     for (int t = 0; t < nt; ++t) {
@@ -328,7 +429,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
       ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds));
       if (!ok) break;
       tc_fence_after();
-      const TileEntry te = tiles[t];
+      const TileEntry te = tile_at(p, tr, t);
       int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
       if (!valid) lim = 0;
       const int nv = max(0, min(BN, lim - te.key0));
@@ -392,20 +493,19 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
       ok = all_lanes(mbar_wait(&bars[ODONE], (nt - 1) & 1, abort_flag, ds));
       tc_fence_after();
     }
-    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-    const size_t total_rows = static_cast<size_t>(p.N) * p.n_q * p.Hq;
-    if (warp_active) {
+    have_o = ok && nt > 0;
+    if (p.num_splits == 1) {
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      if (warp_active) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (ok && nt > 0) {
-          tmem_ld32(lane_base + 2 * BN + c * 32, v);
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          if (have_o) {
+            tmem_ld32(lane_base + 2 * BN + c * 32, v);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        if (!valid) continue;
-        if (p.num_splits == 1) {
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          }
+          if (!valid) continue;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c * 32);
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
@@ -413,21 +513,13 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
                                  pack_bf16x2(v[8 * qq + 2] * inv_l, v[8 * qq + 3] * inv_l),
                                  pack_bf16x2(v[8 * qq + 4] * inv_l, v[8 * qq + 5] * inv_l),
                                  pack_bf16x2(v[8 * qq + 6] * inv_l, v[8 * qq + 7] * inv_l));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + (split * total_rows + orow) * D + c * 32);
-#pragma unroll
-          for (int qq = 0; qq < 8; ++qq)
-            dst[qq] = make_float4(v[4 * qq] * inv_l, v[4 * qq + 1] * inv_l, v[4 * qq + 2] * inv_l,
-                                  v[4 * qq + 3] * inv_l);
         }
       }
-    }
-    if (valid) {
-      if (p.num_splits == 1) {
-        if (p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_v;
-      } else {
-        p.part_lse[split * total_rows + orow] = lse_v;
-      }
+      if (valid && p.lse)
+        p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    } else {
+      reinterpret_cast<float2*>(smem + L::kML)[rl] = make_float2(m_run, l_run);
     }
   } else if (ROPE) {
     // ---------------------------------------------------------------- RoPE on staged prefix keys
@@ -435,7 +527,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
       if (!mbar_wait(&bars[KFULL + s], (t >> 1) & 1, abort_flag, ds)) break;
-      const TileEntry te = tiles[t];
+      const TileEntry te = tile_at(p, tr, t);
       const int key = te.key0 + kr;
       if (te.rollout < 0 && key < p.C) {
         const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
@@ -466,6 +558,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     }
   }
 
+  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run);
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -474,70 +568,39 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   }
 }
 
-// Merges the KV splits of every output row: LSE = ln Σ_s exp(lse_s),
-// O = Σ_s exp(lse_s - LSE) O_s.  One warp per (rollout, position, query head).
-template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  const int total = p.N * p.n_q * p.Hq;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= total) return;
-  const int S = p.num_splits;
-  float mx = -INFINITY;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(s) * total + row]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  for (int s = lane; s < S; s += 32) {
-    const float l = p.part_lse[static_cast<size_t>(s) * total + row];
-    if (l > -INFINITY) sum += exp2f((l - mx) * kLog2e);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float LSE = mx + logf(sum);
-  constexpr int E = D / 32;  // elements per lane
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float l = p.part_lse[static_cast<size_t>(s) * total + row];
-    if (!(l > -INFINITY)) continue;
-    const float w = exp2f((l - LSE) * kLog2e);
-    const float* src = p.part_o + (static_cast<size_t>(s) * total + row) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 x = *reinterpret_cast<const float2*>(src + e);
-      acc[e] = fmaf(w, x.x, acc[e]);
-      acc[e + 1] = fmaf(w, x.y, acc[e + 1]);
-    }
-  }
-  uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.o) + static_cast<size_t>(row) * D +
-                                              lane * E);
-#pragma unroll
-  for (int e = 0; e < E; e += 2) dst[e / 2] = pack_bf16x2(acc[e], acc[e + 1]);
-  if (lane == 0 && p.lse) {
-    const int ri = row / p.Hq, qhead = row - ri * p.Hq;
-    const int r = ri / p.n_q, i = ri - r * p.n_q;
-    p.lse[(static_cast<size_t>(r) * p.Hq + qhead) * p.n_q + i] = LSE;
-  }
-}
-
 template <int D, bool ROPE>
-cudaError_t launch_attn_t(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
+cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
   static bool configured = false;
   const int smem = attn_smem_bytes(D);
+  auto kernel = attn_kernel<D, ROPE>;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid(p.num_splits, m_tiles, p.Hkv);
-  attn_kernel<D, ROPE><<<grid, ROPE ? 320 : 192, smem, stream>>>(p, maps);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.num_splits == 1) return e;
-  const int total = p.N * p.n_q * p.Hq;
-  attn_combine_kernel<D><<<(total + 7) / 8, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(ROPE ? 320 : 192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  for (;;) {
+    cfg.gridDim = dim3(p.num_splits, m_tiles, p.Hkv);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.num_splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.num_splits <= 8) break;
+    // a cluster wider than the portable 8 needs that many SMs free in one GPC
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) break;
+    (void)cudaGetLastError();
+    p.num_splits = 8;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p, maps);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace

@@ -12,8 +12,8 @@ namespace bd {
 
 constexpr int kAttnBM = 128;        // packed query rows per CTA (tcgen05 M)
 constexpr int kAttnBN = 128;        // keys per K/V tile
-constexpr int kAttnMaxTiles = 512;  // K/V tiles a CTA may list before its split
-constexpr int kAttnMaxSplits = 64;
+constexpr int kAttnMaxTiles = 4096; // K/V tiles of one (row tile, KV head) before splitting
+constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 
 // Everything the attention kernels need, in the fork's terms: plain attention is
 // the fork with N = 1, the prefix = rows [0, C) of K/V and the private rows =
@@ -22,8 +22,6 @@ struct AttnParams {
   const void* q;          // bf16 [N, n_q, Hq, D]
   void* o;                // bf16 [N, n_q, Hq, D]
   float* lse;             // fp32 [N, Hq, n_q] or null
-  float* part_o;          // fp32 [splits, N*n_q*Hq, D]       (splits > 1)
-  float* part_lse;        // fp32 [splits, N*n_q*Hq]          (splits > 1)
   const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
   const int32_t* k_pos;        // [C] or null
   int32_t* dev_status;
@@ -69,8 +67,6 @@ struct UnmaskParams {
   int32_t* dev_status;
   // workspace carve-up
   float4* chunk_part;         // [n_pos, chunks]: (max, sum, argmax bits, -)
-  float4* row_result;         // [n_pos]: (conf, lse, pred bits, candidate flag)
-  unsigned int* row_ticket;   // [n_pos]
   unsigned int* grid_ticket;  // [1]
   int chunks;                 // CTAs per logits row
   int chunk_elems;            // elements per chunk (multiple of 8)
@@ -90,16 +86,14 @@ struct VerifyParams {
   int32_t* bonus;
   int32_t* bonus_pos;
   int32_t* dev_status;
-  float4* chunk_part;         // [n_seq * n_rows, chunks]: (score, argmax bits, -, -)
-  int32_t* row_argmax;        // [n_seq * n_rows]
-  unsigned int* row_ticket;   // [n_seq * n_rows]
+  float4* chunk_part;         // [n_seq * n_rows, chunks]: (score, -, argmax bits, -)
   unsigned int* seq_ticket;   // [n_seq]
   int chunks;
   int chunk_elems;
 };
 
 constexpr int kMaxPos = 2048;          // positions of one unmask window
-constexpr int kMaxVerifyRows = 16384;  // n_seq * n_rows of one verify call
+constexpr int kMaxVerifyRows = 65535;  // n_seq * n_rows of one verify call (grid y)
 constexpr int kMaxVerifySeqs = 1024;   // sequences of one verify call
 
 size_t unmask_counter_bytes();

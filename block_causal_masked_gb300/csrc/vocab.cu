@@ -114,6 +114,26 @@ __device__ Acc block_reduce(Acc a, Acc* sh) {
   return a;
 }
 
+// Merges the chunk partials of one row with one warp: lane c folds chunks
+// c, c + 32, ... and the lanes are combined with shuffles.  Valid in every lane.
+__device__ Acc warp_merge_row(const float4* part, int chunks) {
+  const int lane = threadIdx.x & 31;
+  Acc a{-INFINITY, 0.f, 0x7fffffff};
+  for (int c = lane; c < chunks; c += 32) {
+    const float4 q = __ldcg(part + c);
+    acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Acc b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    acc_merge(a, b);
+  }
+  return a;
+}
+
 // Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed scores).
 __device__ Acc reduce_chunk(const void* logits, int dtype, long long row_off, const float* noise, long long noise_off,
                             float inv_temp, int lo, int hi, bool need_sum) {
@@ -170,16 +190,29 @@ __device__ void unmask_select(const UnmaskParams& p) {
     ok_local &= lo < hi && hi - lo <= kMaxBlock;
   }
   if (tid == 0) ok_local &= __ldg(p.block_start) == 0 && __ldg(p.block_start + p.n_blocks) == p.n_pos;
-  for (int j = tid; j < p.n_pos; j += kThreads) {
-    st0[j] = p.state[j];
-    const float4 rr = __ldcg(p.row_result + j);
-    const int pr = __float_as_int(rr.z);
-    conf_s[j] = rr.x;
-    pred_s[j] = pr;
-    if (p.pred) p.pred[j] = pr;
-    if (p.conf) p.conf[j] = pr >= 0 ? rr.x : 0.f;
-    if (p.lse) p.lse[j] = pr >= 0 ? rr.y : 0.f;
-    p.commit[j] = 0;
+  // one warp per position: merge its row's chunk partials
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int j = warp; j < p.n_pos; j += kThreads / 32) {
+    const int row = __ldg(p.logit_row + j);
+    const uint8_t st = p.state[j];
+    const bool cand = st == BD_MASKED && row >= 0 && row < p.R;
+    float conf = 0.f, lse = 0.f;
+    int pred = -1;
+    if (cand) {
+      const Acc a = warp_merge_row(p.chunk_part + static_cast<size_t>(j) * p.chunks, p.chunks);
+      conf = 1.f / a.s;
+      lse = a.m + logf(a.s);
+      pred = a.idx;
+    }
+    if (lane == 0) {
+      st0[j] = st;
+      conf_s[j] = conf;
+      pred_s[j] = pred;
+      if (p.pred) p.pred[j] = pred;
+      if (p.conf) p.conf[j] = conf;
+      if (p.lse) p.lse[j] = lse;
+      p.commit[j] = 0;
+    }
   }
   if (!__syncthreads_and(ok_local)) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
@@ -259,7 +292,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
 
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
   __shared__ Acc red[kThreads / 32];
-  __shared__ int last_row, last_grid;
+  __shared__ int last;
   const int pos = blockIdx.y;
   const int chunk = blockIdx.x;
   const int row = __ldg(p.logit_row + pos);
@@ -270,32 +303,15 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
     Acc a{-INFINITY, 0.f, 0x7fffffff};
     if (lo < hi) a = reduce_chunk(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
     a = block_reduce(a, red);
-    if (threadIdx.x == 0) p.chunk_part[static_cast<size_t>(pos) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
+    if (threadIdx.x == 0)
+      p.chunk_part[static_cast<size_t>(pos) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
   }
   if (threadIdx.x == 0) {
     __threadfence();
-    last_row = atomicAdd(p.row_ticket + pos, 1u) == static_cast<unsigned>(p.chunks - 1);
+    last = atomicAdd(p.grid_ticket, 1u) == gridDim.x * gridDim.y - 1;
   }
   __syncthreads();
-  if (!last_row) return;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    float4 res = make_float4(0.f, 0.f, __int_as_float(-1), 0.f);
-    if (cand) {
-      Acc a{-INFINITY, 0.f, 0x7fffffff};
-      for (int c = 0; c < p.chunks; ++c) {
-        const float4 q = __ldcg(p.chunk_part + static_cast<size_t>(pos) * p.chunks + c);
-        acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
-      }
-      res = make_float4(1.f / a.s, a.m + logf(a.s), __int_as_float(a.idx), 1.f);
-    }
-    p.row_result[pos] = res;
-    p.row_ticket[pos] = 0u;
-    __threadfence();
-    last_grid = atomicAdd(p.grid_ticket, 1u) == static_cast<unsigned>(p.n_pos - 1);
-  }
-  __syncthreads();
-  if (!last_grid) return;
+  if (!last) return;
   __threadfence();
   unmask_select(p);
   if (threadIdx.x == 0) *p.grid_ticket = 0u;
@@ -312,7 +328,11 @@ __device__ void verify_match(const VerifyParams& p, int s) {
     st[j] = p.state[static_cast<size_t>(s) * L + j];
     tok[j] = p.tokens[static_cast<size_t>(s) * L + j];
   }
-  for (int e = threadIdx.x; e < p.n_rows; e += kThreads) arg[e] = __ldcg(p.row_argmax + static_cast<size_t>(s) * p.n_rows + e);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < p.n_rows; e += kThreads / 32) {
+    const Acc a = warp_merge_row(p.chunk_part + (static_cast<size_t>(s) * p.n_rows + e) * p.chunks, p.chunks);
+    if (lane == 0) arg[e] = a.idx == 0x7fffffff ? -1 : a.idx;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     int e = 0, n_acc = 0, bonus = -1, bonus_pos = -1;
@@ -356,7 +376,7 @@ __device__ void verify_match(const VerifyParams& p, int s) {
 
 __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
   __shared__ Acc red[kThreads / 32];
-  __shared__ int last_row, last_seq;
+  __shared__ int last;
   const int row = blockIdx.y;  // sequence * n_rows + e
   const int chunk = blockIdx.x;
   const int s = row / p.n_rows;
@@ -370,25 +390,10 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, 0.f, __int_as_float(a.idx), 0.f);
     __threadfence();
-    last_row = atomicAdd(p.row_ticket + row, 1u) == static_cast<unsigned>(p.chunks - 1);
+    last = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.chunks * p.n_rows - 1);
   }
   __syncthreads();
-  if (!last_row) return;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    Acc m{-INFINITY, 0.f, 0x7fffffff};
-    for (int c = 0; c < p.chunks; ++c) {
-      const float4 q = __ldcg(p.chunk_part + static_cast<size_t>(row) * p.chunks + c);
-      const Acc b{q.x, 0.f, __float_as_int(q.z)};
-      if (b.m > m.m || (b.m == m.m && b.idx < m.idx)) m = b;
-    }
-    p.row_argmax[row] = m.idx == 0x7fffffff ? -1 : m.idx;
-    p.row_ticket[row] = 0u;
-    __threadfence();
-    last_seq = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.n_rows - 1);
-  }
-  __syncthreads();
-  if (!last_seq) return;
+  if (!last) return;
   __threadfence();
   verify_match(p, s);
   if (threadIdx.x == 0) p.seq_ticket[s] = 0u;
@@ -415,19 +420,15 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // Counter words sit in a fixed-size region at the start of the workspace, so a
 // buffer reused for calls of other shapes finds them where the previous call
 // left them: at zero.
-size_t unmask_counter_bytes() { return align256(sizeof(unsigned) * (kMaxPos + 1)); }
-size_t verify_counter_bytes() {
-  return align256(sizeof(unsigned) * kMaxVerifyRows) + align256(sizeof(unsigned) * kMaxVerifySeqs);
-}
+size_t unmask_counter_bytes() { return 256; }
+size_t verify_counter_bytes() { return align256(sizeof(unsigned) * kMaxVerifySeqs); }
 
 size_t unmask_workspace_bytes(int n_pos, int chunks) {
-  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks) +
-         align256(sizeof(float4) * n_pos);
+  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks);
 }
 
 size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
-  const size_t rows = static_cast<size_t>(n_seq) * n_rows;
-  return verify_counter_bytes() + align256(sizeof(float4) * rows * chunks) + align256(sizeof(int32_t) * rows);
+  return verify_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_seq) * n_rows * chunks);
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
