@@ -58,13 +58,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 K/V tensor map with a {64, 128, 1, ...} box and 128-byte swizzle.
-bd_status make_kv_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides) {
+// bf16 tensor map with 128-byte swizzle; the box is {64, 128, 1, ...} unless given.
+bd_status make_kv_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                      const uint32_t* box_in = nullptr) {
   auto fn = encode_fn();
   if (!fn) return BD_ERR_CUDA;
   cuuint64_t gdim[4];
   cuuint64_t gstr[3];
   cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kAttnBN), 1, 1};
+  if (box_in)
+    for (int i = 0; i < rank; ++i) box[i] = box_in[i];
   cuuint32_t estr[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
   for (int i = 0; i < rank - 1; ++i) gstr[i] = strides[i];
@@ -191,6 +194,15 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   AttnMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const uint64_t row_b = static_cast<uint64_t>(d.D) * 2;
+  p.q_tma = (kAttnBM % pl.G) == 0 ? 1 : 0;
+  if (p.q_tma) {
+    // packed rows (position, g) of KV head h are G consecutive heads of each position
+    const uint64_t dims[4] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(pl.G), static_cast<uint64_t>(d.Hkv),
+                              static_cast<uint64_t>(d.N) * d.n_q};
+    const uint64_t strides[3] = {row_b, row_b * pl.G, row_b * d.Hq};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(pl.G), 1, static_cast<uint32_t>(kAttnBM / pl.G)};
+    if ((st = make_kv_map(&maps.q, d.q, 4, dims, strides, box)) != BD_OK) return st;
+  }
   if (d.C > 0) {
     const uint64_t dims[3] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.C), static_cast<uint64_t>(d.Hkv)};
     const uint64_t strides[2] = {row_b, static_cast<uint64_t>(d.prefix_stride) * row_b};

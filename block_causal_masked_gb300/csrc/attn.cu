@@ -186,17 +186,19 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   float* ost = reinterpret_cast<float*>(smem + L::kK);
   cluster.sync();  // every split's (max, sum) is staged
   if (is_sm) {
+    float2 x[kAttnMaxSplits];
+#pragma unroll
+    for (int r = 0; r < kAttnMaxSplits; ++r)
+      if (r < S) x[r] = *cluster.map_shared_rank(ml + rl, r);  // all remote loads in flight at once
     float M = -INFINITY;
-    for (int r = 0; r < S; ++r) {
-      const float2 x = *cluster.map_shared_rank(ml + rl, r);
-      if (x.y > 0.f) M = fmaxf(M, x.x);
-    }
+#pragma unroll
+    for (int r = 0; r < kAttnMaxSplits; ++r)
+      if (r < S && x[r].y > 0.f) M = fmaxf(M, x[r].x);
     float Ls = 0.f;
-    for (int r = 0; r < S; ++r) {
-      const float2 x = *cluster.map_shared_rank(ml + rl, r);
-      if (x.y > 0.f) Ls += x.y * exp2f(x.x - M);
-    }
-    const float w = (l_run > 0.f && Ls > 0.f) ? exp2f(m_run - M) / Ls : 0.f;
+#pragma unroll
+    for (int r = 0; r < kAttnMaxSplits; ++r)
+      if (r < S && x[r].y > 0.f) Ls += x[r].y * fast_exp2(x[r].x - M);
+    const float w = (l_run > 0.f && Ls > 0.f) ? fast_exp2(m_run - M) / Ls : 0.f;
     lse_s[rl] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     const bool warp_active = __any_sync(0xffffffffu, m0 + rl < p.rows_per_head);
     if (warp_active) {
@@ -234,13 +236,20 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       const int grow = m0 + row_l;
       if (grow >= p.rows_per_head) continue;
       const int pos = ch ^ (row_l & (kChunks - 1));
+      float4 part[kAttnMaxSplits];
+      float4* src = reinterpret_cast<float4*>(ost + row_l * D + pos * 4);
+#pragma unroll
+      for (int r = 0; r < kAttnMaxSplits; ++r)
+        if (r < S) part[r] = *cluster.map_shared_rank(src, r);  // all remote loads in flight at once
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int r = 0; r < S; ++r) {
-        const float4 x = *cluster.map_shared_rank(reinterpret_cast<float4*>(ost + row_l * D + pos * 4), r);
-        acc.x += x.x;
-        acc.y += x.y;
-        acc.z += x.z;
-        acc.w += x.w;
+#pragma unroll
+      for (int r = 0; r < kAttnMaxSplits; ++r) {
+        if (r < S) {
+          acc.x += part[r].x;
+          acc.y += part[r].y;
+          acc.z += part[r].z;
+          acc.w += part[r].w;
+        }
       }
       const int r_row = grow / per_roll;
       const int rem = grow - r_row * per_roll;
@@ -272,6 +281,32 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const int kvh = blockIdx.z;
   int32_t* ds = p.dev_status;
 
+  const TileRange tr = tile_range(p, m0, split);
+  const int nt = tr.hi - tr.lo;
+  // TMA of K/V tile t into stage t % 2 (the caller has made sure the stage is free)
+  auto issue_kv = [&](int t) {
+    const int s = t & 1;
+    const TileEntry te = tile_at(p, tr, t);
+    uint8_t* kdst = smem + L::kK + s * L::kKVBytes;
+    uint8_t* vdst = smem + L::kV + s * L::kKVBytes;
+    mbar_arrive_expect_tx(&bars[KFULL + s], L::kKVBytes);
+#pragma unroll
+    for (int hh = 0; hh < D / 64; ++hh) {
+      if (te.rollout < 0)
+        tma_load_3d(kdst + hh * BN * 128, &maps.pk, hh * 64, te.key0, kvh, &bars[KFULL + s]);
+      else
+        tma_load_4d(kdst + hh * BN * 128, &maps.rk, hh * 64, te.key0, kvh, te.rollout, &bars[KFULL + s]);
+    }
+    mbar_arrive_expect_tx(&bars[VFULL + s], L::kKVBytes);
+#pragma unroll
+    for (int hh = 0; hh < D / 64; ++hh) {
+      if (te.rollout < 0)
+        tma_load_3d(vdst + hh * BN * 128, &maps.pv, hh * 64, te.key0, kvh, &bars[VFULL + s]);
+      else
+        tma_load_4d(vdst + hh * BN * 128, &maps.rv, hh * 64, te.key0, kvh, te.rollout, &bars[VFULL + s]);
+    }
+  };
+
   if (threadIdx.x == 0) {
     mbar_init(&bars[KFULL + 0], 1);
     mbar_init(&bars[KFULL + 1], 1);
@@ -285,12 +320,23 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     mbar_init(&bars[SFREE + 1], 128);
     mbar_init(&bars[PFULL], 128);
     mbar_init(&bars[ODONE], 1);
-    mbar_init(&bars[QFULL], 128);
+    mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
     mbar_init(&bars[KREADY + 0], 128);
     mbar_init(&bars[KREADY + 1], 128);
     mbar_init(&bars[DRAIN], 1);
     misc[1] = 0;
     fence_mbar_init();
+    // the first loads leave before the rest of the CTA is set up
+    if (nt > 0) {
+      if (p.q_tma) {
+        mbar_arrive_expect_tx(&bars[QFULL], L::kQBytes);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_4d(smem + L::kQ + hh * BM * 128, &maps.q, hh * 64, 0, kvh, m0 / p.G, &bars[QFULL]);
+      }
+      issue_kv(0);
+      if (nt > 1) issue_kv(1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&misc[0], L::kTmemCols);
@@ -300,8 +346,6 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const TileRange tr = tile_range(p, m0, split);
-  const int nt = tr.hi - tr.lo;
   // softmax state of this thread's packed row (softmax warps), kept for the merge
   float m_run = -INFINITY;  // running max, log2-scaled
   float l_run = 0.f;
@@ -310,34 +354,14 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
-      if (p.n_prefix_tiles > 0) { tma_prefetch_desc(&maps.pk); tma_prefetch_desc(&maps.pv); }
-      tma_prefetch_desc(&maps.rk);
-      tma_prefetch_desc(&maps.rv);
-      int last[2] = {-1, -1};
-      for (int t = 0; t < nt; ++t) {
+      int last[2] = {0, nt > 1 ? 1 : -1};
+      for (int t = 2; t < nt; ++t) {
         const int s = t & 1;
-        if (t >= 2 && !mbar_wait(&bars[KVEMPTY + s], ((t >> 1) - 1) & 1, abort_flag, ds)) break;
-        const TileEntry te = tile_at(p, tr, t);
-        uint8_t* kdst = smem + L::kK + s * L::kKVBytes;
-        uint8_t* vdst = smem + L::kV + s * L::kKVBytes;
-        mbar_arrive_expect_tx(&bars[KFULL + s], L::kKVBytes);
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          if (te.rollout < 0)
-            tma_load_3d(kdst + hh * BN * 128, &maps.pk, hh * 64, te.key0, kvh, &bars[KFULL + s]);
-          else
-            tma_load_4d(kdst + hh * BN * 128, &maps.rk, hh * 64, te.key0, kvh, te.rollout, &bars[KFULL + s]);
-        }
-        mbar_arrive_expect_tx(&bars[VFULL + s], L::kKVBytes);
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          if (te.rollout < 0)
-            tma_load_3d(vdst + hh * BN * 128, &maps.pv, hh * 64, te.key0, kvh, &bars[VFULL + s]);
-          else
-            tma_load_4d(vdst + hh * BN * 128, &maps.rv, hh * 64, te.key0, kvh, te.rollout, &bars[VFULL + s]);
-        }
+        if (!mbar_wait(&bars[KVEMPTY + s], ((t >> 1) - 1) & 1, abort_flag, ds)) break;
+        issue_kv(t);
         last[s] = t;
       }
+      if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
       for (int s = 0; s < 2; ++s) {
         if (last[s] < 0) continue;
         mbar_drain(&bars[KFULL + s], (last[s] >> 1) & 1, ds);
@@ -408,16 +432,16 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     }
     const int qhead = kvh * p.G + g;
     const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-    {
+    if (!p.q_tma) {  // GQA group that does not divide 128: rows gathered by the threads
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + orow * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 val = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(rl, c * 8, BM)) = val;
       }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[QFULL]);
     }
-    fence_proxy_async_smem();
-    mbar_arrive(&bars[QFULL]);
 
     const int lim_priv = valid ? p.priv_len + block_end_of(p, i_row) : 0;
     const bool warp_active = __any_sync(0xffffffffu, valid);
@@ -452,7 +476,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
       const bool grow = m_tile > -INFINITY && (m_run == -INFINITY || m_tile > m_run + kRescaleLog2);
       float alpha = 1.f;
       if (grow) {
-        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_tile);
+        alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_tile);
         m_run = m_tile;
         l_run *= alpha;
       }
@@ -473,8 +497,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int k = c * 32 + 2 * j;
-            const float a = k < nv ? exp2f(fmaf(v[2 * j], p.scale_log2, -m_run)) : 0.f;
-            const float b = k + 1 < nv ? exp2f(fmaf(v[2 * j + 1], p.scale_log2, -m_run)) : 0.f;
+            const float a = k < nv ? fast_exp2(fmaf(v[2 * j], p.scale_log2, -m_run)) : 0.f;
+            const float b = k + 1 < nv ? fast_exp2(fmaf(v[2 * j + 1], p.scale_log2, -m_run)) : 0.f;
             l_run += a + b;
             pk[j] = pack_bf16x2(a, b);
           }

@@ -31,10 +31,12 @@ struct AttnParams {
   float scale_log2;       // sm_scale * log2(e)
   int rope;
   int delta;
+  int q_tma;              // Q tile by TMA (G divides 128)
   unsigned long long rope_turns[64];  // theta^(-2d/D) / (2*pi) as a 0.64 fixed-point fraction
 };
 
 struct AttnMaps {
+  CUtensorMap q;          // Q: 4D (D, G, Hkv, N * n_q), box {64, G, 1, 128 / G}
   CUtensorMap pk, pv;     // prefix K/V: 3D (D, C, Hkv)
   CUtensorMap rk, rv;     // private K/V: 4D (D, priv_len + n_q, Hkv, N)
 };

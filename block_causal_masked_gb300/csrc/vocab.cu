@@ -39,7 +39,7 @@ __device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
     return;
   }
   const float M = fmaxf(a.m, b.m);
-  const float s = a.s * exp2f((a.m - M) * kLog2e) + b.s * exp2f((b.m - M) * kLog2e);
+  const float s = a.s * fast_exp2((a.m - M) * kLog2e) + b.s * fast_exp2((b.m - M) * kLog2e);
   a.idx = a.m > b.m ? a.idx : (b.m > a.m ? b.idx : min(a.idx, b.idx));
   a.m = M;
   a.s = s;
@@ -54,13 +54,13 @@ __device__ __forceinline__ void acc_vec(Acc& a, const float (&x)[N], int i0, boo
   for (int k = 1; k < N; ++k)
     if (x[k] > vm) { vm = x[k]; vi = k; }
   if (vm > a.m) {
-    if (need_sum) a.s = (a.m == -INFINITY) ? 0.f : a.s * exp2f((a.m - vm) * kLog2e);
+    if (need_sum) a.s = (a.m == -INFINITY) ? 0.f : a.s * fast_exp2((a.m - vm) * kLog2e);
     a.m = vm;
     a.idx = i0 + vi;
   }
   if (need_sum) {
 #pragma unroll
-    for (int k = 0; k < N; ++k) a.s += exp2f((x[k] - a.m) * kLog2e);
+    for (int k = 0; k < N; ++k) a.s += fast_exp2((x[k] - a.m) * kLog2e);
   }
 }
 
