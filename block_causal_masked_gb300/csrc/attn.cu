@@ -19,7 +19,7 @@
 //     softmax in fp32 from TMEM, P rounded to bf16 into a swizzled smem tile;
 //     the running max is only moved (and O rescaled in TMEM) when it grows by
 //     more than 2^8, so most tiles need no O round trip;
-//   * with RoPE, warps 6-9 rotate each staged prefix K tile in shared memory at
+//   * with RoPE, warps 6-7 rotate each staged prefix K tile in shared memory at
 //     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
 //     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
@@ -265,7 +265,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
 }
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
+__global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     mbar_init(&bars[PFULL], 128);
     mbar_init(&bars[ODONE], 1);
     mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
-    mbar_init(&bars[KREADY + 0], 128);
-    mbar_init(&bars[KREADY + 1], 128);
+    mbar_init(&bars[KREADY + 0], 64);
+    mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
     misc[1] = 0;
     fence_mbar_init();
@@ -457,16 +457,17 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
       int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
       if (!valid) lim = 0;
       const int nv = max(0, min(BN, lim - te.key0));
+      // the whole S row in registers: one TMEM round trip, then S is free again
+      float sv[BN];
       float mx = -INFINITY;
       if (warp_active) {
+        tmem_ld128(lane_base + s * BN, sv);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld32(lane_base + s * BN + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < nv) mx = fmaxf(mx, v[j]);
-        }
+        for (int j = 0; j < BN; ++j)
+          if (j < nv) mx = fmaxf(mx, sv[j]);
       }
+      tc_fence_before();
+      mbar_arrive(&bars[SFREE + s]);
       const float m_tile = nv > 0 ? mx * p.scale_log2 : -INFINITY;
       if (t > 0) {
         ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
@@ -490,16 +491,16 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         }
       }
       if (warp_active) {
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld32(lane_base + s * BN + c * 32, v);
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int k = c * 32 + 2 * j;
-            const float a = k < nv ? fast_exp2(fmaf(v[2 * j], p.scale_log2, -m_run)) : 0.f;
-            const float b = k + 1 < nv ? fast_exp2(fmaf(v[2 * j + 1], p.scale_log2, -m_run)) : 0.f;
-            l_run += a + b;
+            const float a = k < nv ? fast_exp2(fmaf(sv[k], p.scale_log2, -m_run)) : 0.f;
+            const float b = k + 1 < nv ? fast_exp2(fmaf(sv[k + 1], p.scale_log2, -m_run)) : 0.f;
+            ls[j & 3] += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
 #pragma unroll
@@ -507,9 +508,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
             *reinterpret_cast<uint4*>(smem + L::kP + sw128_offset(rl, c * 32 + qq * 8, BM)) =
                 make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars[SFREE + s]);
       fence_proxy_async_smem();
       mbar_arrive(&bars[PFULL]);
     }
@@ -547,34 +547,37 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     }
   } else if (ROPE) {
     // ---------------------------------------------------------------- RoPE on staged prefix keys
-    const int kr = threadIdx.x - 192;  // key row of the tile
+    const int kr0 = threadIdx.x - 192;  // this thread rotates key rows kr0 and kr0 + 64 of the tile
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
       if (!mbar_wait(&bars[KFULL + s], (t >> 1) & 1, abort_flag, ds)) break;
       const TileEntry te = tile_at(p, tr, t);
-      const int key = te.key0 + kr;
-      if (te.rollout < 0 && key < p.C) {
-        const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
+      if (te.rollout < 0) {
         uint8_t* kt = smem + L::kK + s * L::kKVBytes;
+        for (int kr = kr0; kr < BN; kr += 64) {
+          const int key = te.key0 + kr;
+          if (key >= p.C) break;
+          const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
 #pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-          uint4* a4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8, BN));
-          uint4* b4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8 + D / 2, BN));
-          uint4 xa = *a4, xb = *b4;
-          uint32_t* wa = reinterpret_cast<uint32_t*>(&xa);
-          uint32_t* wb = reinterpret_cast<uint32_t*>(&xb);
+          for (int c = 0; c < D / 16; ++c) {
+            uint4* a4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8, BN));
+            uint4* b4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8 + D / 2, BN));
+            uint4 xa = *a4, xb = *b4;
+            uint32_t* wa = reinterpret_cast<uint32_t*>(&xa);
+            uint32_t* wb = reinterpret_cast<uint32_t*>(&xb);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float a0, a1, b0, b1, c0, s0, c1, s1;
-            bf16x2_unpack(wa[w], a0, a1);
-            bf16x2_unpack(wb[w], b0, b1);
-            rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w], c0, s0);
-            rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w + 1], c1, s1);
-            wa[w] = pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-            wb[w] = pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+            for (int w = 0; w < 4; ++w) {
+              float a0, a1, b0, b1, c0, s0, c1, s1;
+              bf16x2_unpack(wa[w], a0, a1);
+              bf16x2_unpack(wb[w], b0, b1);
+              rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w], c0, s0);
+              rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w + 1], c1, s1);
+              wa[w] = pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+              wb[w] = pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+            }
+            *a4 = xa;
+            *b4 = xb;
           }
-          *a4 = xa;
-          *b4 = xb;
         }
         fence_proxy_async_smem();
       }
@@ -605,7 +608,7 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(ROPE ? 320 : 192);
+  cfg.blockDim = dim3(ROPE ? 256 : 192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   for (;;) {
