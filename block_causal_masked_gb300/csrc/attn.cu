@@ -23,14 +23,14 @@
 //     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
 //     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
-//     the end each CTA stages its rows' (max, sum) and scaled O in shared
-//     memory and the cluster merges them through distributed shared memory,
-//     each CTA reducing and storing a slice of the rows -- no partials in
-//     global memory and no second kernel.
+//     the end each CTA stages its rows' unnormalised O with (max, sum) in
+//     shared memory and bulk-copies row slice q into CTA q of the cluster
+//     (completing on CTA q's mbarrier); each CTA then merges its slice from its
+//     own shared memory and stores it -- no partials in global memory, no
+//     second kernel, no remote loads.
 // Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -52,11 +52,10 @@ struct TileEntry {
   int key0;     // first key of the tile within its segment
 };
 
-namespace cg = cooperative_groups;
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, NUM_BARS = 16
+  KREADY = 13, DRAIN = 15, RECV = 16, NUM_BARS = 17
 };
 
 template <int D>
@@ -70,11 +69,14 @@ struct Layout {
   static constexpr int kP = kV + kStages * kKVBytes;
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kMisc = kBar + NUM_BARS * 8;
-  static constexpr int kML = kMisc + 64;       // [BM] (running max, sum) of each row, for the cluster merge
-  static constexpr int kLse = kML + BM * 8;    // [BM] merged LSE of each row
-  static constexpr int kEnd = kLse + BM * 4;
-  // the merge stages O (BM x D fp32) over the K stages, idle by then
-  static_assert(BM * D * 4 <= kStages * kKVBytes, "O staging must fit in the K ring");
+  static constexpr int kEnd = kMisc + 64;
+  // cluster merge, over the K / V rings and P, idle by then: staged rows of
+  // D + 4 floats (unnormalised O, then max and sum), then the received slices
+  static constexpr int kRowF = D + 4;
+  static constexpr int kStage = kK;
+  static constexpr int kRecv = kK + BM * kRowF * 4;
+  // S * merge_rows_per_cta(S) <= BM + 2 * S rows are received
+  static_assert(kRecv + (BM + 2 * kAttnMaxSplits) * kRowF * 4 <= kP + kPBytes, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
@@ -164,43 +166,43 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
   return {tr.r_first + k / tr.n_priv, (k % tr.n_priv) * BN};
 }
 
+// Rows of the tile each CTA of a cluster of S merges (even, so that slices stay
+// 16-byte multiples together with their (max, sum) words).
+__host__ __device__ __forceinline__ int merge_rows_per_cta(int S) { return ((BM + S - 1) / S + 1) & ~1; }
+
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
-// every thread of every CTA of the cluster; the softmax threads do the work:
-//   1. each row's (max, sum) of every split is read through distributed shared
-//      memory -> merged max M, sum L, and this split's weight 2^(m - M) / L;
-//   2. each CTA stages its weighted O rows (fp32) in its own shared memory;
-//   3. CTA `rank` sums a 1/S slice of the rows over the S CTAs and stores them.
+// every thread of every CTA of the cluster:
+//   1. the softmax threads stage their row: unnormalised O (from TMEM), then
+//      (running max, sum) in the row's padding;
+//   2. once every CTA of the cluster has finished its KV loop (its receive
+//      area overlaps the K/V rings), one thread bulk-copies row slice q to
+//      CTA q (receive slot "this CTA's rank"), completing on CTA q's RECV
+//      mbarrier;
+//   3. each CTA waits for the S slices of its own rows, merges them
+//      (M = max m_s, L = sum l_s 2^(m_s - M), O = sum O_s 2^(m_s - M) / L) and
+//      stores them;
+//   4. a cluster barrier keeps every CTA alive until all copies have landed.
 template <int D>
-__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
-                              float l_run) {
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
+                              uint32_t tmem, int m0, bool have_o, float m_run, float l_run) {
   using L = Layout<D>;
-  constexpr int kChunks = D / 4;  // float4 chunks per staged row
-  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int kRowF = L::kRowF;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 6;
-  const int quad = warp & 3;
-  const int rl = quad * 32 + lane;
   const int S = p.num_splits;
-  float2* ml = reinterpret_cast<float2*>(smem + L::kML);
-  float* lse_s = reinterpret_cast<float*>(smem + L::kLse);
-  float* ost = reinterpret_cast<float*>(smem + L::kK);
-  cluster.sync();  // every split's (max, sum) is staged
+  const int rank = static_cast<int>(cluster_rank());
+  const int rpc = merge_rows_per_cta(S);
+  float* stage = reinterpret_cast<float*>(smem + L::kStage);
+  float* recv = reinterpret_cast<float*>(smem + L::kRecv);
+  // Every role of this CTA is done with the K / V rings and P (the producer and
+  // the MMA thread have drained, the softmax threads have seen the last PV MMA
+  // complete), so other CTAs may now write into the receive area.
+  cluster_arrive();
   if (is_sm) {
-    float2 x[kAttnMaxSplits];
-#pragma unroll
-    for (int r = 0; r < kAttnMaxSplits; ++r)
-      if (r < S) x[r] = *cluster.map_shared_rank(ml + rl, r);  // all remote loads in flight at once
-    float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kAttnMaxSplits; ++r)
-      if (r < S && x[r].y > 0.f) M = fmaxf(M, x[r].x);
-    float Ls = 0.f;
-#pragma unroll
-    for (int r = 0; r < kAttnMaxSplits; ++r)
-      if (r < S && x[r].y > 0.f) Ls += x[r].y * fast_exp2(x[r].x - M);
-    const float w = (l_run > 0.f && Ls > 0.f) ? fast_exp2(m_run - M) / Ls : 0.f;
-    lse_s[rl] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    const int quad = warp & 3;
+    const int rl = quad * 32 + lane;
     const bool warp_active = __any_sync(0xffffffffu, m0 + rl < p.rows_per_head);
+    float* row = stage + rl * kRowF;
     if (warp_active) {
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       float v[32];
@@ -213,55 +215,74 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int pos = (c * 8 + q4) ^ (rl & (kChunks - 1));
-          *reinterpret_cast<float4*>(ost + rl * D + pos * 4) =
-              make_float4(v[4 * q4] * w, v[4 * q4 + 1] * w, v[4 * q4 + 2] * w, v[4 * q4 + 3] * w);
-        }
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<float4*>(row + c * 32 + q4 * 4) = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
       }
     }
+    *reinterpret_cast<float4*>(row + D) = make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f);
+    fence_proxy_async_smem();
   }
-  cluster.sync();  // every split's weighted O is staged
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster is ready to receive
+  if (threadIdx.x == 0) {
+    const uint32_t src0 = smem_addr(stage);
+    const uint32_t dst0 = smem_addr(recv + rank * rpc * kRowF);
+    const uint32_t mbar0 = smem_addr(&bars[RECV]);
+    for (int q = 0; q < S; ++q) {
+      const int n = max(0, min(BM - q * rpc, rpc));
+      if (n == 0) continue;
+      bulk_copy_to_cluster(cluster_addr(dst0, q), src0 + q * rpc * kRowF * 4, n * kRowF * 4,
+                           cluster_addr(mbar0, q));
+    }
+  }
+  const int r0 = rank * rpc;
+  const int mine = max(0, min(BM - r0, rpc));
   if (is_sm) {
+    const bool ok = mbar_wait(&bars[RECV], 0, abort_flag, p.dev_status);
     const int t = threadIdx.x - 64;
-    const int rank = static_cast<int>(cluster.block_rank());
-    const int rpc = (BM + S - 1) / S;
-    const int r0 = rank * rpc;
-    const int r1 = min(BM, r0 + rpc);
     const int per_roll = p.n_q * p.G;
     const int kvh = blockIdx.z;
-    for (int it = t; it < (r1 - r0) * kChunks; it += 128) {
-      const int row_l = r0 + it / kChunks;
-      const int ch = it % kChunks;
-      const int grow = m0 + row_l;
+    constexpr int kChunks = D / 4;
+    for (int it = t; ok && it < mine * kChunks; it += 128) {
+      const int j = it / kChunks;
+      const int ch = it - j * kChunks;
+      const int grow = m0 + r0 + j;
       if (grow >= p.rows_per_head) continue;
-      const int pos = ch ^ (row_l & (kChunks - 1));
-      float4 part[kAttnMaxSplits];
-      float4* src = reinterpret_cast<float4*>(ost + row_l * D + pos * 4);
-#pragma unroll
-      for (int r = 0; r < kAttnMaxSplits; ++r)
-        if (r < S) part[r] = *cluster.map_shared_rank(src, r);  // all remote loads in flight at once
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < kAttnMaxSplits; ++r) {
-        if (r < S) {
-          acc.x += part[r].x;
-          acc.y += part[r].y;
-          acc.z += part[r].z;
-          acc.w += part[r].w;
-        }
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float* ml = recv + (s2 * rpc + j) * kRowF + D;
+        if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
       }
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float* r = recv + (s2 * rpc + j) * kRowF;
+        if (!(r[D + 1] > 0.f)) continue;
+        const float w = fast_exp2(r[D] - M);
+        Ls += r[D + 1] * w;
+        const float4 x = *reinterpret_cast<const float4*>(r + ch * 4);
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       const int r_row = grow / per_roll;
       const int rem = grow - r_row * per_roll;
       const int i_row = rem / p.G;
       const int qhead = kvh * p.G + (rem - i_row * p.G);
       const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
       *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
-          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_s[row_l];
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+      if (ch == 0 && p.lse)
+        p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
+            Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
+  } else if (threadIdx.x == 0) {
+    mbar_drain(&bars[RECV], 0, p.dev_status);  // the slices sent to this CTA have all landed
   }
-  cluster.sync();  // no CTA leaves while another still reads its shared memory
+  cluster_arrive();  // this CTA has received everything: the copies it was sent are done
+  cluster_wait();    // ... and so has every other CTA: the copies this CTA sent are done
 }
 
 template <int D, bool ROPE>
@@ -324,6 +345,13 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     mbar_init(&bars[KREADY + 0], 64);
     mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
+    mbar_init(&bars[RECV], 1);
+    if (p.num_splits > 1) {
+      // this CTA's slice of the cluster merge: rows [rank * rpc, ...) from every split
+      const int rpc = merge_rows_per_cta(p.num_splits);
+      const int mine = max(0, min(BM - static_cast<int>(cluster_rank()) * rpc, rpc));
+      mbar_arrive_expect_tx(&bars[RECV], static_cast<uint32_t>(p.num_splits * mine * L::kRowF * 4));
+    }
     misc[1] = 0;
     fence_mbar_init();
     // the first loads leave before the rest of the CTA is set up
@@ -542,8 +570,6 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       if (valid && p.lse)
         p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
             l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-    } else {
-      reinterpret_cast<float2*>(smem + L::kML)[rl] = make_float2(m_run, l_run);
     }
   } else if (ROPE) {
     // ---------------------------------------------------------------- RoPE on staged prefix keys
@@ -585,7 +611,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
   }
 
-  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run);
+  if (p.num_splits > 1) cluster_merge<D>(p, smem, bars, abort_flag, tmem, m0, have_o, m_run, l_run);
 
   tc_fence_before();
   __syncthreads();

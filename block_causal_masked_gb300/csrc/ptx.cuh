@@ -111,6 +111,34 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// Shared::cluster address of the same shared-memory location in CTA `rank` of
+// this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// shared::cluster address, completing `bytes` transactions on the mbarrier at
+// the shared::cluster address `mbar` (in the destination CTA).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
+// Cluster-wide barrier, split into arrive and wait (every thread of every CTA
+// of the cluster arrives once per phase; all threads of a warp together).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tcgen05.mma operands, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
