@@ -17,7 +17,8 @@ import torch
 
 from . import _build
 
-__all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_spec_verify", "bd_check",
+__all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_unmask_step_noalloc",
+           "bd_spec_verify", "bd_check",
            "bd_status_string", "lib", "BdError", "Workspace", "MASKED", "COMMITTED", "SCAFFOLD",
            "INACTIVE", "HALF", "FULL", "DONE"]
 
@@ -307,3 +308,45 @@ def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.
 def bd_check(dev_status, stream=None) -> int:
     """Synchronises the stream and maps the device status word (0 = ok)."""
     return lib().bd_check(dev_status.data_ptr(), _stream(stream))
+
+
+def bd_unmask_step_noalloc(logits, logit_row, block_start, state, tokens, *, tau_full: float, tau_half: float,
+                           min_frac=(1, 4), k_fixed: int = 0, add_thr=(1, 2), act_thr=(17, 20), write_draft=False,
+                           commit=None, n_committed=None, status=None, pred=None, conf=None, lse=None,
+                           dev_status=None, stream=None):
+    """bd_unmask_step without a workspace: the library's own fixed scratch array
+    is used (for callers that cannot allocate device memory).  Output tensors
+    not given are created here, as in bd_unmask_step; pass them all to
+    allocate nothing on this side either.  Calls that overlap on the GPU race."""
+    R, V = logits.shape
+    n_pos = state.numel()
+    n_blocks = block_start.numel() - 1
+    dev = logits.device
+    commit = torch.empty(n_pos, dtype=torch.uint8, device=dev) if commit is None else commit
+    n_committed = torch.empty(n_blocks, dtype=torch.int32, device=dev) if n_committed is None else n_committed
+    status = torch.empty(n_blocks, dtype=torch.int32, device=dev) if status is None else status
+    pred = torch.empty(n_pos, dtype=torch.int32, device=dev) if pred is None else pred
+    conf = torch.empty(n_pos, dtype=torch.float32, device=dev) if conf is None else conf
+    lse = torch.empty(n_pos, dtype=torch.float32, device=dev) if lse is None else lse
+    a = bd_unmask_args()
+    a.logits = logits.data_ptr()
+    a.logits_dtype = BD_BF16 if logits.dtype == torch.bfloat16 else BD_F32
+    a.logits_ld = logits.stride(0) if R > 1 else (V + 7) // 8 * 8
+    a.R, a.V = R, V
+    a.logit_row, a.n_pos = logit_row.data_ptr(), n_pos
+    a.block_start, a.n_blocks = block_start.data_ptr(), n_blocks
+    a.state, a.tokens = state.data_ptr(), tokens.data_ptr()
+    a.tau_full, a.tau_half = float(tau_full), float(tau_half)
+    a.min_num, a.min_den = int(min_frac[0]), int(min_frac[1])
+    a.k_fixed = int(k_fixed)
+    a.add_num, a.add_den = int(add_thr[0]), int(add_thr[1])
+    a.act_num, a.act_den = int(act_thr[0]), int(act_thr[1])
+    a.commit, a.n_committed, a.status = commit.data_ptr(), n_committed.data_ptr(), status.data_ptr()
+    a.pred, a.conf, a.lse = pred.data_ptr(), conf.data_ptr(), lse.data_ptr()
+    a.write_draft = 1 if write_draft else 0
+    a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    fn = lib().bd_unmask_step_noalloc
+    fn.argtypes = [ct.POINTER(bd_unmask_args), ct.c_void_p]
+    fn.restype = ct.c_int
+    _check("bd_unmask_step_noalloc", fn(a, _stream(stream)))
+    return dict(commit=commit, n_committed=n_committed, status=status, pred=pred, conf=conf, lse=lse)

@@ -465,3 +465,48 @@ bd_status bd_check(const int32_t* dev_status, void* stream) {
 const char* bd_version(void) { return "0.1.0"; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free unmask step
+//
+// For callers that cannot allocate device memory, the scratch of one unmask
+// step lives in this fixed array, which every GPU that loads the library holds
+// until the process exits.  Host code must not pass the array's name to a
+// kernel (on the host it is only a stand-in for the symbol): its device address
+// is looked up once per device with cudaGetSymbolAddress and cached.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_unmask_scratch[BD_UNMASK_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64];  // device address of g_unmask_scratch on each device, once looked up
+
+}  // namespace
+
+extern "C" bd_status bd_unmask_step_noalloc(const bd_unmask_args* a, void* stream) {
+  int chunks, elems;
+  size_t need;
+  bd_status st = plan_unmask(a, &chunks, &elems, &need);
+  if (st != BD_OK) return st;
+  if (need > BD_UNMASK_NOALLOC_SCRATCH_BYTES) return BD_ERR_WORKSPACE;
+  if ((st = check_device()) != BD_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_unmask_scratch) != cudaSuccess || ptr == nullptr) return BD_ERR_CUDA;
+      g_scratch_addr[dev] = ptr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  // The counter words must start at zero; a call cut short may have left them set.
+  if (cudaMemsetAsync(scratch, 0, unmask_counter_bytes(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BD_ERR_CUDA;
+  bd_unmask_args b = *a;
+  b.workspace = scratch;
+  b.workspace_bytes = BD_UNMASK_NOALLOC_SCRATCH_BYTES;
+  return bd_unmask_step(&b, stream);
+}

@@ -273,6 +273,32 @@ bd_status bd_unmask_step(const bd_unmask_args* a, void* stream);
 size_t bd_unmask_workspace_size(const bd_unmask_args* a);
 
 /* -----------------------------------------------------------------------------
+ * bd_unmask_step_noalloc
+ *
+ * No counterpart in the paper: a deployment convenience.  Same computation,
+ * arguments and results as bd_unmask_step, for callers that cannot allocate
+ * device memory -- for example an in-vehicle runtime whose memory plan is fixed
+ * at start-up and forbids device allocation afterwards, or a plug-in host that
+ * owns all device memory and hands a plug-in only its input and output buffers.
+ * Such a caller cannot provide a workspace; this entry point ignores
+ * a->workspace / a->workspace_bytes and uses a scratch array of
+ * BD_UNMASK_NOALLOC_SCRATCH_BYTES inside the library instead (every GPU that
+ * loads the library holds it until the process exits).  It allocates nothing.
+ *
+ * - Problems needing more scratch than that (bd_unmask_workspace_size(a) larger
+ *   than BD_UNMASK_NOALLOC_SCRATCH_BYTES) are refused with BD_ERR_WORKSPACE.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Each call clears the array's counter words on `stream` first; the rest of
+ *   the array keeps the previous call's contents.
+ * - All calls share the one array: calls whose work overlaps on the GPU (other
+ *   streams, or no ordering between them) race and give wrong results.
+ * ---------------------------------------------------------------------------*/
+#define BD_UNMASK_NOALLOC_SCRATCH_BYTES (1u << 20)
+bd_status bd_unmask_step_noalloc(const bd_unmask_args* a, void* stream);
+
+/* -----------------------------------------------------------------------------
  * bd_spec_verify
  *
  * Fast-dDrive method summary (e.mffb.com.cn) §3.2 "模式二：Scaffold Speculative
