@@ -76,7 +76,8 @@ struct Layout {
   static constexpr int kStage = kK;
   static constexpr int kRecv = kK + BM * kRowF * 4;
   // S * merge_rows_per_cta(S) <= BM + 2 * S rows are received
-  static_assert(kRecv + (BM + 2 * kAttnMaxSplits) * kRowF * 4 <= kP + kPBytes, "merge buffers must fit");
+  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * kRowF * 4;  // [rpc][16] weights, [rpc] LSE
+  static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
@@ -243,40 +244,49 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint64_t* bars
     const int per_roll = p.n_q * p.G;
     const int kvh = blockIdx.z;
     constexpr int kChunks = D / 4;
-    for (int it = t; ok && it < mine * kChunks; it += 128) {
-      const int j = it / kChunks;
-      const int ch = it - j * kChunks;
-      const int grow = m0 + r0 + j;
-      if (grow >= p.rows_per_head) continue;
+    // each owned row's merged max / sum and the weight of every split
+    float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][S]
+    float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
+    for (int j = t; ok && j < mine; j += 128) {
       float M = -INFINITY;
       for (int s2 = 0; s2 < S; ++s2) {
         const float* ml = recv + (s2 * rpc + j) * kRowF + D;
         if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
       }
       float Ls = 0.f;
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float* ml = recv + (s2 * rpc + j) * kRowF + D;
+        const float w = ml[1] > 0.f ? fast_exp2(ml[0] - M) : 0.f;
+        wts[j * kAttnMaxSplits + s2] = w;
+        Ls += ml[1] * w;
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      for (int s2 = 0; s2 < S; ++s2) wts[j * kAttnMaxSplits + s2] *= inv;
+      lse_row[j] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    }
+    named_sync(1, 128);
+    for (int it = t; ok && it < mine * kChunks; it += 128) {
+      const int j = it / kChunks;
+      const int ch = it - j * kChunks;
+      const int grow = m0 + r0 + j;
+      if (grow >= p.rows_per_head) continue;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int s2 = 0; s2 < S; ++s2) {
-        const float* r = recv + (s2 * rpc + j) * kRowF;
-        if (!(r[D + 1] > 0.f)) continue;
-        const float w = fast_exp2(r[D] - M);
-        Ls += r[D + 1] * w;
-        const float4 x = *reinterpret_cast<const float4*>(r + ch * 4);
+        const float w = wts[j * kAttnMaxSplits + s2];
+        const float4 x = *reinterpret_cast<const float4*>(recv + (s2 * rpc + j) * kRowF + ch * 4);
         acc.x = fmaf(w, x.x, acc.x);
         acc.y = fmaf(w, x.y, acc.y);
         acc.z = fmaf(w, x.z, acc.z);
         acc.w = fmaf(w, x.w, acc.w);
       }
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       const int r_row = grow / per_roll;
       const int rem = grow - r_row * per_roll;
       const int i_row = rem / p.G;
       const int qhead = kvh * p.G + (rem - i_row * p.G);
       const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
       *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
-          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-      if (ch == 0 && p.lse)
-        p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
-            Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
     }
   } else if (threadIdx.x == 0) {
     mbar_drain(&bars[RECV], 0, p.dev_status);  // the slices sent to this CTA have all landed
@@ -329,6 +339,13 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
   };
 
   if (threadIdx.x == 0) {
+    if (p.q_tma) tma_prefetch_desc(&maps.q);
+    if (p.n_prefix_tiles > 0) {
+      tma_prefetch_desc(&maps.pk);
+      tma_prefetch_desc(&maps.pv);
+    }
+    tma_prefetch_desc(&maps.rk);
+    tma_prefetch_desc(&maps.rv);
     mbar_init(&bars[KFULL + 0], 1);
     mbar_init(&bars[KFULL + 1], 1);
     mbar_init(&bars[VFULL + 0], 1);
@@ -354,6 +371,16 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
     misc[1] = 0;
     fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&misc[0], L::kTmemCols);
+    tmem_relinquish();
+  }
+  // Everything above touches only shared memory, TMEM and the kernel's own
+  // parameters; from here on this thread reads or writes global memory, which
+  // the previous kernel in the stream may still be producing.
+  pdl_wait();
+  if (threadIdx.x == 0) {
     // the first loads leave before the rest of the CTA is set up
     if (nt > 0) {
       if (p.q_tma) {
@@ -366,13 +393,10 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       if (nt > 1) issue_kv(1);
     }
   }
-  if (warp == 1) {
-    tmem_alloc(&misc[0], L::kTmemCols);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // the next kernel may start its own set-up on free SMs
   const uint32_t tmem = misc[0];
   // softmax state of this thread's packed row (softmax warps), kept for the merge
   float m_run = -INFINITY;  // running max, log2-scaled
@@ -490,9 +514,17 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       float mx = -INFINITY;
       if (warp_active) {
         tmem_ld128(lane_base + s * BN, sv);
+        if (!__all_sync(0xffffffffu, nv == BN)) {
 #pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (j < nv) mx = fmaxf(mx, sv[j]);
+          for (int j = 0; j < BN; ++j)
+            if (j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+        }
+        float m8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+#pragma unroll
+        for (int j = 8; j < BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], sv[j]);
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       tc_fence_before();
       mbar_arrive(&bars[SFREE + s]);
@@ -519,16 +551,18 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
         }
       }
       if (warp_active) {
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // masked entries are -inf; a row that has seen no key yet keeps m_run = -inf
+        const float mneg = m_run == -INFINITY ? 0.f : -m_run;
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int k = c * 32 + 2 * j;
-            const float a = k < nv ? fast_exp2(fmaf(sv[k], p.scale_log2, -m_run)) : 0.f;
-            const float b = k + 1 < nv ? fast_exp2(fmaf(sv[k + 1], p.scale_log2, -m_run)) : 0.f;
-            ls[j & 3] += a + b;
+            const float a = fast_exp2(fmaf(sv[k], p.scale_log2, mneg));
+            const float b = fast_exp2(fmaf(sv[k + 1], p.scale_log2, mneg));
+            ls[j & 7] += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
 #pragma unroll
@@ -536,7 +570,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
             *reinterpret_cast<uint4*>(smem + L::kP + sw128_offset(rl, c * 32 + qq * 8, BM)) =
                 make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
-        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[PFULL]);
@@ -633,7 +667,7 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(ROPE ? 256 : 192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -643,8 +677,10 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
     attr[0].val.clusterDim.x = p.num_splits;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (p.num_splits <= 8) break;
     // a cluster wider than the portable 8 needs that many SMs free in one GPC
     int n = 0;

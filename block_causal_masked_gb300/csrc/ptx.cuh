@@ -87,6 +87,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Programmatic dependent launch.  wait: this thread's global reads and writes
+// may begin (the preceding grid has completed and its writes are visible);
+// launch_dependents: the next grid in the stream may start being scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Named barrier over `count` threads (ids 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -293,6 +293,8 @@ __device__ void unmask_select(const UnmaskParams& p) {
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
   __shared__ Acc red[kThreads / 32];
   __shared__ int last;
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_trigger();  // the next kernel may start its own set-up
   const int pos = blockIdx.y;
   const int chunk = blockIdx.x;
   const int row = __ldg(p.logit_row + pos);
@@ -377,6 +379,8 @@ __device__ void verify_match(const VerifyParams& p, int s) {
 __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
   __shared__ Acc red[kThreads / 32];
   __shared__ int last;
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y;  // sequence * n_rows + e
   const int chunk = blockIdx.x;
   const int s = row / p.n_rows;
@@ -431,16 +435,30 @@ size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
   return verify_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_seq) * n_rows * chunks);
 }
 
+// Launch with programmatic stream serialisation, so that the kernel's set-up can
+// overlap the tail of the previous kernel (each kernel waits for it with
+// griddepcontrol.wait before touching global memory).
+template <typename P>
+static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
-  const dim3 grid(p.chunks, p.n_pos);
-  unmask_kernel<<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(unmask_kernel, dim3(p.chunks, p.n_pos), p, stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
-  const dim3 grid(p.chunks, p.n_seq * p.n_rows);
-  verify_kernel<<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(verify_kernel, dim3(p.chunks, p.n_seq * p.n_rows), p, stream);
 }
 
 }  // namespace bd
