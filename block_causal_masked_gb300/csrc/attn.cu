@@ -23,11 +23,11 @@
 //     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
 //     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
-//     the end each CTA stages its rows' unnormalised O with (max, sum) in
-//     shared memory and bulk-copies row slice q into CTA q of the cluster
-//     (completing on CTA q's mbarrier); each CTA then merges its slice from its
-//     own shared memory and stores it -- no partials in global memory, no
-//     second kernel, no remote loads.
+//     the end every softmax thread stores its row's unnormalised O and (max,
+//     sum) straight into the shared memory of the CTA that owns that row's
+//     slice (st.shared::cluster); each CTA then merges its slice from its own
+//     shared memory and stores it -- no partials in global memory, no second
+//     kernel, no remote loads.
 // Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
@@ -55,7 +55,7 @@ struct TileEntry {
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, RECV = 16, NUM_BARS = 17
+  KREADY = 13, DRAIN = 15, NUM_BARS = 16
 };
 
 template <int D>
@@ -70,11 +70,10 @@ struct Layout {
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kMisc = kBar + NUM_BARS * 8;
   static constexpr int kEnd = kMisc + 64;
-  // cluster merge, over the K / V rings and P, idle by then: staged rows of
-  // D + 4 floats (unnormalised O, then max and sum), then the received slices
+  // cluster merge, over the K / V rings and P, idle by then: received rows of
+  // D + 4 floats (unnormalised O, then max and sum), S slots of rpc rows
   static constexpr int kRowF = D + 4;
-  static constexpr int kStage = kK;
-  static constexpr int kRecv = kK + BM * kRowF * 4;
+  static constexpr int kRecv = kK;
   // S * merge_rows_per_cta(S) <= BM + 2 * S rows are received
   static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * kRowF * 4;  // [rpc][16] weights, [rpc] LSE
   static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
@@ -167,44 +166,42 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
   return {tr.r_first + k / tr.n_priv, (k % tr.n_priv) * BN};
 }
 
-// Rows of the tile each CTA of a cluster of S merges (even, so that slices stay
-// 16-byte multiples together with their (max, sum) words).
+// Rows of the tile each CTA of a cluster of S merges (kept even).
 __host__ __device__ __forceinline__ int merge_rows_per_cta(int S) { return ((BM + S - 1) / S + 1) & ~1; }
 
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster:
-//   1. the softmax threads stage their row: unnormalised O (from TMEM), then
-//      (running max, sum) in the row's padding;
-//   2. once every CTA of the cluster has finished its KV loop (its receive
-//      area overlaps the K/V rings), one thread bulk-copies row slice q to
-//      CTA q (receive slot "this CTA's rank"), completing on CTA q's RECV
-//      mbarrier;
-//   3. each CTA waits for the S slices of its own rows, merges them
+//   1. cluster barrier: every CTA has finished its KV loop, so its K/V rings and
+//      P tile (the receive area) may be written;
+//   2. each softmax thread stores its row -- unnormalised O from TMEM, then
+//      (running max, sum) -- into slot "this CTA's rank" of the receive area of
+//      the CTA that owns the row (rows [q * rpc, (q + 1) * rpc) belong to CTA q);
+//   3. cluster barrier (release / acquire): every row has been delivered;
+//   4. each CTA merges its rows from its own shared memory
 //      (M = max m_s, L = sum l_s 2^(m_s - M), O = sum O_s 2^(m_s - M) / L) and
-//      stores them;
-//   4. a cluster barrier keeps every CTA alive until all copies have landed.
+//      stores them.  Nobody reads another CTA's shared memory, so no third
+//      barrier is needed before exit.
 template <int D>
-__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint64_t* bars, volatile int* abort_flag,
-                              uint32_t tmem, int m0, bool have_o, float m_run, float l_run) {
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
+                              float l_run) {
   using L = Layout<D>;
   constexpr int kRowF = L::kRowF;
+  constexpr int kChunks = D / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 6;
   const int S = p.num_splits;
   const int rank = static_cast<int>(cluster_rank());
   const int rpc = merge_rows_per_cta(S);
-  float* stage = reinterpret_cast<float*>(smem + L::kStage);
   float* recv = reinterpret_cast<float*>(smem + L::kRecv);
-  // Every role of this CTA is done with the K / V rings and P (the producer and
-  // the MMA thread have drained, the softmax threads have seen the last PV MMA
-  // complete), so other CTAs may now write into the receive area.
-  cluster_arrive();
+  cluster_arrive();  // this CTA is done with its rings: others may write into them
+  cluster_wait();
   if (is_sm) {
     const int quad = warp & 3;
     const int rl = quad * 32 + lane;
-    const bool warp_active = __any_sync(0xffffffffu, m0 + rl < p.rows_per_head);
-    float* row = stage + rl * kRowF;
-    if (warp_active) {
+    if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
+      const int owner = rl / rpc;
+      const uint32_t dst = cluster_addr(smem_addr(recv + (rank * rpc + (rl - owner * rpc)) * kRowF),
+                                        static_cast<uint32_t>(owner));
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       float v[32];
 #pragma unroll
@@ -217,67 +214,69 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint64_t* bars
         }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          *reinterpret_cast<float4*>(row + c * 32 + q4 * 4) = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          st_cluster_v4(dst + (c * 32 + q4 * 4) * 4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
       }
-    }
-    *reinterpret_cast<float4*>(row + D) = make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f);
-    fence_proxy_async_smem();
-  }
-  __syncthreads();
-  cluster_wait();  // every CTA of the cluster is ready to receive
-  if (threadIdx.x == 0) {
-    const uint32_t src0 = smem_addr(stage);
-    const uint32_t dst0 = smem_addr(recv + rank * rpc * kRowF);
-    const uint32_t mbar0 = smem_addr(&bars[RECV]);
-    for (int q = 0; q < S; ++q) {
-      const int n = max(0, min(BM - q * rpc, rpc));
-      if (n == 0) continue;
-      bulk_copy_to_cluster(cluster_addr(dst0, q), src0 + q * rpc * kRowF * 4, n * kRowF * 4,
-                           cluster_addr(mbar0, q));
+      st_cluster_v4(dst + D * 4, m_run, have_o ? l_run : 0.f, 0.f, 0.f);
     }
   }
+  cluster_arrive();  // release: this CTA's rows are delivered
+  cluster_wait();    // acquire: every CTA's rows are delivered
   const int r0 = rank * rpc;
   const int mine = max(0, min(BM - r0, rpc));
   if (is_sm) {
-    const bool ok = mbar_wait(&bars[RECV], 0, abort_flag, p.dev_status);
     const int t = threadIdx.x - 64;
     const int per_roll = p.n_q * p.G;
     const int kvh = blockIdx.z;
-    constexpr int kChunks = D / 4;
-    // each owned row's merged max / sum and the weight of every split
-    float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][S]
+    float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][16] weights of the splits
     float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
-    for (int j = t; ok && j < mine; j += 128) {
+    for (int j = t; j < mine; j += 128) {
+      float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
       float M = -INFINITY;
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float* ml = recv + (s2 * rpc + j) * kRowF + D;
-        if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+        mv[s2] = -INFINITY;
+        lv[s2] = 0.f;
+        if (s2 < S) {
+          const float* ml = recv + (s2 * rpc + j) * kRowF + D;
+          mv[s2] = ml[0];
+          lv[s2] = ml[1];
+        }
       }
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
       float Ls = 0.f;
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float* ml = recv + (s2 * rpc + j) * kRowF + D;
-        const float w = ml[1] > 0.f ? fast_exp2(ml[0] - M) : 0.f;
-        wts[j * kAttnMaxSplits + s2] = w;
-        Ls += ml[1] * w;
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+        mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
+        Ls += lv[s2] * mv[s2];
       }
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-      for (int s2 = 0; s2 < S; ++s2) wts[j * kAttnMaxSplits + s2] *= inv;
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (s2 < S) wts[j * kAttnMaxSplits + s2] = mv[s2] * inv;
       lse_row[j] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
     named_sync(1, 128);
-    for (int it = t; ok && it < mine * kChunks; it += 128) {
+    for (int it = t; it < mine * kChunks; it += 128) {
       const int j = it / kChunks;
       const int ch = it - j * kChunks;
       const int grow = m0 + r0 + j;
       if (grow >= p.rows_per_head) continue;
+      float4 x[kAttnMaxSplits];
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (s2 < S) x[s2] = *reinterpret_cast<const float4*>(recv + (s2 * rpc + j) * kRowF + ch * 4);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float w = wts[j * kAttnMaxSplits + s2];
-        const float4 x = *reinterpret_cast<const float4*>(recv + (s2 * rpc + j) * kRowF + ch * 4);
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+        if (s2 < S) {
+          const float w = wts[j * kAttnMaxSplits + s2];
+          acc.x = fmaf(w, x[s2].x, acc.x);
+          acc.y = fmaf(w, x[s2].y, acc.y);
+          acc.z = fmaf(w, x[s2].z, acc.z);
+          acc.w = fmaf(w, x[s2].w, acc.w);
+        }
       }
       const int r_row = grow / per_roll;
       const int rem = grow - r_row * per_roll;
@@ -288,11 +287,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint64_t* bars
           make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
       if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
     }
-  } else if (threadIdx.x == 0) {
-    mbar_drain(&bars[RECV], 0, p.dev_status);  // the slices sent to this CTA have all landed
   }
-  cluster_arrive();  // this CTA has received everything: the copies it was sent are done
-  cluster_wait();    // ... and so has every other CTA: the copies this CTA sent are done
 }
 
 template <int D, bool ROPE>
@@ -362,13 +357,6 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     mbar_init(&bars[KREADY + 0], 64);
     mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
-    mbar_init(&bars[RECV], 1);
-    if (p.num_splits > 1) {
-      // this CTA's slice of the cluster merge: rows [rank * rpc, ...) from every split
-      const int rpc = merge_rows_per_cta(p.num_splits);
-      const int mine = max(0, min(BM - static_cast<int>(cluster_rank()) * rpc, rpc));
-      mbar_arrive_expect_tx(&bars[RECV], static_cast<uint32_t>(p.num_splits * mine * L::kRowF * 4));
-    }
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -645,7 +633,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
   }
 
-  if (p.num_splits > 1) cluster_merge<D>(p, smem, bars, abort_flag, tmem, m0, have_o, m_run, l_run);
+  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run);
 
   tc_fence_before();
   __syncthreads();

@@ -140,6 +140,12 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
                : "memory");
 }
 
+// 16-byte store to a shared::cluster address (possibly another CTA's shared memory).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // Cluster-wide barrier, split into arrive and wait (every thread of every CTA
 // of the cluster arrives once per phase; all threads of a warp together).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
