@@ -140,7 +140,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
     splits = s < 1 ? 1 : static_cast<int>(s);
   }
   pl->splits = splits;
-  pl->ws_bytes = 0;  // splits are merged on chip, in the cluster
+  // split partials: [Hkv, m_tiles, splits, 128 rows, D + 4 floats]
+  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * splits * kAttnBM * (d.D + 4) * 4 : 0;
   return BD_OK;
 }
 
@@ -161,6 +162,8 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.q = d.q;
   p.o = d.o;
   p.lse = d.lse;
+  p.part = pl.splits > 1 ? static_cast<float*>(d.ws) : nullptr;
+  p.m_tiles = pl.m_tiles;
   p.block_start = d.block_start;
   p.k_pos = d.rope.enabled ? d.rope.k_pos : nullptr;
   p.dev_status = d.ds;

@@ -23,11 +23,10 @@
 //     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
 //     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
-//     the end every softmax thread stores its row's unnormalised O and (max,
-//     sum) straight into the shared memory of the CTA that owns that row's
-//     slice (st.shared::cluster); each CTA then merges its slice from its own
-//     shared memory and stores it -- no partials in global memory, no second
-//     kernel, no remote loads.
+//     the end every softmax thread writes its row's unnormalised O and (max,
+//     sum) to a workspace that stays in L2, one cluster barrier makes them
+//     visible, and each CTA merges 1/S of the rows from all splits and stores
+//     them -- one kernel, no second launch.
 // Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
@@ -171,16 +170,12 @@ __host__ __device__ __forceinline__ int merge_rows_per_cta(int S) { return ((BM 
 
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster:
-//   1. cluster barrier: every CTA has finished its KV loop, so its K/V rings and
-//      P tile (the receive area) may be written;
-//   2. each softmax thread stores its row -- unnormalised O from TMEM, then
-//      (running max, sum) -- into slot "this CTA's rank" of the receive area of
-//      the CTA that owns the row (rows [q * rpc, (q + 1) * rpc) belong to CTA q);
-//   3. cluster barrier (release / acquire): every row has been delivered;
-//   4. each CTA merges its rows from its own shared memory
-//      (M = max m_s, L = sum l_s 2^(m_s - M), O = sum O_s 2^(m_s - M) / L) and
-//      stores them.  Nobody reads another CTA's shared memory, so no third
-//      barrier is needed before exit.
+//   1. each softmax thread writes its row -- unnormalised O from TMEM, then
+//      (running max, sum) -- to the workspace (slot of this split);
+//   2. cluster barrier (release / acquire): every split's rows are visible;
+//   3. CTA q merges rows [q * rpc, (q + 1) * rpc) from the S splits
+//      (M = max m_s, L = sum l_s 2^(m_s - M), O = sum O_s 2^(m_s - M) / L),
+//      reading them through L2, and stores them.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
                               float l_run) {
@@ -190,18 +185,15 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 6;
   const int S = p.num_splits;
-  const int rank = static_cast<int>(cluster_rank());
+  const int split = blockIdx.x;
   const int rpc = merge_rows_per_cta(S);
-  float* recv = reinterpret_cast<float*>(smem + L::kRecv);
-  cluster_arrive();  // this CTA is done with its rings: others may write into them
-  cluster_wait();
+  // this (row tile, KV head)'s partials: [S][BM][kRowF]
+  float* part = p.part + (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * S * BM * kRowF;
   if (is_sm) {
     const int quad = warp & 3;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
-      const int owner = rl / rpc;
-      const uint32_t dst = cluster_addr(smem_addr(recv + (rank * rpc + (rl - owner * rpc)) * kRowF),
-                                        static_cast<uint32_t>(owner));
+      float* dst = part + (static_cast<size_t>(split) * BM + rl) * kRowF;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       float v[32];
 #pragma unroll
@@ -214,14 +206,15 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
         }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          st_cluster_v4(dst + (c * 32 + q4 * 4) * 4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          __stcg(reinterpret_cast<float4*>(dst + c * 32 + q4 * 4),
+                 make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
       }
-      st_cluster_v4(dst + D * 4, m_run, have_o ? l_run : 0.f, 0.f, 0.f);
+      __stcg(reinterpret_cast<float4*>(dst + D), make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
     }
   }
-  cluster_arrive();  // release: this CTA's rows are delivered
-  cluster_wait();    // acquire: every CTA's rows are delivered
-  const int r0 = rank * rpc;
+  cluster_arrive();  // release: this split's rows are written
+  cluster_wait();    // acquire: every split's rows are written
+  const int r0 = split * rpc;
   const int mine = max(0, min(BM - r0, rpc));
   if (is_sm) {
     const int t = threadIdx.x - 64;
@@ -231,17 +224,17 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
     for (int j = t; j < mine; j += 128) {
       float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
-      float M = -INFINITY;
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
         mv[s2] = -INFINITY;
         lv[s2] = 0.f;
         if (s2 < S) {
-          const float* ml = recv + (s2 * rpc + j) * kRowF + D;
-          mv[s2] = ml[0];
-          lv[s2] = ml[1];
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(part + (static_cast<size_t>(s2) * BM + r0 + j) * kRowF + D));
+          mv[s2] = ml.x;
+          lv[s2] = ml.y;
         }
       }
+      float M = -INFINITY;
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
         if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
@@ -266,12 +259,13 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       float4 x[kAttnMaxSplits];
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-        if (s2 < S) x[s2] = *reinterpret_cast<const float4*>(recv + (s2 * rpc + j) * kRowF + ch * 4);
+        if (s2 < S && wts[j * kAttnMaxSplits + s2] != 0.f)
+          x[s2] = __ldcg(reinterpret_cast<const float4*>(part + (static_cast<size_t>(s2) * BM + r0 + j) * kRowF + ch * 4));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-        if (s2 < S) {
-          const float w = wts[j * kAttnMaxSplits + s2];
+        const float w = s2 < S ? wts[j * kAttnMaxSplits + s2] : 0.f;
+        if (w != 0.f) {
           acc.x = fmaf(w, x[s2].x, acc.x);
           acc.y = fmaf(w, x[s2].y, acc.y);
           acc.z = fmaf(w, x[s2].z, acc.z);

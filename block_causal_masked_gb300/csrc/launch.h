@@ -22,6 +22,8 @@ struct AttnParams {
   const void* q;          // bf16 [N, n_q, Hq, D]
   void* o;                // bf16 [N, n_q, Hq, D]
   float* lse;             // fp32 [N, Hq, n_q] or null
+  float* part;            // fp32 [Hkv, m_tiles, splits, BM, D + 4] split partials (splits > 1)
+  int m_tiles;
   const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
   const int32_t* k_pos;        // [C] or null
   int32_t* dev_status;

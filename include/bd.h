@@ -117,9 +117,9 @@ typedef struct bd_rope {
  *                block_start[n_blocks] = n_q; or NULL for uniform blocks of
  *                block_size positions (the last one ragged)
  *   sm_scale     0 -> D^-1/2
- *   num_splits   KV splits (1..16): the CTAs of one thread-block cluster, merged
- *                on chip; 0 -> chosen by the library.  Needs no workspace
- *                (bd_attn_workspace_size returns 0; workspace may be NULL)
+ *   num_splits   KV splits (1..16): the CTAs of one thread-block cluster, whose
+ *                partial rows meet in the workspace (in L2); 0 -> chosen by the
+ *                library.  With one split no workspace is needed (NULL is fine)
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= n_q; 0 <= C; kv_stride >= C + n_q.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_attn_args {

@@ -81,6 +81,7 @@ def _attn(**kw):
 @pytest.mark.parametrize("kw,want", [
     (dict(q=None), 1), (dict(n_q=0), 1), (dict(C=-1), 1), (dict(kv_stride=50), 1), (dict(block_size=0), 1),
     (dict(D=96), 2), (dict(Hq=5), 2), (dict(q=FAKE + 8), 2), (dict(o=FAKE + 2), 2), (dict(num_splits=17), 1),
+    (dict(num_splits=4), 3),  # split partials need a workspace, none given
 ])
 def test_attention_argument_errors_on_host(kw, want):
     a = _attn(**kw)
@@ -98,8 +99,8 @@ def test_fork_argument_errors_on_host():
 
 
 def test_workspace_sizes_are_host_arithmetic():
-    # attention merges its KV splits on chip (cluster shared memory): no workspace
-    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 0
+    # split partials: Hkv * row tiles * splits * 128 rows * (D + 4) floats; none with one split
+    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 2 * 1 * 4 * 128 * (128 + 4) * 4
     assert bd.lib().bd_attn_workspace_size(_attn(num_splits=1)) == 0
     u = bd.bd_unmask_args()
     u.R, u.V, u.n_pos, u.n_blocks, u.logits_ld, u.min_den, u.add_den, u.act_den = 32, 151936, 33, 1, 151936, 4, 2, 20
