@@ -180,20 +180,22 @@ template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
                               float l_run) {
   using L = Layout<D>;
-  constexpr int kRowF = L::kRowF;
   constexpr int kChunks = D / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 6;
   const int S = p.num_splits;
   const int split = blockIdx.x;
   const int rpc = merge_rows_per_cta(S);
-  // this (row tile, KV head)'s partials: [S][BM][kRowF]
-  float* part = p.part + (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * S * BM * kRowF;
+  // this (row tile, KV head)'s partials, chunk-major so that a warp's 32 rows
+  // are 512 contiguous bytes: [S][kChunks + 1][BM] float4 (chunk kChunks holds
+  // (max, sum, -, -))
+  float4* part = reinterpret_cast<float4*>(p.part) +
+                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * S * (kChunks + 1) * BM;
   if (is_sm) {
     const int quad = warp & 3;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
-      float* dst = part + (static_cast<size_t>(split) * BM + rl) * kRowF;
+      float4* dst = part + static_cast<size_t>(split) * (kChunks + 1) * BM + rl;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       float v[32];
 #pragma unroll
@@ -206,10 +208,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
         }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          __stcg(reinterpret_cast<float4*>(dst + c * 32 + q4 * 4),
-                 make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+          __stcg(dst + (c * 8 + q4) * BM, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
       }
-      __stcg(reinterpret_cast<float4*>(dst + D), make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
+      __stcg(dst + kChunks * BM, make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
     }
   }
   cluster_arrive();  // release: this split's rows are written
@@ -229,7 +230,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
         mv[s2] = -INFINITY;
         lv[s2] = 0.f;
         if (s2 < S) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(part + (static_cast<size_t>(s2) * BM + r0 + j) * kRowF + D));
+          const float4 ml = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + kChunks) * BM + r0 + j);
           mv[s2] = ml.x;
           lv[s2] = ml.y;
         }
@@ -252,15 +253,15 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     }
     named_sync(1, 128);
     for (int it = t; it < mine * kChunks; it += 128) {
-      const int j = it / kChunks;
-      const int ch = it - j * kChunks;
+      const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
+      const int j = it - ch * mine;
       const int grow = m0 + r0 + j;
       if (grow >= p.rows_per_head) continue;
       float4 x[kAttnMaxSplits];
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
         if (s2 < S && wts[j * kAttnMaxSplits + s2] != 0.f)
-          x[s2] = __ldcg(reinterpret_cast<const float4*>(part + (static_cast<size_t>(s2) * BM + r0 + j) * kRowF + ch * 4));
+          x[s2] = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + ch) * BM + r0 + j);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
