@@ -217,87 +217,70 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   cluster_wait();    // acquire: every split's rows are written
   const int r0 = split * rpc;
   const int mine = max(0, min(BM - r0, rpc));
-  const int per_roll = p.n_q * p.G;
-  const int kvh = blockIdx.z;
-  float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][16] normalised weights of the splits
-  float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
-  const int n_items = mine * kChunks;                    // (row, 16-byte chunk) pairs to merge
-  // 256 items per pass: the softmax threads load the O chunks of two items from
-  // every split while warps 0-1 turn the rows' (max, sum) into weights, so a
-  // pass costs one round trip to L2.
-  for (int base = 0; base < n_items; base += 256) {
-    float4 xa[kAttnMaxSplits], xb[kAttnMaxSplits];
+  if (is_sm) {
     const int t = threadIdx.x - 64;
-    const int ita = base + t, itb = base + t + 128;
-    auto row_of = [&](int it) { return it - (it / mine) * mine; };
-    auto valid_item = [&](int it) { return it < n_items && m0 + r0 + row_of(it) < p.rows_per_head; };
-    if (is_sm) {
+    const int per_roll = p.n_q * p.G;
+    const int kvh = blockIdx.z;
+    float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][16] weights of the splits
+    float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
+    for (int j = t; j < mine; j += 128) {
+      float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
 #pragma unroll
       for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-        if (s2 < S && valid_item(ita))
-          xa[s2] = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + ita / mine) * BM + r0 + row_of(ita));
-        if (s2 < S && valid_item(itb))
-          xb[s2] = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + itb / mine) * BM + r0 + row_of(itb));
-      }
-    } else if (base == 0 && warp < 2) {
-      for (int j = threadIdx.x; j < mine; j += 64) {
-        float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-          mv[s2] = -INFINITY;
-          lv[s2] = 0.f;
-          if (s2 < S) {
-            const float4 ml = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + kChunks) * BM + r0 + j);
-            mv[s2] = ml.x;
-            lv[s2] = ml.y;
-          }
+        mv[s2] = -INFINITY;
+        lv[s2] = 0.f;
+        if (s2 < S) {
+          const float4 ml = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + kChunks) * BM + r0 + j);
+          mv[s2] = ml.x;
+          lv[s2] = ml.y;
         }
-        float M = -INFINITY;
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-          if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
-        float Ls = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-          mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
-          Ls += lv[s2] * mv[s2];
-        }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) wts[j * kAttnMaxSplits + s2] = mv[s2] * inv;
-        lse_row[j] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
+      float Ls = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+        mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
+        Ls += lv[s2] * mv[s2];
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (s2 < S) wts[j * kAttnMaxSplits + s2] = mv[s2] * inv;
+      lse_row[j] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
-    __syncthreads();
-    if (is_sm) {
+    named_sync(1, 128);
+    for (int it = t; it < mine * kChunks; it += 128) {
+      const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
+      const int j = it - ch * mine;
+      const int grow = m0 + r0 + j;
+      if (grow >= p.rows_per_head) continue;
+      float4 x[kAttnMaxSplits];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int it = h == 0 ? ita : itb;
-        if (!valid_item(it)) continue;
-        const int j = row_of(it);
-        const int ch = it / mine;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+        if (s2 < S && wts[j * kAttnMaxSplits + s2] != 0.f)
+          x[s2] = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + ch) * BM + r0 + j);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-          const float w = s2 < S ? wts[j * kAttnMaxSplits + s2] : 0.f;
-          if (w != 0.f) {
-            const float4 x = h == 0 ? xa[s2] : xb[s2];
-            acc.x = fmaf(w, x.x, acc.x);
-            acc.y = fmaf(w, x.y, acc.y);
-            acc.z = fmaf(w, x.z, acc.z);
-            acc.w = fmaf(w, x.w, acc.w);
-          }
+      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+        const float w = s2 < S ? wts[j * kAttnMaxSplits + s2] : 0.f;
+        if (w != 0.f) {
+          acc.x = fmaf(w, x[s2].x, acc.x);
+          acc.y = fmaf(w, x[s2].y, acc.y);
+          acc.z = fmaf(w, x[s2].z, acc.z);
+          acc.w = fmaf(w, x[s2].w, acc.w);
         }
-        const int grow = m0 + r0 + j;
-        const int r_row = grow / per_roll;
-        const int rem = grow - r_row * per_roll;
-        const int i_row = rem / p.G;
-        const int qhead = kvh * p.G + (rem - i_row * p.G);
-        const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
-            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-        if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
       }
+      const int r_row = grow / per_roll;
+      const int rem = grow - r_row * per_roll;
+      const int i_row = rem / p.G;
+      const int qhead = kvh * p.G + (rem - i_row * p.G);
+      const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
     }
   }
 }
