@@ -321,11 +321,29 @@ def e2e_measure(rd, inp, steps: int):
     return {"value": toks / total, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def aggregate(seconds: float, tokens: float, world: int, device="cpu"):
+    """Whole-job totals over the ranks: the slowest rank's timed seconds and the
+    sum of the committed tokens (each rank decodes its own independent request)."""
+    if world == 1:
+        return seconds, tokens
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    c = torch.tensor([tokens], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(c)
+    return float(t[0]), float(c[0])
+
+
+def replica_seed(rank: int) -> int:
+    """Seed of the request rank `rank` decodes (independent inputs per replica)."""
+    return W.seed + 100 * rank
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     device = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
-    inp = make_inputs(W.seed + 100 * rank)
+    inp = make_inputs(replica_seed(rank))
     rd = GpuRound(inp, device)
     rd.capture()
     clocks = Clocks(local_rank)
@@ -345,14 +363,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_s = sum(steps_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        c = torch.tensor([committed], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(c)
-        total_s, committed_all = float(t[0]), float(c[0])
-    else:
-        committed_all = committed
+    total_s, committed_all = aggregate(total_s, committed, world, device)
     e2e = e2e_measure(rd, inp, max(3, args.steps // 2))
     if rank != 0:
         return None
