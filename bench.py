@@ -222,7 +222,7 @@ class Clocks:
                  "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -245,6 +245,20 @@ class Clocks:
         reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 3 + i and r[3 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+def attn_traffic():
+    """DRAM bytes per attention launch from the committed ncu capture, if the
+    attention kernel's source is still the one that capture measured (else None)."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "attn_kernel_traffic.json")))
+        h = hashlib.sha256()
+        for f in rec["files"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+    except (OSError, ValueError, KeyError):
+        return None
 
 
 def measured_peaks():
@@ -391,7 +405,7 @@ def run_gpu(args, rank, world, local_rank):
                    "planted_accept_len": inp["planted_accept"], "attn_splits": splits},
         "roofline": {"bound": "hbm", "kernel": "attn_kernel (bd_block_causal_attn)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": "measured" if peaks else "fallback", "traffic": None,
+                     "peak_source": "measured" if peaks else "fallback", "traffic": attn_traffic(),
                      "alg_bytes_per_launch": attn_bytes, "avg_launch_us": attn_launch_s * 1e6,
                      "unmask": {"alg_bytes": alg["unmask_bytes"], "us": unmask_s * 1e6,
                                 "achieved_gbs": alg["unmask_bytes"] / unmask_s / 1e9,
