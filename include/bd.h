@@ -326,7 +326,7 @@ bd_status bd_unmask_step_noalloc(const bd_unmask_args* a, void* stream);
  *                 logits_ld, or NULL for greedy
  *   accepted_len  int32 [n_seq] out: slots committed this round, bonus included
  *   bonus, bonus_pos  int32 [n_seq] out
- * Supported: L <= 1024, n_seq <= 1024, n_seq * n_rows <= 16384.
+ * Supported: L <= 1024, n_seq <= 1024, n_seq * n_rows <= 65535.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_verify_args {
   int32_t n_seq;
