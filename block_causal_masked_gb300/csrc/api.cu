@@ -140,8 +140,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
     splits = s < 1 ? 1 : static_cast<int>(s);
   }
   pl->splits = splits;
-  // split partials: [Hkv, m_tiles, splits, 128 rows, D + 4 floats]
-  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * splits * kAttnBM * (d.D + 4) * 4 : 0;
+  // split partials: Hkv * m_tiles blocks of attn_part_float4s(splits, D) float4
+  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * attn_part_float4s(splits, d.D) * 16 : 0;
   return BD_OK;
 }
 

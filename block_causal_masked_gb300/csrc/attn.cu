@@ -54,7 +54,7 @@ struct TileEntry {
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, NUM_BARS = 16
+  KREADY = 13, DRAIN = 15, MERGE = 16, NUM_BARS = 17
 };
 
 template <int D>
@@ -69,12 +69,11 @@ struct Layout {
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kMisc = kBar + NUM_BARS * 8;
   static constexpr int kEnd = kMisc + 64;
-  // cluster merge, over the K / V rings and P, idle by then: received rows of
-  // D + 4 floats (unnormalised O, then max and sum), S slots of rpc rows
-  static constexpr int kRowF = D + 4;
+  // split-KV merge, over the K / V rings and P (idle by then): the S slices of
+  // this CTA's rows, S * r <= BM + 2 * S rows of D / 4 + 1 float4 each, then
+  // the weights [S][r] and LSE [r] of those rows
   static constexpr int kRecv = kK;
-  // S * merge_rows_per_cta(S) <= BM + 2 * S rows are received
-  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * kRowF * 4;  // [rpc][16] weights, [rpc] LSE
+  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * (D / 4 + 1) * 16;
   static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
@@ -165,37 +164,35 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
   return {tr.r_first + k / tr.n_priv, (k % tr.n_priv) * BN};
 }
 
-// Rows of the tile each CTA of a cluster of S merges (kept even).
-__host__ __device__ __forceinline__ int merge_rows_per_cta(int S) { return ((BM + S - 1) / S + 1) & ~1; }
-
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
-// every thread of every CTA of the cluster:
+// every thread of every CTA of the cluster once its own K/V range is done:
 //   1. each softmax thread writes its row -- unnormalised O from TMEM, then
-//      (running max, sum) -- to the workspace (slot of this split);
-//   2. cluster barrier (release / acquire): every split's rows are visible;
-//   3. CTA q merges rows [q * rpc, (q + 1) * rpc) from the S splits
-//      (M = max m_s, L = sum l_s 2^(m_s - M), O = sum O_s 2^(m_s - M) / L),
-//      reading them through L2, and stores them.
+//      (running max, sum) -- into the workspace slice of the CTA that owns it;
+//   2. cluster barrier (release / acquire): every split's slices are written;
+//   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S slices into
+//      shared memory with bulk copies on one mbarrier, the softmax threads form
+//      the weights 2^(m_s - M) / L once per row (M = max m_s, L = sum l_s
+//      2^(m_s - M)) and store O = sum w_s O_s in bf16 and LSE = (M + log2 L) ln 2.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
-                              float l_run) {
+                              float l_run, uint64_t* bar, volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int kChunks = D / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 6;
   const int S = p.num_splits;
   const int split = blockIdx.x;
-  const int rpc = merge_rows_per_cta(S);
-  // this (row tile, KV head)'s partials, chunk-major so that a warp's 32 rows
-  // are 512 contiguous bytes: [S][kChunks + 1][BM] float4 (chunk kChunks holds
-  // (max, sum, -, -))
+  const int rpc = attn_merge_rows(S);
+  const int slice = (kChunks + 1) * rpc;  // float4 of one (split, owner) slice
+  int32_t* ds = p.dev_status;
   float4* part = reinterpret_cast<float4*>(p.part) +
-                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * S * (kChunks + 1) * BM;
+                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * attn_part_float4s(S, D);
   if (is_sm) {
     const int quad = warp & 3;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
-      float4* dst = part + static_cast<size_t>(split) * (kChunks + 1) * BM + rl;
+      const int q = rl / rpc;
+      float4* dst = part + static_cast<size_t>(split * S + q) * slice + (rl - q * rpc);
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
       float v[32];
 #pragma unroll
@@ -208,80 +205,87 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
         }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          __stcg(dst + (c * 8 + q4) * BM, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+          __stcg(dst + (c * 8 + q4) * rpc, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
       }
-      __stcg(dst + kChunks * BM, make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
+      __stcg(dst + kChunks * rpc, make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
+      fence_proxy_async_global();
     }
   }
-  cluster_arrive();  // release: this split's rows are written
-  cluster_wait();    // acquire: every split's rows are written
+  cluster_arrive();  // release: this split's slices are written
+  cluster_wait();    // acquire: every split's slices are written
   const int r0 = split * rpc;
-  const int mine = max(0, min(BM - r0, rpc));
-  if (is_sm) {
-    const int t = threadIdx.x - 64;
-    const int per_roll = p.n_q * p.G;
-    const int kvh = blockIdx.z;
-    float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [rpc][16] weights of the splits
-    float* lse_row = wts + rpc * kAttnMaxSplits;           // [rpc]
-    for (int j = t; j < mine; j += 128) {
-      float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
+  const int mine = max(0, min(min(BM - r0, rpc), p.rows_per_head - m0 - r0));
+  if (mine == 0) return;
+  float4* recv = reinterpret_cast<float4*>(smem + L::kRecv);  // [S][kChunks + 1][rpc]
+  if (threadIdx.x == 0) {
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(S * slice * 16));
+    for (int s2 = 0; s2 < S; ++s2)
+      bulk_load(recv + s2 * slice, part + static_cast<size_t>(s2 * S + split) * slice, slice * 16, bar);
+    // the copies land before this thread reaches the CTA's final barrier
+    mbar_drain(bar, 0, ds);
+  }
+  if (!is_sm) return;
+  const int t = threadIdx.x - 64;
+  const int per_roll = p.n_q * p.G;
+  const int kvh = blockIdx.z;
+  float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [S][rpc] weights of the splits
+  float* lse_row = wts + S * rpc;                        // [rpc]
+  const bool ok = all_lanes(mbar_wait(bar, 0, abort_flag, ds));
+  if (ok && t < mine) {
+    float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
 #pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-        mv[s2] = -INFINITY;
-        lv[s2] = 0.f;
-        if (s2 < S) {
-          const float4 ml = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + kChunks) * BM + r0 + j);
-          mv[s2] = ml.x;
-          lv[s2] = ml.y;
-        }
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+      mv[s2] = -INFINITY;
+      lv[s2] = 0.f;
+      if (s2 < S) {
+        const float4 ml = recv[s2 * slice + kChunks * rpc + t];
+        mv[s2] = ml.x;
+        lv[s2] = ml.y;
       }
-      float M = -INFINITY;
-#pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-        if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
-      float Ls = 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-        mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
-        Ls += lv[s2] * mv[s2];
-      }
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-        if (s2 < S) wts[j * kAttnMaxSplits + s2] = mv[s2] * inv;
-      lse_row[j] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
-    named_sync(1, 128);
-    for (int it = t; it < mine * kChunks; it += 128) {
-      const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
-      const int j = it - ch * mine;
-      const int grow = m0 + r0 + j;
-      if (grow >= p.rows_per_head) continue;
-      float4 x[kAttnMaxSplits];
+    float M = -INFINITY;
 #pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-        if (s2 < S && wts[j * kAttnMaxSplits + s2] != 0.f)
-          x[s2] = __ldcg(part + (static_cast<size_t>(s2) * (kChunks + 1) + ch) * BM + r0 + j);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+      if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
+    float Ls = 0.f;
 #pragma unroll
-      for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-        const float w = s2 < S ? wts[j * kAttnMaxSplits + s2] : 0.f;
-        if (w != 0.f) {
-          acc.x = fmaf(w, x[s2].x, acc.x);
-          acc.y = fmaf(w, x[s2].y, acc.y);
-          acc.z = fmaf(w, x[s2].z, acc.z);
-          acc.w = fmaf(w, x[s2].w, acc.w);
-        }
-      }
-      const int r_row = grow / per_roll;
-      const int rem = grow - r_row * per_roll;
-      const int i_row = rem / p.G;
-      const int qhead = kvh * p.G + (rem - i_row * p.G);
-      const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
-          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+      mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
+      Ls += lv[s2] * mv[s2];
     }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+      if (s2 < S) wts[s2 * rpc + t] = mv[s2] * inv;
+    lse_row[t] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+  }
+  named_sync(1, 128);
+  if (!ok) return;
+  for (int it = t; it < mine * kChunks; it += 128) {
+    const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
+    const int j = it - ch * mine;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+      if (s2 < S) {
+        const float w = wts[s2 * rpc + j];
+        const float4 x = recv[s2 * slice + ch * rpc + j];
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+    }
+    const int grow = m0 + r0 + j;
+    const int r_row = grow / per_roll;
+    const int rem = grow - r_row * per_roll;
+    const int i_row = rem / p.G;
+    const int qhead = kvh * p.G + (rem - i_row * p.G);
+    const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
   }
 }
 
@@ -352,6 +356,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     mbar_init(&bars[KREADY + 0], 64);
     mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
+    mbar_init(&bars[MERGE], 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
   }
 
-  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run);
+  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run, &bars[MERGE], abort_flag);
 
   tc_fence_before();
   __syncthreads();

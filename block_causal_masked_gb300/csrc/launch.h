@@ -15,6 +15,16 @@ constexpr int kAttnBN = 128;        // keys per K/V tile
 constexpr int kAttnMaxTiles = 4096; // K/V tiles of one (row tile, KV head) before splitting
 constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 
+// Split-KV merge: CTA q of a cluster of S merges packed rows [q * r, (q + 1) * r)
+// of the tile, r = ceil(128 / S) rounded up to even.
+__host__ __device__ constexpr int attn_merge_rows(int S) { return ((kAttnBM + S - 1) / S + 1) & ~1; }
+// fp32 partials of one (KV head, row tile): [S splits][S owners][D / 4 + 1][r]
+// float4 -- unnormalised O in D / 4 chunks of 4, then (max, sum, -, -) -- so
+// that the slice one split hands one owner is contiguous.
+__host__ __device__ constexpr long long attn_part_float4s(int S, int D) {
+  return static_cast<long long>(S) * S * (D / 4 + 1) * attn_merge_rows(S);
+}
+
 // Everything the attention kernels need, in the fork's terms: plain attention is
 // the fork with N = 1, the prefix = rows [0, C) of K/V and the private rows =
 // the active rows [C, C + n_q) (priv_len = 0).
@@ -22,7 +32,7 @@ struct AttnParams {
   const void* q;          // bf16 [N, n_q, Hq, D]
   void* o;                // bf16 [N, n_q, Hq, D]
   float* lse;             // fp32 [N, Hq, n_q] or null
-  float* part;            // fp32 [Hkv, m_tiles, splits, BM, D + 4] split partials (splits > 1)
+  float* part;            // split partials (splits > 1): [Hkv, m_tiles] blocks of attn_part_float4s float4
   int m_tiles;
   const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
   const int32_t* k_pos;        // [C] or null

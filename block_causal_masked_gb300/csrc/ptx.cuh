@@ -122,28 +122,20 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
-// Shared::cluster address of the same shared-memory location in CTA `rank` of
-// this cluster.
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
-// shared::cluster address, completing `bytes` transactions on the mbarrier at
-// the shared::cluster address `mbar` (in the destination CTA).
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst),
-               "r"(src), "r"(bytes), "r"(mbar)
+// Bulk copy (no tensor map) of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing `bytes`
+// transactions on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
 }
 
-// 16-byte store to a shared::cluster address (possibly another CTA's shared memory).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+// Orders generic-proxy global-memory accesses before later async-proxy ones
+// (bulk copies) and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Cluster-wide barrier, split into arrive and wait (every thread of every CTA

@@ -99,8 +99,8 @@ def test_fork_argument_errors_on_host():
 
 
 def test_workspace_sizes_are_host_arithmetic():
-    # split partials: Hkv * row tiles * splits * 128 rows * (D + 4) floats; none with one split
-    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 2 * 1 * 4 * 128 * (128 + 4) * 4
+    # split partials: Hkv * row tiles * S * S owner slices of (D/4 + 1) * r float4, r = 32 rows at S = 4; none with one split
+    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 2 * 1 * 4 * 4 * (128 // 4 + 1) * 32 * 16
     assert bd.lib().bd_attn_workspace_size(_attn(num_splits=1)) == 0
     u = bd.bd_unmask_args()
     u.R, u.V, u.n_pos, u.n_blocks, u.logits_ld, u.min_den, u.add_den, u.act_den = 32, 151936, 33, 1, 151936, 4, 2, 20
