@@ -45,6 +45,10 @@ constexpr int BN = kAttnBN;
 constexpr int kStages = 2;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
+// warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax, then 2 RoPE warps
+constexpr int kSmWarps = 8;
+constexpr int kThreadsPlain = 32 * (2 + kSmWarps);
+constexpr int kThreadsRope = kThreadsPlain + 64;
 
 struct TileEntry {
   int rollout;  // -1: shared prefix tile
@@ -68,7 +72,10 @@ struct Layout {
   static constexpr int kP = kV + kStages * kKVBytes;
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kMisc = kBar + NUM_BARS * 8;
-  static constexpr int kEnd = kMisc + 64;
+  // the two halves of a row trade tile maxima ([2 parities][2 halves][BM])
+  // and final sums ([2 halves][BM])
+  static constexpr int kXch = kMisc + 64;
+  static constexpr int kEnd = kXch + 6 * BM * 4;
   // split-KV merge, over the K / V rings and P (idle by then): the S slices of
   // this CTA's rows, S * r <= BM + 2 * S rows of D / 4 + 1 float4 each, then
   // the weights [S][r] and LSE [r] of those rows
@@ -166,8 +173,9 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster once its own K/V range is done:
-//   1. each softmax thread writes its row -- unnormalised O from TMEM, then
-//      (running max, sum) -- into the workspace slice of the CTA that owns it;
+//   1. each softmax thread writes its half of its row -- unnormalised O from
+//      TMEM, then (running max, sum) -- into the workspace slice of the CTA
+//      that owns the row;
 //   2. cluster barrier (release / acquire): every split's slices are written;
 //   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S slices into
 //      shared memory with bulk copies on one mbarrier, the softmax threads form
@@ -175,11 +183,12 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 //      2^(m_s - M)) and store O = sum w_s O_s in bf16 and LSE = (M + log2 L) ln 2.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
-                              float l_run, uint64_t* bar, volatile int* abort_flag) {
+                              float l_tot, uint64_t* bar, volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int kChunks = D / 4;
+  constexpr int kThreads = 32 * kSmWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool is_sm = warp >= 2 && warp < 6;
+  const bool is_sm = warp >= 2 && warp < 2 + kSmWarps;
   const int S = p.num_splits;
   const int split = blockIdx.x;
   const int rpc = attn_merge_rows(S);
@@ -189,25 +198,27 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
                  (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * attn_part_float4s(S, D);
   if (is_sm) {
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
       const int q = rl / rpc;
       float4* dst = part + static_cast<size_t>(split * S + q) * slice + (rl - q * rpc);
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + 2 * BN + half * (D / 2);
       float v[32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         if (have_o) {
-          tmem_ld32(lane_base + 2 * BN + c * 32, v);
+          tmem_ld32(lane_base + c * 32, v);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          __stcg(dst + (c * 8 + q4) * rpc, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+          __stcg(dst + (half * (kChunks / 2) + c * 8 + q4) * rpc,
+                 make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
       }
-      __stcg(dst + kChunks * rpc, make_float4(m_run, have_o ? l_run : 0.f, 0.f, 0.f));
+      if (half == 0) __stcg(dst + kChunks * rpc, make_float4(m_run, have_o ? l_tot : 0.f, 0.f, 0.f));
       fence_proxy_async_global();
     }
   }
@@ -260,9 +271,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       if (s2 < S) wts[s2 * rpc + t] = mv[s2] * inv;
     lse_row[t] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
   }
-  named_sync(1, 128);
+  named_sync(1, kThreads);
   if (!ok) return;
-  for (int it = t; it < mine * kChunks; it += 128) {
+  for (int it = t; it < mine * kChunks; it += kThreads) {
     const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
     const int j = it - ch * mine;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -290,7 +301,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
 }
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
+__global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -348,9 +359,9 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     mbar_init(&bars[KVEMPTY + 1], 1);
     mbar_init(&bars[SFULL + 0], 1);
     mbar_init(&bars[SFULL + 1], 1);
-    mbar_init(&bars[SFREE + 0], 128);
-    mbar_init(&bars[SFREE + 1], 128);
-    mbar_init(&bars[PFULL], 128);
+    mbar_init(&bars[SFREE + 0], 32 * kSmWarps);
+    mbar_init(&bars[SFREE + 1], 32 * kSmWarps);
+    mbar_init(&bars[PFULL], 32 * kSmWarps);
     mbar_init(&bars[ODONE], 1);
     mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
     mbar_init(&bars[KREADY + 0], 64);
@@ -456,10 +467,16 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       mma_commit(&bars[DRAIN]);
       mbar_drain(&bars[DRAIN], 0, ds);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kSmWarps) {
     // ---------------------------------------------------------------- softmax rows
+    // Two warps per TMEM lane quadrant: warp 2 + 4h + q holds the rows of lanes
+    // [32q, 32q + 32) and key columns [h BN/2, (h+1) BN/2) of each S tile (and
+    // O columns [h D/2, (h+1) D/2)); the halves of a row trade their tile maxima
+    // through shared memory and add their sums at the end.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int rl = quad * 32 + lane;  // TMEM lane = packed row within the tile
+    const int c0 = half * (BN / 2);   // first key column of this half
     const int row = m0 + rl;
     const int per_roll = p.n_q * p.G;
     const bool valid = row < p.rows_per_head;
@@ -472,7 +489,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
     const int qhead = kvh * p.G + g;
     const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-    if (!p.q_tma) {  // GQA group that does not divide 128: rows gathered by the threads
+    if (!p.q_tma && half == 0) {  // GQA group that does not divide 128: rows gathered by the threads
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + orow * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
@@ -486,42 +503,52 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     const int lim_priv = valid ? p.priv_len + block_end_of(p, i_row) : 0;
     const bool warp_active = __any_sync(0xffffffffu, valid);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + L::kXch);
     bool ok = true;
     float v[32];
+    // Every named barrier below is reached by all 256 softmax threads the same
+    // number of times (nt + 1), whatever the waits return.
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
-      ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds));
-      if (!ok) break;
-      tc_fence_after();
-      const TileEntry te = tile_at(p, tr, t);
-      int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
-      if (!valid) lim = 0;
-      const int nv = max(0, min(BN, lim - te.key0));
-      // the whole S row in registers: one TMEM round trip, then S is free again
-      float sv[BN];
+      if (ok) ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds));
+      // this half of the S row in registers: one TMEM round trip, then S is free again
+      float sv[BN / 2];
       float mx = -INFINITY;
-      if (warp_active) {
-        tmem_ld128(lane_base + s * BN, sv);
-        if (!__all_sync(0xffffffffu, nv == BN)) {
+      int nv = 0;
+      if (ok) {
+        tc_fence_after();
+        const TileEntry te = tile_at(p, tr, t);
+        int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
+        if (!valid) lim = 0;
+        nv = max(0, min(BN, lim - te.key0));
+        if (warp_active) {
+          tmem_ld64(lane_base + s * BN + c0, sv);
+          if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+            for (int j = 0; j < BN / 2; ++j)
+              if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+          }
+          float m8[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+#pragma unroll
+          for (int j = 8; j < BN / 2; ++j) m8[j & 7] = fmaxf(m8[j & 7], sv[j]);
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
-        float m8[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = sv[q];
-#pragma unroll
-        for (int j = 8; j < BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], sv[j]);
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        tc_fence_before();
+        mbar_arrive(&bars[SFREE + s]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars[SFREE + s]);
+      xch[(s * 2 + half) * BM + rl] = mx;
+      named_sync(2, 32 * kSmWarps);
+      mx = fmaxf(mx, xch[(s * 2 + (half ^ 1)) * BM + rl]);
+      if (!ok) continue;
       const float m_tile = nv > 0 ? mx * p.scale_log2 : -INFINITY;
       if (t > 0) {
         ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
-        if (!ok) break;
+        if (!ok) continue;
         tc_fence_after();
       }
+      // both halves see the same m_tile and m_run, so they take the same decision
       const bool grow = m_tile > -INFINITY && (m_run == -INFINITY || m_tile > m_run + kRescaleLog2);
       float alpha = 1.f;
       if (grow) {
@@ -531,11 +558,12 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       }
       if (warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(lane_base + 2 * BN + c * 32, v);
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t oa = lane_base + 2 * BN + half * (D / 2) + c * 32;
+          tmem_ld32(oa, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= alpha;
-          tmem_st32(lane_base + 2 * BN + c * 32, v);
+          tmem_st32(oa, v);
         }
       }
       if (warp_active) {
@@ -543,7 +571,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
         const float mneg = m_run == -INFINITY ? 0.f : -m_run;
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -555,7 +583,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
           }
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
-            *reinterpret_cast<uint4*>(smem + L::kP + sw128_offset(rl, c * 32 + qq * 8, BM)) =
+            *reinterpret_cast<uint4*>(smem + L::kP + sw128_offset(rl, c0 + c * 32 + qq * 8, BM)) =
                 make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
@@ -568,19 +596,23 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
       tc_fence_after();
     }
     have_o = ok && nt > 0;
+    xch[(4 + half) * BM + rl] = l_run;
+    named_sync(2, 32 * kSmWarps);
+    l_run += xch[(4 + (half ^ 1)) * BM + rl];  // the row's sum over both halves
     if (p.num_splits == 1) {
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       if (warp_active) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = half * (D / 2) + c * 32;
           if (have_o) {
-            tmem_ld32(lane_base + 2 * BN + c * 32, v);
+            tmem_ld32(lane_base + 2 * BN + col, v);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
           }
           if (!valid) continue;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
             dst[qq] = make_uint4(pack_bf16x2(v[8 * qq + 0] * inv_l, v[8 * qq + 1] * inv_l),
@@ -589,13 +621,13 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                                  pack_bf16x2(v[8 * qq + 6] * inv_l, v[8 * qq + 7] * inv_l));
         }
       }
-      if (valid && p.lse)
+      if (valid && half == 0 && p.lse)
         p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
             l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
   } else if (ROPE) {
     // ---------------------------------------------------------------- RoPE on staged prefix keys
-    const int kr0 = threadIdx.x - 192;  // this thread rotates key rows kr0 and kr0 + 64 of the tile
+    const int kr0 = threadIdx.x - 32 * (2 + kSmWarps);  // this thread rotates key rows kr0 and kr0 + 64 of the tile
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
       if (!mbar_wait(&bars[KFULL + s], (t >> 1) & 1, abort_flag, ds)) break;
@@ -656,7 +688,7 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
-  cfg.blockDim = dim3(ROPE ? 256 : 192);
+  cfg.blockDim = dim3(ROPE ? kThreadsRope : kThreadsPlain);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   for (;;) {
