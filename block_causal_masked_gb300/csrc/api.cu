@@ -140,8 +140,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
     splits = s < 1 ? 1 : static_cast<int>(s);
   }
   pl->splits = splits;
-  // split partials: Hkv * m_tiles blocks of attn_part_float4s(splits, D) float4
-  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * attn_part_float4s(splits, d.D) * 16 : 0;
+  // split partials: Hkv * m_tiles blocks of attn_part_bytes(splits, D)
+  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * attn_part_bytes(splits, d.D) : 0;
   return BD_OK;
 }
 
@@ -162,7 +162,7 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.q = d.q;
   p.o = d.o;
   p.lse = d.lse;
-  p.part = pl.splits > 1 ? static_cast<float*>(d.ws) : nullptr;
+  p.part = pl.splits > 1 ? d.ws : nullptr;
   p.m_tiles = pl.m_tiles;
   p.block_start = d.block_start;
   p.k_pos = d.rope.enabled ? d.rope.k_pos : nullptr;

@@ -58,7 +58,7 @@ struct TileEntry {
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, MERGE = 16, NUM_BARS = 17
+  KREADY = 13, DRAIN = 15, MERGE_ML = 16, MERGE_O = 17, NUM_BARS = 18
 };
 
 template <int D>
@@ -77,10 +77,11 @@ struct Layout {
   static constexpr int kXch = kMisc + 64;
   static constexpr int kEnd = kXch + 6 * BM * 4;
   // split-KV merge, over the K / V rings and P (idle by then): the S slices of
-  // this CTA's rows, S * r <= BM + 2 * S rows of D / 4 + 1 float4 each, then
+  // this CTA's rows (S * r <= BM + 2 * S rows: bf16 O, then (max, sum)), then
   // the weights [S][r] and LSE [r] of those rows
   static constexpr int kRecv = kK;
-  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * (D / 4 + 1) * 16;
+  static constexpr int kRecvML = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
+  static constexpr int kWts = kRecvML + (BM + 2 * kAttnMaxSplits) * 8;
   static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
@@ -173,37 +174,41 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster once its own K/V range is done:
-//   1. each softmax thread writes its half of its row -- unnormalised O from
-//      TMEM, then (running max, sum) -- into the workspace slice of the CTA
+//   1. each softmax thread writes its half of its row -- O / l in bf16 from
+//      TMEM, and (running max m, sum l) -- into the workspace slices of the CTA
 //      that owns the row;
 //   2. cluster barrier (release / acquire): every split's slices are written;
-//   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S slices into
-//      shared memory with bulk copies on one mbarrier, the softmax threads form
-//      the weights 2^(m_s - M) / L once per row (M = max m_s, L = sum l_s
-//      2^(m_s - M)) and store O = sum w_s O_s in bf16 and LSE = (M + log2 L) ln 2.
+//   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S (m, l)
+//      slices and then its S O slices into shared memory with bulk copies (one
+//      mbarrier each); while the O slices travel the softmax threads form the
+//      weights l_s 2^(m_s - M) / L once per row (M = max m_s, L = sum l_s
+//      2^(m_s - M)), then store O = sum w_s O_s in bf16 and LSE = (M + log2 L) ln 2.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
-                              float l_tot, uint64_t* bar, volatile int* abort_flag) {
+                              float l_tot, uint64_t* bars, volatile int* abort_flag) {
   using L = Layout<D>;
-  constexpr int kChunks = D / 4;
+  constexpr int kCh = D / 8;  // bf16x8 chunks of a row
   constexpr int kThreads = 32 * kSmWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_sm = warp >= 2 && warp < 2 + kSmWarps;
   const int S = p.num_splits;
   const int split = blockIdx.x;
   const int rpc = attn_merge_rows(S);
-  const int slice = (kChunks + 1) * rpc;  // float4 of one (split, owner) slice
   int32_t* ds = p.dev_status;
-  float4* part = reinterpret_cast<float4*>(p.part) +
-                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * attn_part_float4s(S, D);
+  uint8_t* blk = static_cast<uint8_t*>(p.part) +
+                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * attn_part_bytes(S, D);
+  float2* part_ml = reinterpret_cast<float2*>(blk);                        // [S][S][rpc]
+  uint4* part_o = reinterpret_cast<uint4*>(blk + attn_part_ml_bytes(S));  // [S][S][kCh][rpc]
   if (is_sm) {
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
       const int q = rl / rpc;
-      float4* dst = part + static_cast<size_t>(split * S + q) * slice + (rl - q * rpc);
+      const int r = rl - q * rpc;
+      uint4* dst = part_o + static_cast<size_t>(split * S + q) * kCh * rpc + r;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + 2 * BN + half * (D / 2);
+      const float inv_l = have_o && l_tot > 0.f ? 1.f / l_tot : 0.f;
       float v[32];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -214,11 +219,15 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          __stcg(dst + (half * (kChunks / 2) + c * 8 + q4) * rpc,
-                 make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+        for (int q8 = 0; q8 < 4; ++q8)
+          __stcg(dst + (half * (kCh / 2) + c * 4 + q8) * rpc,
+                 make_uint4(pack_bf16x2(v[8 * q8 + 0] * inv_l, v[8 * q8 + 1] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 2] * inv_l, v[8 * q8 + 3] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 4] * inv_l, v[8 * q8 + 5] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 6] * inv_l, v[8 * q8 + 7] * inv_l)));
       }
-      if (half == 0) __stcg(dst + kChunks * rpc, make_float4(m_run, have_o ? l_tot : 0.f, 0.f, 0.f));
+      if (half == 0)
+        __stcg(part_ml + static_cast<size_t>(split * S + q) * rpc + r, make_float2(m_run, have_o ? l_tot : 0.f));
       fence_proxy_async_global();
     }
   }
@@ -227,14 +236,20 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int r0 = split * rpc;
   const int mine = max(0, min(min(BM - r0, rpc), p.rows_per_head - m0 - r0));
   if (mine == 0) return;
-  float4* recv = reinterpret_cast<float4*>(smem + L::kRecv);  // [S][kChunks + 1][rpc]
+  uint4* recv_o = reinterpret_cast<uint4*>(smem + L::kRecv);      // [S][kCh][rpc]
+  float2* recv_ml = reinterpret_cast<float2*>(smem + L::kRecvML);  // [S][rpc]
   if (threadIdx.x == 0) {
     fence_proxy_async_global();
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(S * slice * 16));
+    mbar_arrive_expect_tx(&bars[MERGE_ML], static_cast<uint32_t>(S * rpc * 8));
     for (int s2 = 0; s2 < S; ++s2)
-      bulk_load(recv + s2 * slice, part + static_cast<size_t>(s2 * S + split) * slice, slice * 16, bar);
+      bulk_load(recv_ml + s2 * rpc, part_ml + static_cast<size_t>(s2 * S + split) * rpc, rpc * 8, &bars[MERGE_ML]);
+    mbar_arrive_expect_tx(&bars[MERGE_O], static_cast<uint32_t>(S * kCh * rpc * 16));
+    for (int s2 = 0; s2 < S; ++s2)
+      bulk_load(recv_o + s2 * kCh * rpc, part_o + static_cast<size_t>(s2 * S + split) * kCh * rpc, kCh * rpc * 16,
+                &bars[MERGE_O]);
     // the copies land before this thread reaches the CTA's final barrier
-    mbar_drain(bar, 0, ds);
+    mbar_drain(&bars[MERGE_ML], 0, ds);
+    mbar_drain(&bars[MERGE_O], 0, ds);
   }
   if (!is_sm) return;
   const int t = threadIdx.x - 64;
@@ -242,50 +257,43 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int kvh = blockIdx.z;
   float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [S][rpc] weights of the splits
   float* lse_row = wts + S * rpc;                        // [rpc]
-  const bool ok = all_lanes(mbar_wait(bar, 0, abort_flag, ds));
-  if (ok && t < mine) {
-    float mv[kAttnMaxSplits], lv[kAttnMaxSplits];
+  bool ok = all_lanes(mbar_wait(&bars[MERGE_ML], 0, abort_flag, ds));
+  if (ok) {
+    // one half-warp per row, lane s2 = split s2 (S <= 16)
+    const int s2 = lane & 15;
+    for (int j = (warp - 2) * 2 + (lane >> 4); j < mine; j += 2 * kSmWarps) {
+      const float2 ml = s2 < S ? recv_ml[s2 * rpc + j] : make_float2(-INFINITY, 0.f);
+      float M = ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
-    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-      mv[s2] = -INFINITY;
-      lv[s2] = 0.f;
-      if (s2 < S) {
-        const float4 ml = recv[s2 * slice + kChunks * rpc + t];
-        mv[s2] = ml.x;
-        lv[s2] = ml.y;
-      }
+      for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float wl = ml.y > 0.f ? ml.y * fast_exp2(ml.x - M) : 0.f;
+      float Ls = wl;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (s2 < S) wts[s2 * rpc + j] = Ls > 0.f ? wl * fast_rcp(Ls) : 0.f;
+      if (s2 == 0) lse_row[j] = Ls > 0.f ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
     }
-    float M = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-      if (lv[s2] > 0.f) M = fmaxf(M, mv[s2]);
-    float Ls = 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-      mv[s2] = lv[s2] > 0.f ? fast_exp2(mv[s2] - M) : 0.f;
-      Ls += lv[s2] * mv[s2];
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-      if (s2 < S) wts[s2 * rpc + t] = mv[s2] * inv;
-    lse_row[t] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
   }
   named_sync(1, kThreads);
+  if (ok) ok = all_lanes(mbar_wait(&bars[MERGE_O], 0, abort_flag, ds));
   if (!ok) return;
-  for (int it = t; it < mine * kChunks; it += kThreads) {
+  for (int it = t; it < mine * kCh; it += kThreads) {
     const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
     const int j = it - ch * mine;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
       if (s2 < S) {
         const float w = wts[s2 * rpc + j];
-        const float4 x = recv[s2 * slice + ch * rpc + j];
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
+        const uint4 x = recv_o[(s2 * kCh + ch) * rpc + j];
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float a, b;
+          bf16x2_unpack(xw[e], a, b);
+          acc[2 * e] = fmaf(w, a, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(w, b, acc[2 * e + 1]);
+        }
       }
     }
     const int grow = m0 + r0 + j;
@@ -294,8 +302,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     const int i_row = rem / p.G;
     const int qhead = kvh * p.G + (rem - i_row * p.G);
     const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 4) =
-        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 8) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
     if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
   }
 }
@@ -367,7 +376,8 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     mbar_init(&bars[KREADY + 0], 64);
     mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
-    mbar_init(&bars[MERGE], 1);
+    mbar_init(&bars[MERGE_ML], 1);
+    mbar_init(&bars[MERGE_O], 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -405,18 +415,19 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
-      int last[2] = {0, nt > 1 ? 1 : -1};
+      int last0 = 0, last1 = nt > 1 ? 1 : -1;  // last tile issued into stage 0 / 1
       for (int t = 2; t < nt; ++t) {
         const int s = t & 1;
         if (!mbar_wait(&bars[KVEMPTY + s], ((t >> 1) - 1) & 1, abort_flag, ds)) break;
         issue_kv(t);
-        last[s] = t;
+        if (s == 0) last0 = t; else last1 = t;
       }
       if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
-      for (int s = 0; s < 2; ++s) {
-        if (last[s] < 0) continue;
-        mbar_drain(&bars[KFULL + s], (last[s] >> 1) & 1, ds);
-        mbar_drain(&bars[VFULL + s], (last[s] >> 1) & 1, ds);
+      mbar_drain(&bars[KFULL + 0], (last0 >> 1) & 1, ds);
+      mbar_drain(&bars[VFULL + 0], (last0 >> 1) & 1, ds);
+      if (last1 >= 0) {
+        mbar_drain(&bars[KFULL + 1], (last1 >> 1) & 1, ds);
+        mbar_drain(&bars[VFULL + 1], (last1 >> 1) & 1, ds);
       }
     }
   } else if (warp == 1) {
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     }
   }
 
-  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run, &bars[MERGE], abort_flag);
+  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run, bars, abort_flag);
 
   tc_fence_before();
   __syncthreads();

@@ -18,11 +18,14 @@ constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 // Split-KV merge: CTA q of a cluster of S merges packed rows [q * r, (q + 1) * r)
 // of the tile, r = ceil(128 / S) rounded up to even.
 __host__ __device__ constexpr int attn_merge_rows(int S) { return ((kAttnBM + S - 1) / S + 1) & ~1; }
-// fp32 partials of one (KV head, row tile): [S splits][S owners][D / 4 + 1][r]
-// float4 -- unnormalised O in D / 4 chunks of 4, then (max, sum, -, -) -- so
-// that the slice one split hands one owner is contiguous.
-__host__ __device__ constexpr long long attn_part_float4s(int S, int D) {
-  return static_cast<long long>(S) * S * (D / 4 + 1) * attn_merge_rows(S);
+// Partials of one (KV head, row tile), in slices that one split hands one
+// owner, contiguous: first [S splits][S owners][r] float2 (running max, sum),
+// then [S splits][S owners][D / 8][r] bf16x8 chunks of the split's normalised O.
+__host__ __device__ constexpr long long attn_part_ml_bytes(int S) {
+  return static_cast<long long>(S) * S * attn_merge_rows(S) * 8;
+}
+__host__ __device__ constexpr long long attn_part_bytes(int S, int D) {
+  return static_cast<long long>(S) * S * attn_merge_rows(S) * (8 + 2 * D);
 }
 
 // Everything the attention kernels need, in the fork's terms: plain attention is
@@ -32,7 +35,7 @@ struct AttnParams {
   const void* q;          // bf16 [N, n_q, Hq, D]
   void* o;                // bf16 [N, n_q, Hq, D]
   float* lse;             // fp32 [N, Hq, n_q] or null
-  float* part;            // split partials (splits > 1): [Hkv, m_tiles] blocks of attn_part_float4s float4
+  void* part;             // split partials (splits > 1): [Hkv, m_tiles] blocks of attn_part_bytes
   int m_tiles;
   const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
   const int32_t* k_pos;        // [C] or null

@@ -87,6 +87,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// log2(x) and 1/x on the MUFU unit: PTX lg2.approx.ftz.f32 and rcp.approx.ftz.f32.
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Programmatic dependent launch.  wait: this thread's global reads and writes
 // may begin (the preceding grid has completed and its writes are visible);
 // launch_dependents: the next grid in the stream may start being scheduled.
