@@ -58,7 +58,7 @@ struct TileEntry {
 
 enum Bar : int {
   KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, MERGE_ML = 16, MERGE_O = 17, NUM_BARS = 18
+  KREADY = 13, DRAIN = 15, MERGE_O = 16, NUM_BARS = 17
 };
 
 template <int D>
@@ -75,13 +75,15 @@ struct Layout {
   // the two halves of a row trade tile maxima ([2 parities][2 halves][BM])
   // and final sums ([2 halves][BM])
   static constexpr int kXch = kMisc + 64;
-  static constexpr int kEnd = kXch + 6 * BM * 4;
-  // split-KV merge, over the K / V rings and P (idle by then): the S slices of
-  // this CTA's rows (S * r <= BM + 2 * S rows: bf16 O, then (max, sum)), then
-  // the weights [S][r] and LSE [r] of those rows
+  // (max, sum) of this CTA's rows from every split of the cluster, written by
+  // the other CTAs through distributed shared memory: [S][r] float2
+  static constexpr int kMLRecv = kXch + 6 * BM * 4;
+  static constexpr int kEnd = kMLRecv + (BM + 2 * kAttnMaxSplits) * 8;
+  // split-KV merge, over the K / V rings and P (idle by then): the S bf16 O
+  // slices of this CTA's rows (S * r <= BM + 2 * S rows), then the weights
+  // [S][r] and LSE [r] of those rows
   static constexpr int kRecv = kK;
-  static constexpr int kRecvML = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
-  static constexpr int kWts = kRecvML + (BM + 2 * kAttnMaxSplits) * 8;
+  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
   static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
@@ -175,14 +177,14 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster once its own K/V range is done:
 //   1. each softmax thread writes its half of its row -- O / l in bf16 from
-//      TMEM, and (running max m, sum l) -- into the workspace slices of the CTA
-//      that owns the row;
-//   2. cluster barrier (release / acquire): every split's slices are written;
-//   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S (m, l)
-//      slices and then its S O slices into shared memory with bulk copies (one
-//      mbarrier each); while the O slices travel the softmax threads form the
-//      weights l_s 2^(m_s - M) / L once per row (M = max m_s, L = sum l_s
-//      2^(m_s - M)), then store O = sum w_s O_s in bf16 and LSE = (M + log2 L) ln 2.
+//      TMEM -- into the workspace slice of the CTA that owns the row, and its
+//      (running max m, sum l) straight into that CTA's shared memory;
+//   2. cluster barrier (release / acquire): every split's rows are written;
+//   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S O slices
+//      into shared memory with bulk copies on one mbarrier; meanwhile the
+//      softmax threads form the weights l_s 2^(m_s - M) / L once per row
+//      (M = max m_s, L = sum l_s 2^(m_s - M)), then store O = sum w_s O_s in
+//      bf16 and LSE = (M + log2 L) ln 2.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
                               float l_tot, uint64_t* bars, volatile int* abort_flag) {
@@ -195,10 +197,10 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int split = blockIdx.x;
   const int rpc = attn_merge_rows(S);
   int32_t* ds = p.dev_status;
-  uint8_t* blk = static_cast<uint8_t*>(p.part) +
-                 (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) * attn_part_bytes(S, D);
-  float2* part_ml = reinterpret_cast<float2*>(blk);                        // [S][S][rpc]
-  uint4* part_o = reinterpret_cast<uint4*>(blk + attn_part_ml_bytes(S));  // [S][S][kCh][rpc]
+  uint4* part_o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.part) +
+                                           (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) *
+                                               attn_part_bytes(S, D));  // [S][S][kCh][rpc]
+  float2* recv_ml = reinterpret_cast<float2*>(smem + L::kMLRecv);         // [S][rpc]
   if (is_sm) {
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -227,7 +229,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
                             pack_bf16x2(v[8 * q8 + 6] * inv_l, v[8 * q8 + 7] * inv_l)));
       }
       if (half == 0)
-        __stcg(part_ml + static_cast<size_t>(split * S + q) * rpc + r, make_float2(m_run, have_o ? l_tot : 0.f));
+        st_cluster_v2(cluster_addr(smem_addr(recv_ml + split * rpc + r), q), m_run, have_o ? l_tot : 0.f);
       fence_proxy_async_global();
     }
   }
@@ -236,19 +238,14 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int r0 = split * rpc;
   const int mine = max(0, min(min(BM - r0, rpc), p.rows_per_head - m0 - r0));
   if (mine == 0) return;
-  uint4* recv_o = reinterpret_cast<uint4*>(smem + L::kRecv);      // [S][kCh][rpc]
-  float2* recv_ml = reinterpret_cast<float2*>(smem + L::kRecvML);  // [S][rpc]
+  uint4* recv_o = reinterpret_cast<uint4*>(smem + L::kRecv);  // [S][kCh][rpc]
   if (threadIdx.x == 0) {
     fence_proxy_async_global();
-    mbar_arrive_expect_tx(&bars[MERGE_ML], static_cast<uint32_t>(S * rpc * 8));
-    for (int s2 = 0; s2 < S; ++s2)
-      bulk_load(recv_ml + s2 * rpc, part_ml + static_cast<size_t>(s2 * S + split) * rpc, rpc * 8, &bars[MERGE_ML]);
     mbar_arrive_expect_tx(&bars[MERGE_O], static_cast<uint32_t>(S * kCh * rpc * 16));
     for (int s2 = 0; s2 < S; ++s2)
       bulk_load(recv_o + s2 * kCh * rpc, part_o + static_cast<size_t>(s2 * S + split) * kCh * rpc, kCh * rpc * 16,
                 &bars[MERGE_O]);
     // the copies land before this thread reaches the CTA's final barrier
-    mbar_drain(&bars[MERGE_ML], 0, ds);
     mbar_drain(&bars[MERGE_O], 0, ds);
   }
   if (!is_sm) return;
@@ -257,8 +254,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int kvh = blockIdx.z;
   float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [S][rpc] weights of the splits
   float* lse_row = wts + S * rpc;                        // [rpc]
-  bool ok = all_lanes(mbar_wait(&bars[MERGE_ML], 0, abort_flag, ds));
-  if (ok) {
+  {
     // one half-warp per row, lane s2 = split s2 (S <= 16)
     const int s2 = lane & 15;
     for (int j = (warp - 2) * 2 + (lane >> 4); j < mine; j += 2 * kSmWarps) {
@@ -275,8 +271,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     }
   }
   named_sync(1, kThreads);
-  if (ok) ok = all_lanes(mbar_wait(&bars[MERGE_O], 0, abort_flag, ds));
-  if (!ok) return;
+  if (!all_lanes(mbar_wait(&bars[MERGE_O], 0, abort_flag, ds))) return;
   for (int it = t; it < mine * kCh; it += kThreads) {
     const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
     const int j = it - ch * mine;
@@ -376,7 +371,6 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     mbar_init(&bars[KREADY + 0], 64);
     mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
-    mbar_init(&bars[MERGE_ML], 1);
     mbar_init(&bars[MERGE_O], 1);
     misc[1] = 0;
     fence_mbar_init();

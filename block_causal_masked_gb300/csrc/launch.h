@@ -18,14 +18,12 @@ constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 // Split-KV merge: CTA q of a cluster of S merges packed rows [q * r, (q + 1) * r)
 // of the tile, r = ceil(128 / S) rounded up to even.
 __host__ __device__ constexpr int attn_merge_rows(int S) { return ((kAttnBM + S - 1) / S + 1) & ~1; }
-// Partials of one (KV head, row tile), in slices that one split hands one
-// owner, contiguous: first [S splits][S owners][r] float2 (running max, sum),
-// then [S splits][S owners][D / 8][r] bf16x8 chunks of the split's normalised O.
-__host__ __device__ constexpr long long attn_part_ml_bytes(int S) {
-  return static_cast<long long>(S) * S * attn_merge_rows(S) * 8;
-}
+// Partial O of one (KV head, row tile) in the slices that one split hands one
+// owner, contiguous: [S splits][S owners][D / 8][r] bf16x8 chunks of the
+// split's normalised O.  (The splits' running max and sum travel through
+// distributed shared memory.)
 __host__ __device__ constexpr long long attn_part_bytes(int S, int D) {
-  return static_cast<long long>(S) * S * attn_merge_rows(S) * (8 + 2 * D);
+  return static_cast<long long>(S) * S * attn_merge_rows(S) * 2 * D;
 }
 
 // Everything the attention kernels need, in the fork's terms: plain attention is

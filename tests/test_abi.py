@@ -99,9 +99,9 @@ def test_fork_argument_errors_on_host():
 
 
 def test_workspace_sizes_are_host_arithmetic():
-    # split partials: Hkv * row tiles * S * S owner slices of r rows (r = 32 at S = 4), each row
-    # (max, sum) in fp32 and D bf16 values of O; none with one split
-    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 2 * 1 * 4 * 4 * 32 * (8 + 2 * 128)
+    # split partials: Hkv * row tiles * S * S owner slices of r rows (r = 32 at S = 4) of D bf16
+    # values of O; none with one split
+    assert bd.lib().bd_attn_workspace_size(_attn(num_splits=4)) == 2 * 1 * 4 * 4 * 32 * 2 * 128
     assert bd.lib().bd_attn_workspace_size(_attn(num_splits=1)) == 0
     u = bd.bd_unmask_args()
     u.R, u.V, u.n_pos, u.n_blocks, u.logits_ld, u.min_den, u.add_den, u.act_den = 32, 151936, 33, 1, 151936, 4, 2, 20
