@@ -114,58 +114,39 @@ __device__ Acc block_reduce(Acc a, Acc* sh) {
   return a;
 }
 
-// Merges the chunk partials of one row with one warp: lane c folds chunks
-// c, c + 32, ... and the lanes are combined with shuffles.  Valid in every lane.
-__device__ Acc warp_merge_row(const float4* part, int chunks) {
-  const int lane = threadIdx.x & 31;
-  Acc a{-INFINITY, 0.f, 0x7fffffff};
-  for (int c = lane; c < chunks; c += 32) {
-    const float4 q = __ldcg(part + c);
-    acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Acc b;
-    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
-    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
-    b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
-    acc_merge(a, b);
-  }
-  return a;
-}
-
-// Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed scores).
+// Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed
+// scores).  Each thread keeps U 8-element vectors in flight, so a chunk of up
+// to U * 8 * 256 elements costs one memory round trip.
+template <int U>
 __device__ Acc reduce_chunk(const void* logits, int dtype, long long row_off, const float* noise, long long noise_off,
                             float inv_temp, int lo, int hi, bool need_sum) {
   Acc a{-INFINITY, 0.f, 0x7fffffff};
   const int vlo = lo / 8, vhi = hi / 8;  // whole 8-element vectors (lo is a multiple of 8)
-  int v = vlo + threadIdx.x;
-  // four vectors in flight per thread
-  for (; v + 3 * kThreads < vhi; v += 4 * kThreads) {
-    float x[4][8];
+  for (int v0 = vlo; v0 < vhi; v0 += U * kThreads) {
+    float x[U][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) load_vec8(logits, dtype, row_off + 8ll * (v + u * kThreads), x[u]);
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * kThreads + threadIdx.x;
+      if (v < vhi) load_vec8(logits, dtype, row_off + 8ll * v, x[u]);
+    }
     if (noise) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4* np4 = reinterpret_cast<const float4*>(noise + noise_off + 8ll * (v + u * kThreads));
-        const float4 n0 = __ldg(np4), n1 = __ldg(np4 + 1);
-        const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * kThreads + threadIdx.x;
+        if (v < vhi) {
+          const float4* np4 = reinterpret_cast<const float4*>(noise + noise_off + 8ll * v);
+          const float4 n0 = __ldg(np4), n1 = __ldg(np4 + 1);
+          const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[u][k] = gumbel_score(x[u][k], nn[k], inv_temp);
+          for (int k = 0; k < 8; ++k) x[u][k] = gumbel_score(x[u][k], nn[k], inv_temp);
+        }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc_vec<8>(a, x[u], 8 * (v + u * kThreads), need_sum);
-  }
-  for (; v < vhi; v += kThreads) {
-    float x[8];
-    load_vec8(logits, dtype, row_off + 8ll * v, x);
-    if (noise) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = gumbel_score(x[k], __ldg(noise + noise_off + 8ll * v + k), inv_temp);
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * kThreads + threadIdx.x;
+      if (v < vhi) acc_vec<8>(a, x[u], 8 * v, need_sum);
     }
-    acc_vec<8>(a, x, 8 * v, need_sum);
   }
   // ragged tail of the row (only when the row length is not a multiple of 8)
   for (int i = vhi * 8 + threadIdx.x; i < hi; i += kThreads) {
@@ -175,6 +156,35 @@ __device__ Acc reduce_chunk(const void* logits, int dtype, long long row_off, co
   }
   return a;
 }
+
+// Copies n chunk partials to shared memory, four loads in flight per thread.
+__device__ void stage_partials(const float4* src, int n, float4* dst) {
+  for (int i0 = 0; i0 < n; i0 += 4 * kThreads) {
+    float4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kThreads + threadIdx.x;
+      if (i < n) q[u] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kThreads + threadIdx.x;
+      if (i < n) dst[i] = q[u];
+    }
+  }
+}
+
+// Merge of one row's chunk partials (staged in shared memory), in chunk order.
+__device__ Acc merge_staged(const float4* part, int chunks) {
+  Acc a{-INFINITY, 0.f, 0x7fffffff};
+  for (int c = 0; c < chunks; ++c) {
+    const float4 q = part[c];
+    acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
+  }
+  return a;
+}
+
+constexpr int kStageF4 = 1024;  // chunk partials staged at a time by the deciding CTA (16 KB)
 
 // ======================================================================= unmask
 
@@ -190,21 +200,26 @@ __device__ void unmask_select(const UnmaskParams& p) {
     ok_local &= lo < hi && hi - lo <= kMaxBlock;
   }
   if (tid == 0) ok_local &= __ldg(p.block_start) == 0 && __ldg(p.block_start + p.n_blocks) == p.n_pos;
-  // one warp per position: merge its row's chunk partials
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int j = warp; j < p.n_pos; j += kThreads / 32) {
-    const int row = __ldg(p.logit_row + j);
-    const uint8_t st = p.state[j];
-    const bool cand = st == BD_MASKED && row >= 0 && row < p.R;
-    float conf = 0.f, lse = 0.f;
-    int pred = -1;
-    if (cand) {
-      const Acc a = warp_merge_row(p.chunk_part + static_cast<size_t>(j) * p.chunks, p.chunks);
-      conf = 1.f / a.s;
-      lse = a.m + logf(a.s);
-      pred = a.idx;
-    }
-    if (lane == 0) {
+  // every position's chunk partials, staged in batches: one thread per position
+  __shared__ float4 stage[kStageF4];
+  const int per_batch = max(1, kStageF4 / p.chunks);
+  for (int j0 = 0; j0 < p.n_pos; j0 += per_batch) {
+    const int nb = min(per_batch, p.n_pos - j0);
+    stage_partials(p.chunk_part + static_cast<size_t>(j0) * p.chunks, nb * p.chunks, stage);
+    __syncthreads();
+    for (int jj = tid; jj < nb; jj += kThreads) {
+      const int j = j0 + jj;
+      const int row = __ldg(p.logit_row + j);
+      const uint8_t st = p.state[j];
+      const bool cand = st == BD_MASKED && row >= 0 && row < p.R;
+      float conf = 0.f, lse = 0.f;
+      int pred = -1;
+      if (cand) {
+        const Acc a = merge_staged(stage + jj * p.chunks, p.chunks);
+        conf = 1.f / a.s;
+        lse = a.m + logf(a.s);
+        pred = a.idx;
+      }
       st0[j] = st;
       conf_s[j] = conf;
       pred_s[j] = pred;
@@ -213,6 +228,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
       if (p.lse) p.lse[j] = lse;
       p.commit[j] = 0;
     }
+    __syncthreads();
   }
   if (!__syncthreads_and(ok_local)) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
@@ -303,7 +319,8 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
     const int lo = chunk * p.chunk_elems;
     const int hi = min(p.V, lo + p.chunk_elems);
     Acc a{-INFINITY, 0.f, 0x7fffffff};
-    if (lo < hi) a = reduce_chunk(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
+    if (lo < hi)
+      a = reduce_chunk<8>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
     a = block_reduce(a, red);
     if (threadIdx.x == 0)
       p.chunk_part[static_cast<size_t>(pos) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
@@ -330,12 +347,19 @@ __device__ void verify_match(const VerifyParams& p, int s) {
     st[j] = p.state[static_cast<size_t>(s) * L + j];
     tok[j] = p.tokens[static_cast<size_t>(s) * L + j];
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < p.n_rows; e += kThreads / 32) {
-    const Acc a = warp_merge_row(p.chunk_part + (static_cast<size_t>(s) * p.n_rows + e) * p.chunks, p.chunks);
-    if (lane == 0) arg[e] = a.idx == 0x7fffffff ? -1 : a.idx;
+  // the rows' chunk partials, staged in batches: one thread per row
+  __shared__ float4 stage[kStageF4];
+  const int per_batch = max(1, kStageF4 / p.chunks);
+  for (int e0 = 0; e0 < p.n_rows; e0 += per_batch) {
+    const int nb = min(per_batch, p.n_rows - e0);
+    stage_partials(p.chunk_part + (static_cast<size_t>(s) * p.n_rows + e0) * p.chunks, nb * p.chunks, stage);
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < nb; ee += kThreads) {
+      const Acc a = merge_staged(stage + ee * p.chunks, p.chunks);
+      arg[e0 + ee] = a.idx == 0x7fffffff ? -1 : a.idx;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (threadIdx.x == 0) {
     int e = 0, n_acc = 0, bonus = -1, bonus_pos = -1;
     bool mismatch = false;
@@ -388,8 +412,9 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
   const int hi = min(p.V, lo + p.chunk_elems);
   Acc a{-INFINITY, 0.f, 0x7fffffff};
   if (lo < hi)
-    a = reduce_chunk(p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise, static_cast<long long>(row) * p.ld,
-                     p.inv_temp, lo, hi, false);
+    a = p.noise ? reduce_chunk<4>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise,
+                                  static_cast<long long>(row) * p.ld, p.inv_temp, lo, hi, false)
+                : reduce_chunk<8>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, false);
   a = block_reduce(a, red);
   if (threadIdx.x == 0) {
     p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, 0.f, __int_as_float(a.idx), 0.f);
@@ -411,6 +436,7 @@ void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems) {
   int c = (target + rows - 1) / rows;
   const int max_c = (V + 2047) / 2048;
   if (c > max_c) c = max_c;
+  if (c > kStageF4) c = kStageF4;  // the deciding CTA stages one row's partials at once
   if (c < 1) c = 1;
   int e = (V + c - 1) / c;
   e = (e + 7) / 8 * 8;
