@@ -190,6 +190,134 @@ class GpuRound:
         return max(1, min(152 // (m_tiles * W.Hkv), tiles, 16))
 
 
+# ------------------------------------------------------------------------------ device-resident decode
+
+WAM = synth.WAM_SWEEP
+WAM_TOKENS = 256
+
+
+def wam_steps(B: int) -> int:
+    """Steps per block of the WAM-Diff2 sweep: top k = max(1, B / 8) commits per
+    step, at most 8 steps, a block ends once complete."""
+    return min(8, -(-B // max(1, B // 8)))
+
+
+class WamDecode:
+    """The whole 256-token WAM-Diff2 decode at block size B as ONE CUDA graph:
+    for every block, wam_steps(B) denoise steps of `layers` x
+    bd_block_causal_attn (16/8 heads, head dim 128, prefix 2,048 + the blocks
+    already decoded) and one bd_unmask_step (top k by confidence).  Block state
+    and tokens stay on the device; nothing returns to the host between steps.
+    logits: float32 host array [n_blocks, steps, B, V] of bf16 values, or None
+    for seeded N(0, 3) rows drawn on the device."""
+
+    def __init__(self, B: int, layers: int, device, logits=None, seed: int = WAM.seed, num_splits: int = 0):
+        import torch
+        import block_causal_masked_gb300 as bd
+        self.torch, self.bd, self.dev = torch, bd, device
+        self.B, self.layers, self.num_splits = B, layers, num_splits
+        self.n_blocks = WAM_TOKENS // B
+        self.steps = wam_steps(B)
+        self.k = max(1, B // 8)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + B)
+        bf = torch.bfloat16
+        kv_len = WAM.prefix + WAM_TOKENS
+        self.q = [torch.randn((B, WAM.Hq, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+        self.kk = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+        self.vv = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+        self.o = torch.empty((B, WAM.Hq, WAM.D), dtype=bf, device=device)
+        self.lse = torch.empty((WAM.Hq, B), dtype=torch.float32, device=device)
+        if logits is None:
+            self.logits = (torch.randn((self.n_blocks, self.steps, B, synth.VOCAB), generator=g, device=device)
+                           * 3.0).to(bf)
+        else:
+            self.logits = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(device).to(bf)
+        self.block = torch.tensor([0, B], dtype=torch.int32, device=device)
+        self.logit_row = torch.arange(B, dtype=torch.int32, device=device)
+        self.state = torch.zeros(WAM_TOKENS, dtype=torch.uint8, device=device)
+        self.tokens = torch.full((WAM_TOKENS,), -1, dtype=torch.int32, device=device)
+        self.um = dict(commit=torch.empty(B, dtype=torch.uint8, device=device),
+                       n_committed=torch.empty(1, dtype=torch.int32, device=device),
+                       status=torch.empty(1, dtype=torch.int32, device=device),
+                       pred=torch.empty(B, dtype=torch.int32, device=device),
+                       conf=torch.empty(B, dtype=torch.float32, device=device),
+                       lse=torch.empty(B, dtype=torch.float32, device=device))
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.launches = self.n_blocks * self.steps * (layers + 1)
+
+    def _block_step(self, b: int, s: int):
+        bd, B = self.bd, self.B
+        C = WAM.prefix + b * B
+        for l in range(self.layers):
+            bd.bd_block_causal_attn(self.q[l], self.kk[l], self.vv[l], C, block_start=self.block, o=self.o,
+                                    lse=self.lse, num_splits=self.num_splits, dev_status=self.dev_status)
+        bd.bd_unmask_step(self.logits[b, s], self.logit_row, self.block, self.state[b * B:(b + 1) * B],
+                          self.tokens[b * B:(b + 1) * B], tau_full=2.0, tau_half=2.0, min_frac=(0, 1),
+                          k_fixed=self.k, add_thr=(1, 2), act_thr=(17, 20), dev_status=self.dev_status, **self.um)
+
+    def reset(self):
+        self.state.zero_()
+        self.tokens.fill_(-1)
+
+    def capture(self):
+        torch = self.torch
+        self._block_step(0, 0)                    # workspaces and kernel attributes, outside the capture
+        torch.cuda.synchronize()
+        self.reset()
+        stream = torch.cuda.Stream(self.dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for b in range(self.n_blocks):
+                for s in range(self.steps):
+                    self._block_step(b, s)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.reset()
+        self.graph.replay()
+
+
+def run_wam_sweep(args, device):
+    """One JSON line per block size: committed tokens/s of the whole decode."""
+    import torch
+    torch.cuda.set_device(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    for B in (1, 4, 8, 16, 32):
+        dec = WamDecode(B, WAM.layers, device)
+        t0 = time.time()
+        dec.capture()
+        cap_s = time.time() - t0
+        for _ in range(args.warmup):
+            dec.replay()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            dec.reset()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            dec.graph.replay()
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        committed = int((dec.state == synth.COMMITTED).sum())
+        status = int(dec.dev_status[0])
+        t = statistics.median(ms)
+        print(json.dumps({"metric": "committed tokens/s (whole decode, one CUDA graph)", "value": committed / t * 1e3,
+                          "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_decode": t, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": f"wam_diff2_sweep B={B}: {WAM_TOKENS} tokens, blocks of {B}, top "
+                                                 f"{dec.k} per step, {dec.steps} steps per block, 16/8 heads, "
+                                                 f"head dim 128, {WAM.layers} layers, prefix {WAM.prefix}",
+                                     "gpu_launches_per_decode": dec.launches, "graph_capture_s": round(cap_s, 2),
+                                     "l2": "flushed before every timed decode"},
+                          "committed": committed, "dev_status": status}), flush=True)
+        del dec
+        torch.cuda.empty_cache()
+
+
 def algorithmic(inp):
     """Bytes (and FLOPs) the round must move: visible K/V, Q, O, LSE per layer;
     logits rows of masked editable positions; AR rows."""
@@ -443,12 +571,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep"], default="fast_ddrive",
+                    help="wam_sweep: the whole WAM-Diff2 decode per block size as one CUDA graph (extra lines)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload == "wam_sweep":
+        run_wam_sweep(args, int(os.environ.get("LOCAL_RANK", "0")))
+        return 0
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

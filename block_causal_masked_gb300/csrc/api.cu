@@ -132,11 +132,14 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   int splits = d.num_splits;
   if (splits == 0) {
     // spread the KV range of every (row tile, KV head) over the SMs as a cluster
-    // of up to 16 CTAs, at least one tile each
+    // of up to 16 CTAs, at least one tile each, and keep every cluster of the
+    // launch resident at once (one wave): the widest split count whose
+    // clusters all fit
     const long long base = static_cast<long long>(pl->m_tiles) * d.Hkv;
     long long s = kPlanSms / base;
     if (s > max_tiles) s = max_tiles;
     if (s > kAttnMaxSplits) s = kAttnMaxSplits;
+    while (s > 1 && base > attn_resident_clusters(static_cast<int>(s))) --s;
     splits = s < 1 ? 1 : static_cast<int>(s);
   }
   pl->splits = splits;

@@ -15,6 +15,15 @@ constexpr int kAttnBN = 128;        // keys per K/V tile
 constexpr int kAttnMaxTiles = 4096; // K/V tiles of one (row tile, KV head) before splitting
 constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 
+// Clusters of S attention CTAs (one CTA per SM: ~200 KB of shared memory and
+// all 512 TMEM columns) that a GB300 holds at once, as
+// cudaOccupancyMaxActiveClusters reports it for 1 <= S <= 16: the GPCs fit
+// fewer wide clusters than 152 / S.
+__host__ __device__ constexpr int attn_resident_clusters(int S) {
+  constexpr int kTable[17] = {0, 152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7};
+  return S >= 1 && S <= 16 ? kTable[S] : 0;
+}
+
 // Split-KV merge: CTA q of a cluster of S merges packed rows [q * r, (q + 1) * r)
 // of the tile, r = ceil(128 / S) rounded up to even.
 __host__ __device__ constexpr int attn_merge_rows(int S) { return ((kAttnBM + S - 1) / S + 1) & ~1; }
