@@ -300,9 +300,10 @@ bd_status plan_unmask(const bd_unmask_args* a, int* chunks, int* elems, size_t* 
   if (a->min_den < 1 || a->add_den < 1 || a->act_den < 1 || a->min_num < 0 || a->add_num < 0 || a->act_num < 0 ||
       a->k_fixed < 0)
     return BD_ERR_INVALID_ARG;
-  const int rows = a->R < a->n_pos ? a->R : a->n_pos;
+  if (a->R > kMaxVerifyRows) return BD_ERR_UNSUPPORTED;  // one CTA row per logits row (grid y)
+  const int rows = a->R;
   vocab_split(rows, a->V, kPlanSms, chunks, elems);
-  *ws = unmask_workspace_bytes(a->n_pos, *chunks);
+  *ws = unmask_workspace_bytes(a->R, *chunks);
   return BD_OK;
 }
 

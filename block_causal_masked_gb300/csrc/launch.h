@@ -90,7 +90,7 @@ struct UnmaskParams {
   int write_draft;
   int32_t* dev_status;
   // workspace carve-up
-  float4* chunk_part;         // [n_pos, chunks]: (max, sum, argmax bits, -)
+  float4* chunk_part;         // [R, chunks]: (max, sum, argmax bits, -)
   unsigned int* grid_ticket;  // [1]
   int chunks;                 // CTAs per logits row
   int chunk_elems;            // elements per chunk (multiple of 8)
@@ -122,7 +122,7 @@ constexpr int kMaxVerifySeqs = 1024;   // sequences of one verify call
 
 size_t unmask_counter_bytes();
 size_t verify_counter_bytes();
-size_t unmask_workspace_bytes(int n_pos, int chunks);
+size_t unmask_workspace_bytes(int R, int chunks);
 size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks);
 void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems);
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream);

@@ -184,58 +184,100 @@ __device__ Acc merge_staged(const float4* part, int chunks) {
   return a;
 }
 
-constexpr int kStageF4 = 1024;  // chunk partials staged at a time by the deciding CTA (16 KB)
+constexpr int kStageF4 = 512;  // chunk partials staged at a time by the deciding CTA (8 KB)
 
 // ======================================================================= unmask
 
 __device__ void unmask_select(const UnmaskParams& p) {
+  constexpr int kPer = kMaxPos / kThreads;  // positions per thread
   __shared__ uint8_t st0[kMaxPos];
   __shared__ float conf_s[kMaxPos];
   __shared__ int pred_s[kMaxPos];
+  __shared__ int row_s[kMaxPos];
+  __shared__ int bs_s[kMaxPos + 1];
   __shared__ int cnt[4];
-  const int tid = threadIdx.x;
-  int ok_local = 1;
-  for (int b = tid; b < p.n_blocks; b += kThreads) {
-    const int lo = __ldg(p.block_start + b), hi = __ldg(p.block_start + b + 1);
-    ok_local &= lo < hi && hi - lo <= kMaxBlock;
-  }
-  if (tid == 0) ok_local &= __ldg(p.block_start) == 0 && __ldg(p.block_start + p.n_blocks) == p.n_pos;
-  // every position's chunk partials, staged in batches: one thread per position
   __shared__ float4 stage[kStageF4];
-  const int per_batch = max(1, kStageF4 / p.chunks);
-  for (int j0 = 0; j0 < p.n_pos; j0 += per_batch) {
-    const int nb = min(per_batch, p.n_pos - j0);
-    stage_partials(p.chunk_part + static_cast<size_t>(j0) * p.chunks, nb * p.chunks, stage);
-    __syncthreads();
-    for (int jj = tid; jj < nb; jj += kThreads) {
-      const int j = j0 + jj;
-      const int row = __ldg(p.logit_row + j);
-      const uint8_t st = p.state[j];
-      const bool cand = st == BD_MASKED && row >= 0 && row < p.R;
-      float conf = 0.f, lse = 0.f;
-      int pred = -1;
-      if (cand) {
-        const Acc a = merge_staged(stage + jj * p.chunks, p.chunks);
-        conf = 1.f / a.s;
-        lse = a.m + logf(a.s);
-        pred = a.idx;
+  const int tid = threadIdx.x;
+  const int per_batch = max(1, kStageF4 / p.chunks);  // logits rows whose partials are staged at once
+  {
+    // one memory round trip: every load is issued before the first is used
+    uint8_t stv[kPer];
+    int rv[kPer], bv[kPer + 1];
+    float4 q[kStageF4 / kThreads];
+    const int n0 = min(per_batch, p.R) * p.chunks;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = u * kThreads + tid;
+      if (j < p.n_pos) {
+        stv[u] = p.state[j];
+        rv[u] = __ldg(p.logit_row + j);
       }
-      st0[j] = st;
-      conf_s[j] = conf;
-      pred_s[j] = pred;
-      if (p.pred) p.pred[j] = pred;
-      if (p.conf) p.conf[j] = conf;
-      if (p.lse) p.lse[j] = lse;
-      p.commit[j] = 0;
+    }
+#pragma unroll
+    for (int u = 0; u <= kPer; ++u) {
+      const int b = u * kThreads + tid;
+      if (b <= p.n_blocks) bv[u] = __ldg(p.block_start + b);
+    }
+#pragma unroll
+    for (int u = 0; u < kStageF4 / kThreads; ++u) {
+      const int i = u * kThreads + tid;
+      if (i < n0) q[u] = __ldcg(p.chunk_part + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = u * kThreads + tid;
+      if (j < p.n_pos) {
+        st0[j] = stv[u];
+        row_s[j] = rv[u];
+        conf_s[j] = 0.f;
+        pred_s[j] = -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u <= kPer; ++u) {
+      const int b = u * kThreads + tid;
+      if (b <= p.n_blocks) bs_s[b] = bv[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kStageF4 / kThreads; ++u) {
+      const int i = u * kThreads + tid;
+      if (i < n0) stage[i] = q[u];
+    }
+  }
+  // every masked position with a logits row: merge that row's chunk partials
+  for (int r0 = 0; r0 < p.R; r0 += per_batch) {
+    const int nb = min(per_batch, p.R - r0);
+    if (r0 > 0) stage_partials(p.chunk_part + static_cast<size_t>(r0) * p.chunks, nb * p.chunks, stage);
+    __syncthreads();
+    for (int j = tid; j < p.n_pos; j += kThreads) {
+      const int row = row_s[j];
+      if (row < r0 || row >= r0 + nb || st0[j] != BD_MASKED) continue;
+      const Acc a = merge_staged(stage + (row - r0) * p.chunks, p.chunks);
+      conf_s[j] = 1.f / a.s;
+      pred_s[j] = a.idx;
+      if (p.lse) p.lse[j] = a.m + logf(a.s);
     }
     __syncthreads();
   }
+  int ok_local = 1;
+  for (int j = tid; j < p.n_pos; j += kThreads) {
+    const int pred = pred_s[j];
+    if (p.pred) p.pred[j] = pred;
+    if (p.conf) p.conf[j] = conf_s[j];
+    if (p.lse && pred < 0) p.lse[j] = 0.f;
+    p.commit[j] = 0;
+  }
+  for (int b = tid; b < p.n_blocks; b += kThreads) {
+    const int lo = bs_s[b], hi = bs_s[b + 1];
+    ok_local &= lo < hi && hi - lo <= kMaxBlock;
+  }
+  if (tid == 0) ok_local &= bs_s[0] == 0 && bs_s[p.n_blocks] == p.n_pos;
   if (!__syncthreads_and(ok_local)) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
     return;
   }
   for (int b = 0; b < p.n_blocks; ++b) {
-    const int lo = __ldg(p.block_start + b), hi = __ldg(p.block_start + b + 1);
+    const int lo = bs_s[b], hi = bs_s[b + 1];
     if (tid < 4) cnt[tid] = 0;
     __syncthreads();
     int masked = 0, cand = 0, prev_done = 0;
@@ -244,7 +286,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
       cand += pred_s[j] >= 0;
     }
     if (b > 0) {
-      const int plo = __ldg(p.block_start + b - 1);
+      const int plo = bs_s[b - 1];
       for (int j = plo + tid; j < lo; j += kThreads) prev_done += st0[j] != BD_MASKED;
     }
     if (masked) atomicAdd(&cnt[0], masked);
@@ -257,7 +299,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
     } else if (b == 0) {
       status = BD_FULL;
     } else {
-      const long long psize = lo - __ldg(p.block_start + b - 1);
+      const long long psize = lo - bs_s[b - 1];
       const long long done = cnt[2];
       status = done * p.act_den >= static_cast<long long>(p.act_num) * psize   ? BD_FULL
                : done * p.add_den >= static_cast<long long>(p.add_num) * psize ? BD_HALF
@@ -311,11 +353,11 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
   __shared__ int last;
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_trigger();  // the next kernel may start its own set-up
-  const int pos = blockIdx.y;
+  // one CTA per (chunk, logits row): every row is streamed, whichever position
+  // it belongs to, so no lookup stands before the first load
+  const int row = blockIdx.y;
   const int chunk = blockIdx.x;
-  const int row = __ldg(p.logit_row + pos);
-  const bool cand = p.state[pos] == BD_MASKED && row >= 0 && row < p.R;
-  if (cand) {
+  {
     const int lo = chunk * p.chunk_elems;
     const int hi = min(p.V, lo + p.chunk_elems);
     Acc a{-INFINITY, 0.f, 0x7fffffff};
@@ -323,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
       a = reduce_chunk<8>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
     a = block_reduce(a, red);
     if (threadIdx.x == 0)
-      p.chunk_part[static_cast<size_t>(pos) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
+      p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -339,20 +381,51 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
 // ======================================================================= verify
 
 __device__ void verify_match(const VerifyParams& p, int s) {
+  constexpr int kPer = kMaxVerifyL / kThreads;
   __shared__ uint8_t st[kMaxVerifyL];
   __shared__ int tok[kMaxVerifyL];
   __shared__ int arg[kMaxVerifyL + 1];
+  __shared__ float4 stage[kStageF4];
   const int L = p.L;
-  for (int j = threadIdx.x; j < L; j += kThreads) {
-    st[j] = p.state[static_cast<size_t>(s) * L + j];
-    tok[j] = p.tokens[static_cast<size_t>(s) * L + j];
+  const int per_batch = max(1, kStageF4 / p.chunks);  // rows whose partials are staged at once
+  const float4* part = p.chunk_part + static_cast<size_t>(s) * p.n_rows * p.chunks;
+  {
+    // one memory round trip: every load is issued before the first is used
+    uint8_t sv[kPer];
+    int tv[kPer];
+    float4 q[kStageF4 / kThreads];
+    const int n0 = min(per_batch, p.n_rows) * p.chunks;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = u * kThreads + threadIdx.x;
+      if (j < L) {
+        sv[u] = p.state[static_cast<size_t>(s) * L + j];
+        tv[u] = p.tokens[static_cast<size_t>(s) * L + j];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageF4 / kThreads; ++u) {
+      const int i = u * kThreads + threadIdx.x;
+      if (i < n0) q[u] = __ldcg(part + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = u * kThreads + threadIdx.x;
+      if (j < L) {
+        st[j] = sv[u];
+        tok[j] = tv[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageF4 / kThreads; ++u) {
+      const int i = u * kThreads + threadIdx.x;
+      if (i < n0) stage[i] = q[u];
+    }
   }
   // the rows' chunk partials, staged in batches: one thread per row
-  __shared__ float4 stage[kStageF4];
-  const int per_batch = max(1, kStageF4 / p.chunks);
   for (int e0 = 0; e0 < p.n_rows; e0 += per_batch) {
     const int nb = min(per_batch, p.n_rows - e0);
-    stage_partials(p.chunk_part + (static_cast<size_t>(s) * p.n_rows + e0) * p.chunks, nb * p.chunks, stage);
+    if (e0 > 0) stage_partials(part + static_cast<size_t>(e0) * p.chunks, nb * p.chunks, stage);
     __syncthreads();
     for (int ee = threadIdx.x; ee < nb; ee += kThreads) {
       const Acc a = merge_staged(stage + ee * p.chunks, p.chunks);
@@ -453,8 +526,8 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 size_t unmask_counter_bytes() { return 256; }
 size_t verify_counter_bytes() { return align256(sizeof(unsigned) * kMaxVerifySeqs); }
 
-size_t unmask_workspace_bytes(int n_pos, int chunks) {
-  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_pos) * chunks);
+size_t unmask_workspace_bytes(int R, int chunks) {
+  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(R) * chunks);
 }
 
 size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
@@ -480,7 +553,7 @@ static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, cudaStre
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
-  return launch_pdl(unmask_kernel, dim3(p.chunks, p.n_pos), p, stream);
+  return launch_pdl(unmask_kernel, dim3(p.chunks, p.R), p, stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {

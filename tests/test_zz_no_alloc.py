@@ -100,8 +100,8 @@ def test_noalloc_unmask_equals_workspace_unmask_on_two_calls():
 def test_noalloc_refuses_problems_beyond_its_scratch():
     L = bd.lib()
     a = bd.bd_unmask_args()
-    # one logits row spread over many chunks, for a window of 2048 positions
-    a.R, a.V, a.n_pos, a.n_blocks, a.logits_ld = 1, 151936, 2048, 1, 151936
+    # the partials of 65,535 logits rows (the most one call takes) need more than the scratch
+    a.R, a.V, a.n_pos, a.n_blocks, a.logits_ld = 65535, 151936, 2048, 1, 151936
     a.min_den, a.add_den, a.act_den = 4, 2, 20
     assert L.bd_unmask_workspace_size(a) > (1 << 20)
     L.bd_unmask_step_noalloc.argtypes = [ct.POINTER(bd.bd_unmask_args), ct.c_void_p]
