@@ -42,7 +42,8 @@ namespace {
 
 constexpr int BM = kAttnBM;
 constexpr int BN = kAttnBN;
-constexpr int kStages = 2;
+constexpr int kKStages = 3;  // K ring: a stage is free once S = Q.K^T of its tile is done
+constexpr int kVStages = 2;  // V ring: a stage is free once P.V of its tile is done
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
 // warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax, then 2 RoPE warps
@@ -57,20 +58,19 @@ struct TileEntry {
 
 
 enum Bar : int {
-  KFULL = 0, VFULL = 2, KVEMPTY = 4, SFULL = 6, SFREE = 8, PFULL = 10, ODONE = 11, QFULL = 12,
-  KREADY = 13, DRAIN = 15, MERGE_O = 16, NUM_BARS = 17
+  KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 13, QFULL = 14,
+  KREADY = 15, DRAIN = 18, MERGE_O = 19, NUM_BARS = 20
 };
 
 template <int D>
 struct Layout {
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;  // one K or one V tile
-  static constexpr int kPBytes = BM * BN * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + kStages * kKVBytes;
-  static constexpr int kP = kV + kStages * kKVBytes;
-  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kV = kK + kKStages * kKVBytes;
+  static constexpr int kRingEnd = kV + kVStages * kKVBytes;
+  static constexpr int kBar = kRingEnd;
   static constexpr int kMisc = kBar + NUM_BARS * 8;
   // the two halves of a row trade tile maxima ([2 parities][2 halves][BM])
   // and final sums ([2 halves][BM])
@@ -79,12 +79,12 @@ struct Layout {
   // the other CTAs through distributed shared memory: [S][r] float2
   static constexpr int kMLRecv = kXch + 6 * BM * 4;
   static constexpr int kEnd = kMLRecv + (BM + 2 * kAttnMaxSplits) * 8;
-  // split-KV merge, over the K / V rings and P (idle by then): the S bf16 O
+  // split-KV merge, over the K / V rings (idle by then): the S bf16 O
   // slices of this CTA's rows (S * r <= BM + 2 * S rows), then the weights
   // [S][r] and LSE [r] of those rows
   static constexpr int kRecv = kK;
   static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
-  static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kP + kPBytes, "merge buffers must fit");
+  static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kRingEnd, "merge buffers must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
@@ -323,27 +323,22 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
 
   const TileRange tr = tile_range(p, m0, split);
   const int nt = tr.hi - tr.lo;
-  // TMA of K/V tile t into stage t % 2 (the caller has made sure the stage is free)
-  auto issue_kv = [&](int t) {
-    const int s = t & 1;
+  // TMA of K tile t into K stage t % 3 and of V tile t into V stage t % 2 (the
+  // caller has made sure the stage is free)
+  auto issue_tile = [&](int t, bool is_v) {
+    const int s = is_v ? t % kVStages : t % kKStages;
     const TileEntry te = tile_at(p, tr, t);
-    uint8_t* kdst = smem + L::kK + s * L::kKVBytes;
-    uint8_t* vdst = smem + L::kV + s * L::kKVBytes;
-    mbar_arrive_expect_tx(&bars[KFULL + s], L::kKVBytes);
+    uint8_t* dst = smem + (is_v ? L::kV : L::kK) + s * L::kKVBytes;
+    uint64_t* bar = &bars[(is_v ? VFULL : KFULL) + s];
+    const CUtensorMap* pm = is_v ? &maps.pv : &maps.pk;
+    const CUtensorMap* rm = is_v ? &maps.rv : &maps.rk;
+    mbar_arrive_expect_tx(bar, L::kKVBytes);
 #pragma unroll
     for (int hh = 0; hh < D / 64; ++hh) {
       if (te.rollout < 0)
-        tma_load_3d(kdst + hh * BN * 128, &maps.pk, hh * 64, te.key0, kvh, &bars[KFULL + s]);
+        tma_load_3d(dst + hh * BN * 128, pm, hh * 64, te.key0, kvh, bar);
       else
-        tma_load_4d(kdst + hh * BN * 128, &maps.rk, hh * 64, te.key0, kvh, te.rollout, &bars[KFULL + s]);
-    }
-    mbar_arrive_expect_tx(&bars[VFULL + s], L::kKVBytes);
-#pragma unroll
-    for (int hh = 0; hh < D / 64; ++hh) {
-      if (te.rollout < 0)
-        tma_load_3d(vdst + hh * BN * 128, &maps.pv, hh * 64, te.key0, kvh, &bars[VFULL + s]);
-      else
-        tma_load_4d(vdst + hh * BN * 128, &maps.rv, hh * 64, te.key0, kvh, te.rollout, &bars[VFULL + s]);
+        tma_load_4d(dst + hh * BN * 128, rm, hh * 64, te.key0, kvh, te.rollout, bar);
     }
   };
 
@@ -355,21 +350,20 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     }
     tma_prefetch_desc(&maps.rk);
     tma_prefetch_desc(&maps.rv);
-    mbar_init(&bars[KFULL + 0], 1);
-    mbar_init(&bars[KFULL + 1], 1);
-    mbar_init(&bars[VFULL + 0], 1);
-    mbar_init(&bars[VFULL + 1], 1);
-    mbar_init(&bars[KVEMPTY + 0], 1);
-    mbar_init(&bars[KVEMPTY + 1], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars[KFULL + i], 1);
+      mbar_init(&bars[KEMPTY + i], 1);
+      mbar_init(&bars[KREADY + i], 64);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars[VFULL + i], 1);
+      mbar_init(&bars[VEMPTY + i], 1);
+    }
     mbar_init(&bars[SFULL + 0], 1);
     mbar_init(&bars[SFULL + 1], 1);
-    mbar_init(&bars[SFREE + 0], 32 * kSmWarps);
-    mbar_init(&bars[SFREE + 1], 32 * kSmWarps);
     mbar_init(&bars[PFULL], 32 * kSmWarps);
     mbar_init(&bars[ODONE], 1);
     mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
-    mbar_init(&bars[KREADY + 0], 64);
-    mbar_init(&bars[KREADY + 1], 64);
     mbar_init(&bars[DRAIN], 1);
     mbar_init(&bars[MERGE_O], 1);
     misc[1] = 0;
@@ -392,8 +386,12 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
         for (int hh = 0; hh < D / 64; ++hh)
           tma_load_4d(smem + L::kQ + hh * BM * 128, &maps.q, hh * 64, 0, kvh, m0 / p.G, &bars[QFULL]);
       }
-      issue_kv(0);
-      if (nt > 1) issue_kv(1);
+      // K runs one tile ahead of V: K 0, V 0, K 1, V 1, K 2
+      for (int t = 0; t < 2 && t < nt; ++t) {
+        issue_tile(t, false);
+        issue_tile(t, true);
+      }
+      if (nt > 2) issue_tile(2, false);
     }
   }
   tc_fence_before();
@@ -409,20 +407,26 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
-      int last0 = 0, last1 = nt > 1 ? 1 : -1;  // last tile issued into stage 0 / 1
+      // K tile t + 1 needs S of tile t - 2 done (its stage), V tile t needs P.V
+      // of tile t - 2 done; S(t - 2) completes before P.V(t - 3), so issuing in
+      // the order K(t + 1), V(t) never waits behind a later event
+      int nk = nt < 3 ? nt : 3, nv = nt < 2 ? nt : 2;  // tiles issued so far
       for (int t = 2; t < nt; ++t) {
-        const int s = t & 1;
-        if (!mbar_wait(&bars[KVEMPTY + s], ((t >> 1) - 1) & 1, abort_flag, ds)) break;
-        issue_kv(t);
-        if (s == 0) last0 = t; else last1 = t;
+        if (t + 1 < nt) {
+          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKStages], ((t + 1) / kKStages - 1) & 1, abort_flag, ds)) break;
+          issue_tile(t + 1, false);
+          nk = t + 2;
+        }
+        if (!mbar_wait(&bars[VEMPTY + t % kVStages], (t / kVStages - 1) & 1, abort_flag, ds)) break;
+        issue_tile(t, true);
+        nv = t + 1;
       }
+      // every copy issued lands before the CTA gives up its shared memory
       if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
-      mbar_drain(&bars[KFULL + 0], (last0 >> 1) & 1, ds);
-      mbar_drain(&bars[VFULL + 0], (last0 >> 1) & 1, ds);
-      if (last1 >= 0) {
-        mbar_drain(&bars[KFULL + 1], (last1 >> 1) & 1, ds);
-        mbar_drain(&bars[VFULL + 1], (last1 >> 1) & 1, ds);
-      }
+      for (int u = nk > kKStages ? nk - kKStages : 0; u < nk; ++u)
+        mbar_drain(&bars[KFULL + u % kKStages], (u / kKStages) & 1, ds);
+      for (int u = nv > kVStages ? nv - kVStages : 0; u < nv; ++u)
+        mbar_drain(&bars[VFULL + u % kVStages], (u / kVStages) & 1, ds);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -430,14 +434,15 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
       constexpr uint32_t kIdS = mma_idesc_bf16(BM, BN, false);
       constexpr uint32_t kIdPV = mma_idesc_bf16(BM, D, true);
       const uint32_t qa = smem_addr(smem + L::kQ);
-      const uint32_t pa = smem_addr(smem + L::kP);
       auto issue_s = [&](int u) -> bool {
         const int s = u & 1;
-        uint64_t* kb = ROPE ? &bars[KREADY + s] : &bars[KFULL + s];
-        if (!mbar_wait(kb, (u >> 1) & 1, abort_flag, ds)) return false;
-        if (u >= 2 && !mbar_wait(&bars[SFREE + s], ((u >> 1) - 1) & 1, abort_flag, ds)) return false;
+        const int ks = u % kKStages;
+        uint64_t* kb = ROPE ? &bars[KREADY + ks] : &bars[KFULL + ks];
+        // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
+        // point by this thread, and executed in issue order -- has consumed
+        if (!mbar_wait(kb, (u / kKStages) & 1, abort_flag, ds)) return false;
         tc_fence_after();
-        const uint32_t ka = smem_addr(smem + L::kK + s * L::kKVBytes);
+        const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
@@ -446,6 +451,7 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[SFULL + s]);
+        mma_commit(&bars[KEMPTY + ks]);  // K tile consumed: the producer may refill the stage
         return true;
       };
       bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds);
@@ -456,18 +462,20 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
       for (int t = 0; ok && t < nt; ++t) {
         if (t + 1 < nt && !issue_s(t + 1)) break;
         if (!mbar_wait(&bars[PFULL], t & 1, abort_flag, ds)) break;
-        if (!mbar_wait(&bars[VFULL + (t & 1)], (t >> 1) & 1, abort_flag, ds)) break;
+        if (!mbar_wait(&bars[VFULL + t % kVStages], (t / kVStages) & 1, abort_flag, ds)) break;
         tc_fence_after();
-        const uint32_t va = smem_addr(smem + L::kV + (t & 1) * L::kKVBytes);
+        const uint32_t va = smem_addr(smem + L::kV + (t % kVStages) * L::kKVBytes);
+        const uint32_t pt = tmem + (t & 1) * BN;  // P(t), in the S buffer it was formed from
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          // keys [16 kk, 16 kk + 16): the half of the row that holds them, 8 packed columns
+          const uint32_t acol = (kk >> 2) * (BN / 2) + (kk & 3) * 8;
           const uint32_t voff = kk * 16 * 128;
-          mma_bf16(tmem + 2 * BN, sw128_desc(pa + poff, 16, 1024), sw128_desc(va + voff, BN * 128, 1024),
-                   kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 2 * BN, pt + acol, sw128_desc(va + voff, BN * 128, 1024), kIdPV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars[ODONE]);
-        mma_commit(&bars[KVEMPTY + (t & 1)]);
+        mma_commit(&bars[VEMPTY + t % kVStages]);
       }
       mma_commit(&bars[DRAIN]);
       mbar_drain(&bars[DRAIN], 0, ds);
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     float* xch = reinterpret_cast<float*>(smem + L::kXch);
     bool ok = true;
     float v[32];
-    // Every named barrier below is reached by all 256 softmax threads the same
+    // Named barrier 2 + quad is reached by the quadrant's two warps the same
     // number of times (nt + 1), whatever the waits return.
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
@@ -540,19 +548,12 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
           for (int j = 8; j < BN / 2; ++j) m8[j & 7] = fmaxf(m8[j & 7], sv[j]);
           mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
-        tc_fence_before();
-        mbar_arrive(&bars[SFREE + s]);
       }
       xch[(s * 2 + half) * BM + rl] = mx;
-      named_sync(2, 32 * kSmWarps);
+      named_sync(2 + quad, 64);  // the two halves of these 32 rows
       mx = fmaxf(mx, xch[(s * 2 + (half ^ 1)) * BM + rl]);
       if (!ok) continue;
       const float m_tile = nv > 0 ? mx * p.scale_log2 : -INFINITY;
-      if (t > 0) {
-        ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
-        if (!ok) continue;
-        tc_fence_after();
-      }
       // both halves see the same m_tile and m_run, so they take the same decision
       const bool grow = m_tile > -INFINITY && (m_run == -INFINITY || m_tile > m_run + kRescaleLog2);
       float alpha = 1.f;
@@ -561,7 +562,13 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
         m_run = m_tile;
         l_run *= alpha;
       }
-      if (warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // O must be rescaled (rare once the running max has settled): that needs
+      // the previous tile's P.V to have finished first
+      const bool rescale = warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (rescale) {
+        ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
+        if (!ok) continue;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           const uint32_t oa = lane_base + 2 * BN + half * (D / 2) + c * 32;
@@ -571,6 +578,9 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
           tmem_st32(oa, v);
         }
       }
+      // P of this tile, rounded to bf16, goes into the first half of this
+      // half's S columns (S buffer s), while the previous tile's P.V -- which
+      // reads the other buffer -- is still running on the tensor pipe
       if (warp_active) {
         // masked entries are -inf; a row that has seen no key yet keeps m_run = -inf
         const float mneg = m_run == -INFINITY ? 0.f : -m_run;
@@ -580,20 +590,21 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int k = c * 32 + 2 * j;
-            const float a = fast_exp2(fmaf(sv[k], p.scale_log2, mneg));
-            const float b = fast_exp2(fmaf(sv[k + 1], p.scale_log2, mneg));
+            const float a = fast_exp2(fmaf(sv[32 * c + 2 * j], p.scale_log2, mneg));
+            const float b = fast_exp2(fmaf(sv[32 * c + 2 * j + 1], p.scale_log2, mneg));
             ls[j & 7] += a + b;
             pk[j] = pack_bf16x2(a, b);
           }
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            *reinterpret_cast<uint4*>(smem + L::kP + sw128_offset(rl, c0 + c * 32 + qq * 8, BM)) =
-                make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+          tmem_st16(lane_base + s * BN + c0 + 16 * c, pk);
         }
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      if (t > 0 && !rescale) {  // keeps the wait on every P.V phase in order
+        ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
+        if (!ok) continue;
+      }
+      tc_fence_before();
       mbar_arrive(&bars[PFULL]);
     }
     if (ok && nt > 0) {
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     }
     have_o = ok && nt > 0;
     xch[(4 + half) * BM + rl] = l_run;
-    named_sync(2, 32 * kSmWarps);
+    named_sync(2 + quad, 64);
     l_run += xch[(4 + (half ^ 1)) * BM + rl];  // the row's sum over both halves
     if (p.num_splits == 1) {
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -634,8 +645,8 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     // ---------------------------------------------------------------- RoPE on staged prefix keys
     const int kr0 = threadIdx.x - 32 * (2 + kSmWarps);  // this thread rotates key rows kr0 and kr0 + 64 of the tile
     for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
-      if (!mbar_wait(&bars[KFULL + s], (t >> 1) & 1, abort_flag, ds)) break;
+      const int s = t % kKStages;
+      if (!mbar_wait(&bars[KFULL + s], (t / kKStages) & 1, abort_flag, ds)) break;
       const TileEntry te = tile_at(p, tr, t);
       if (te.rollout < 0) {
         uint8_t* kt = smem + L::kK + s * L::kKVBytes;
