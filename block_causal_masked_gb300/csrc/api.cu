@@ -101,10 +101,31 @@ struct AttnDesc {
   int32_t* ds;
 };
 
+// One call runs as one launch, or as two when its (row tile, KV head) groups
+// exceed one wave of SMs: a bulk launch of whole waves with one CTA per group,
+// then the remaining groups split wide across the SMs (instead of a second,
+// nearly empty wave of unsplit groups).
+struct AttnPart {
+  int m_tile0, m_tiles, splits;
+};
+
 struct AttnPlan {
-  int G, rows_per_head, m_tiles, n_prefix_tiles, splits;
+  int G, rows_per_head, m_tiles, n_prefix_tiles, splits;  // splits: widest over the parts
+  int n_parts;
+  AttnPart part[2];
+  size_t rope_off;  // workspace offset of the rotated prefix keys (RoPE)
   size_t ws_bytes;
 };
+
+// Widest split count (<= 16, <= the tile count) that keeps `groups` clusters
+// of it resident at once, one CTA per SM.
+int one_wave_splits(long long groups, long long max_tiles) {
+  long long s = kPlanSms / groups;
+  if (s > max_tiles) s = max_tiles;
+  if (s > kAttnMaxSplits) s = kAttnMaxSplits;
+  while (s > 1 && groups > attn_resident_clusters(static_cast<int>(s))) --s;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
 
 bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   if (d.N < 1 || d.n_q < 1 || d.C < 0 || d.Hq < 1 || d.Hkv < 1 || d.priv_len < 0) return BD_ERR_INVALID_ARG;
@@ -129,22 +150,35 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   const long long rolls_per_tile = (kAttnBM - 1) / per_roll + 2 < d.N ? (kAttnBM - 1) / per_roll + 2 : d.N;
   const long long max_tiles = pl->n_prefix_tiles + rolls_per_tile * priv_tiles;
   if (max_tiles > kAttnMaxTiles) return BD_ERR_UNSUPPORTED;
-  int splits = d.num_splits;
-  if (splits == 0) {
+  pl->n_parts = 1;
+  pl->part[0] = {0, pl->m_tiles, d.num_splits};
+  if (d.num_splits == 0) {
     // spread the KV range of every (row tile, KV head) over the SMs as a cluster
     // of up to 16 CTAs, at least one tile each, and keep every cluster of the
     // launch resident at once (one wave): the widest split count whose
     // clusters all fit
-    const long long base = static_cast<long long>(pl->m_tiles) * d.Hkv;
-    long long s = kPlanSms / base;
-    if (s > max_tiles) s = max_tiles;
-    if (s > kAttnMaxSplits) s = kAttnMaxSplits;
-    while (s > 1 && base > attn_resident_clusters(static_cast<int>(s))) --s;
-    splits = s < 1 ? 1 : static_cast<int>(s);
+    const long long groups = static_cast<long long>(pl->m_tiles) * d.Hkv;
+    pl->part[0].splits = one_wave_splits(groups, max_tiles);
+    const long long waves = groups / kPlanSms;
+    const int bulk = static_cast<int>(waves * kPlanSms / d.Hkv);  // whole waves of row tiles
+    if (waves > 0 && bulk > 0 && bulk < pl->m_tiles) {
+      const int tail_splits = one_wave_splits(static_cast<long long>(pl->m_tiles - bulk) * d.Hkv, max_tiles);
+      if (tail_splits > 1) {
+        pl->n_parts = 2;
+        pl->part[0] = {0, bulk, 1};
+        pl->part[1] = {bulk, pl->m_tiles - bulk, tail_splits};
+      }
+    }
   }
+  int splits = 1;
+  for (int i = 0; i < pl->n_parts; ++i) splits = pl->part[i].splits > splits ? pl->part[i].splits : splits;
   pl->splits = splits;
-  // split partials: Hkv * m_tiles blocks of attn_part_bytes(splits, D)
-  pl->ws_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * attn_part_bytes(splits, d.D) : 0;
+  // split partials: Hkv * m_tiles blocks of attn_part_bytes(splits, D); then,
+  // with RoPE, the rotated prefix keys bf16 [Hkv, C, D]
+  const size_t part_bytes = splits > 1 ? static_cast<size_t>(d.Hkv) * pl->m_tiles * attn_part_bytes(splits, d.D) : 0;
+  pl->rope_off = (part_bytes + 255) / 256 * 256;
+  const bool rope = d.rope.enabled && d.C > 0;
+  pl->ws_bytes = rope ? pl->rope_off + static_cast<size_t>(d.Hkv) * d.C * d.D * 2 : part_bytes;
   return BD_OK;
 }
 
@@ -167,8 +201,8 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.lse = d.lse;
   p.part = pl.splits > 1 ? d.ws : nullptr;
   p.m_tiles = pl.m_tiles;
+  p.m_tile0 = 0;
   p.block_start = d.block_start;
-  p.k_pos = d.rope.enabled ? d.rope.k_pos : nullptr;
   p.dev_status = d.ds;
   p.N = d.N;
   p.n_q = d.n_q;
@@ -180,21 +214,36 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.priv_len = d.priv_len;
   p.n_blocks = d.n_blocks;
   p.block_size = d.block_size;
-  p.num_splits = pl.splits;
+  p.num_splits = pl.part[0].splits;
   p.rows_per_head = pl.rows_per_head;
   p.n_prefix_tiles = pl.n_prefix_tiles;
   const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.rope = d.rope.enabled ? 1 : 0;
-  p.delta = d.rope.delta;
-  if (p.rope) {
+  // RoPE: the pre-RoPE prefix keys are rotated once for the whole call into
+  // the workspace, and the attention reads that copy
+  const void* prefix_k = d.pk;
+  long long prefix_k_stride = d.prefix_stride;
+  RopeParams rp;
+  std::memset(&rp, 0, sizeof(rp));
+  const bool rope = d.rope.enabled && d.C > 0;
+  if (rope) {
+    rp.k = d.pk;
+    rp.out = static_cast<char*>(d.ws) + pl.rope_off;
+    rp.k_pos = d.rope.k_pos;
+    rp.Hkv = d.Hkv;
+    rp.C = d.C;
+    rp.D = d.D;
+    rp.delta = d.rope.delta;
+    rp.stride = d.prefix_stride;
     const double two_pi = 6.283185307179586476925286766559;
     for (int i = 0; i < d.D / 2; ++i) {
       const double f = std::pow(static_cast<double>(d.rope.theta), -2.0 * i / d.D);
       double x = f / two_pi;
       x -= std::floor(x);
-      p.rope_turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
+      rp.turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
     }
+    prefix_k = rp.out;
+    prefix_k_stride = d.C;
   }
 
   AttnMaps maps;
@@ -211,8 +260,9 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   }
   if (d.C > 0) {
     const uint64_t dims[3] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.C), static_cast<uint64_t>(d.Hkv)};
+    const uint64_t kstrides[2] = {row_b, static_cast<uint64_t>(prefix_k_stride) * row_b};
     const uint64_t strides[2] = {row_b, static_cast<uint64_t>(d.prefix_stride) * row_b};
-    if ((st = make_kv_map(&maps.pk, d.pk, 3, dims, strides)) != BD_OK) return st;
+    if ((st = make_kv_map(&maps.pk, prefix_k, 3, dims, kstrides)) != BD_OK) return st;
     if ((st = make_kv_map(&maps.pv, d.pv, 3, dims, strides)) != BD_OK) return st;
   }
   {
@@ -223,7 +273,13 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
     if ((st = make_kv_map(&maps.rk, d.rk, 4, dims, strides)) != BD_OK) return st;
     if ((st = make_kv_map(&maps.rv, d.rv, 4, dims, strides)) != BD_OK) return st;
   }
-  return launch_attention(p, maps, pl.m_tiles, stream) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+  if (rope && launch_rope_prefix(rp, stream) != cudaSuccess) return BD_ERR_CUDA;
+  for (int i = 0; i < pl.n_parts; ++i) {
+    p.m_tile0 = pl.part[i].m_tile0;
+    p.num_splits = pl.part[i].splits;
+    if (launch_attention(p, maps, pl.part[i].m_tiles, stream) != cudaSuccess) return BD_ERR_CUDA;
+  }
+  return BD_OK;
 }
 
 AttnDesc desc_of(const bd_attn_args* a) {

@@ -11,22 +11,26 @@
 //   * GQA rows of one KV head are packed: row = (rollout * n_q + i) * G + g, so
 //     one tcgen05.mma with M = 128 serves G query heads of up to 128/G positions;
 //   * warp 0 streams 128-key K and V tiles with TMA (128-byte swizzle) into a
-//     two-stage ring; the prefix tiles come from one shared tensor map and are
-//     reused by every packed row, private tiles from a per-rollout map;
+//     three-stage K ring (a stage is refilled as soon as S of its tile is done)
+//     and a two-stage V ring; the prefix tiles come from one shared tensor map
+//     and are reused by every packed row, private tiles from a per-rollout map;
 //   * warp 1 allocates TMEM and issues S = Q·Kᵀ (into one of two TMEM S buffers)
-//     and O += P·V (O stays in TMEM for the whole KV range), one thread;
-//   * warps 2-5 own one TMEM lane (= one packed row) each thread: masked online
-//     softmax in fp32 from TMEM, P rounded to bf16 into a swizzled smem tile;
-//     the running max is only moved (and O rescaled in TMEM) when it grows by
-//     more than 2^8, so most tiles need no O round trip;
-//   * with RoPE, warps 6-7 rotate each staged prefix K tile in shared memory at
-//     k_pos - delta before the MMA warp may read it (FlashDrive tutorial,
-//     "流式推理"); the angle is reduced exactly in 0.64 fixed-point turns;
+//     and O += P·V (P read from TMEM, O resident in TMEM for the whole KV
+//     range), one thread;
+//   * warps 2-9, two per TMEM lane quadrant, each hold half of the key columns
+//     of their 32 packed rows: masked online softmax in fp32 from TMEM, P
+//     rounded to bf16 and written back into its own S buffer; the running max
+//     is only moved (and O rescaled in TMEM) when it grows by more than 2^8;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
-//     the end every softmax thread writes its row's unnormalised O and (max,
-//     sum) to a workspace that stays in L2, one cluster barrier makes them
+//     the end every softmax thread writes its row's normalised O and (max,
+//     sum) for the CTA that owns the row, one cluster barrier makes them
 //     visible, and each CTA merges 1/S of the rows from all splits and stores
 //     them -- one kernel, no second launch.
+// With RoPE (FlashDrive tutorial, "流式推理"), the cached prefix keys stay
+// pre-RoPE in memory and a small kernel of the same call rotates them at
+// k_pos - delta into a bf16 copy that every row tile then reads -- once per
+// call instead of once per row tile; the angle is reduced exactly in 0.64
+// fixed-point turns.
 // Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
@@ -46,10 +50,9 @@ constexpr int kKStages = 3;  // K ring: a stage is free once S = Q.K^T of its ti
 constexpr int kVStages = 2;  // V ring: a stage is free once P.V of its tile is done
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
-// warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax, then 2 RoPE warps
+// warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax
 constexpr int kSmWarps = 8;
-constexpr int kThreadsPlain = 32 * (2 + kSmWarps);
-constexpr int kThreadsRope = kThreadsPlain + 64;
+constexpr int kThreads = 32 * (2 + kSmWarps);
 
 struct TileEntry {
   int rollout;  // -1: shared prefix tile
@@ -59,7 +62,7 @@ struct TileEntry {
 
 enum Bar : int {
   KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 13, QFULL = 14,
-  KREADY = 15, DRAIN = 18, MERGE_O = 19, NUM_BARS = 20
+  DRAIN = 15, MERGE_O = 16, NUM_BARS = 17
 };
 
 template <int D>
@@ -198,7 +201,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int rpc = attn_merge_rows(S);
   int32_t* ds = p.dev_status;
   uint4* part_o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.part) +
-                                           (static_cast<size_t>(blockIdx.z) * p.m_tiles + blockIdx.y) *
+                                           (static_cast<size_t>(blockIdx.z) * p.m_tiles + p.m_tile0 + blockIdx.y) *
                                                attn_part_bytes(S, D));  // [S][S][kCh][rpc]
   float2* recv_ml = reinterpret_cast<float2*>(smem + L::kMLRecv);         // [S][rpc]
   if (is_sm) {
@@ -304,8 +307,8 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   }
 }
 
-template <int D, bool ROPE>
-__global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.x;
-  const int m0 = blockIdx.y * BM;
+  const int m0 = (p.m_tile0 + blockIdx.y) * BM;
   const int kvh = blockIdx.z;
   int32_t* ds = p.dev_status;
 
@@ -353,7 +356,6 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars[KFULL + i], 1);
       mbar_init(&bars[KEMPTY + i], 1);
-      mbar_init(&bars[KREADY + i], 64);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bars[VFULL + i], 1);
@@ -437,10 +439,9 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
       auto issue_s = [&](int u) -> bool {
         const int s = u & 1;
         const int ks = u % kKStages;
-        uint64_t* kb = ROPE ? &bars[KREADY + ks] : &bars[KFULL + ks];
         // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
         // point by this thread, and executed in issue order -- has consumed
-        if (!mbar_wait(kb, (u / kKStages) & 1, abort_flag, ds)) return false;
+        if (!mbar_wait(&bars[KFULL + ks], (u / kKStages) & 1, abort_flag, ds)) return false;
         tc_fence_after();
         const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
 #pragma unroll
@@ -641,44 +642,6 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
         p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
             l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
-  } else if (ROPE) {
-    // ---------------------------------------------------------------- RoPE on staged prefix keys
-    const int kr0 = threadIdx.x - 32 * (2 + kSmWarps);  // this thread rotates key rows kr0 and kr0 + 64 of the tile
-    for (int t = 0; t < nt; ++t) {
-      const int s = t % kKStages;
-      if (!mbar_wait(&bars[KFULL + s], (t / kKStages) & 1, abort_flag, ds)) break;
-      const TileEntry te = tile_at(p, tr, t);
-      if (te.rollout < 0) {
-        uint8_t* kt = smem + L::kK + s * L::kKVBytes;
-        for (int kr = kr0; kr < BN; kr += 64) {
-          const int key = te.key0 + kr;
-          if (key >= p.C) break;
-          const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
-#pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            uint4* a4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8, BN));
-            uint4* b4 = reinterpret_cast<uint4*>(kt + sw128_offset(kr, c * 8 + D / 2, BN));
-            uint4 xa = *a4, xb = *b4;
-            uint32_t* wa = reinterpret_cast<uint32_t*>(&xa);
-            uint32_t* wb = reinterpret_cast<uint32_t*>(&xb);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              float a0, a1, b0, b1, c0, s0, c1, s1;
-              bf16x2_unpack(wa[w], a0, a1);
-              bf16x2_unpack(wb[w], b0, b1);
-              rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w], c0, s0);
-              rope_cos_sin(pos, p.rope_turns[c * 8 + 2 * w + 1], c1, s1);
-              wa[w] = pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-              wb[w] = pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
-            }
-            *a4 = xa;
-            *b4 = xb;
-          }
-        }
-        fence_proxy_async_smem();
-      }
-      mbar_arrive(&bars[KREADY + s]);
-    }
   }
 
   if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run, bars, abort_flag);
@@ -691,11 +654,11 @@ __global__ void __launch_bounds__(ROPE ? kThreadsRope : kThreadsPlain, 1)
   }
 }
 
-template <int D, bool ROPE>
+template <int D>
 cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
   static bool configured = false;
   const int smem = attn_smem_bytes(D);
-  auto kernel = attn_kernel<D, ROPE>;
+  auto kernel = attn_kernel<D>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -704,7 +667,7 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
-  cfg.blockDim = dim3(ROPE ? kThreadsRope : kThreadsPlain);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   for (;;) {
@@ -728,6 +691,61 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
+// Rotates the cached prefix keys [0, C) of every KV head at k_pos - delta into
+// a contiguous bf16 copy [Hkv, C, D] (FlashDrive tutorial, "流式推理": the cache
+// stays pre-RoPE; the operator applies the rotation at the re-based
+// positions).  One thread per (KV head, key, 8 rotation pairs): the pairs
+// (d, d + D/2) for d in [8 c, 8 c + 8).
+template <int D>
+__global__ void __launch_bounds__(256) rope_prefix_kernel(const __grid_constant__ RopeParams p) {
+  constexpr int kChunks = D / 16;  // 8-pair chunks of a key row
+  pdl_wait();
+  pdl_trigger();
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(p.Hkv) * p.C * kChunks;
+  if (i >= total) return;
+  const int c = static_cast<int>(i % kChunks);
+  const long long row = i / kChunks;  // kvh * C + key
+  const int key = static_cast<int>(row % p.C);
+  const int kvh = static_cast<int>(row / p.C);
+  const __nv_bfloat16* src =
+      static_cast<const __nv_bfloat16*>(p.k) + (static_cast<size_t>(kvh) * p.stride + key) * D;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * D;
+  const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
+  uint4 xa = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
+  uint4 xb = __ldg(reinterpret_cast<const uint4*>(src + c * 8 + D / 2));
+  uint32_t* wa = reinterpret_cast<uint32_t*>(&xa);
+  uint32_t* wb = reinterpret_cast<uint32_t*>(&xb);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float a0, a1, b0, b1, c0, s0, c1, s1;
+    bf16x2_unpack(wa[w], a0, a1);
+    bf16x2_unpack(wb[w], b0, b1);
+    rope_cos_sin(pos, p.turns[c * 8 + 2 * w], c0, s0);
+    rope_cos_sin(pos, p.turns[c * 8 + 2 * w + 1], c1, s1);
+    wa[w] = pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+    wb[w] = pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+  }
+  *reinterpret_cast<uint4*>(dst + c * 8) = xa;
+  *reinterpret_cast<uint4*>(dst + c * 8 + D / 2) = xb;
+}
+
+template <int D>
+cudaError_t launch_rope_t(const RopeParams& p, cudaStream_t stream) {
+  const long long total = static_cast<long long>(p.Hkv) * p.C * (D / 16);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>((total + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, rope_prefix_kernel<D>, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 }  // namespace
 
 int attn_smem_bytes(int D) {
@@ -736,10 +754,12 @@ int attn_smem_bytes(int D) {
 }
 
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
-  if (p.D == 128) return p.rope ? launch_attn_t<128, true>(p, maps, m_tiles, stream)
-                                : launch_attn_t<128, false>(p, maps, m_tiles, stream);
-  return p.rope ? launch_attn_t<64, true>(p, maps, m_tiles, stream)
-                : launch_attn_t<64, false>(p, maps, m_tiles, stream);
+  return p.D == 128 ? launch_attn_t<128>(p, maps, m_tiles, stream) : launch_attn_t<64>(p, maps, m_tiles, stream);
+}
+
+cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream) {
+  if (p.Hkv < 1 || p.C < 1) return cudaSuccess;
+  return p.D == 128 ? launch_rope_t<128>(p, stream) : launch_rope_t<64>(p, stream);
 }
 
 }  // namespace bd

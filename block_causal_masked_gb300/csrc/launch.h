@@ -43,18 +43,25 @@ struct AttnParams {
   void* o;                // bf16 [N, n_q, Hq, D]
   float* lse;             // fp32 [N, Hq, n_q] or null
   void* part;             // split partials (splits > 1): [Hkv, m_tiles] blocks of attn_part_bytes
-  int m_tiles;
+  int m_tiles;            // row tiles per KV head (all launches of the call)
+  int m_tile0;            // first row tile of this launch (grid y counts from here)
   const int32_t* block_start;  // [n_blocks + 1] or null (uniform block_size)
-  const int32_t* k_pos;        // [C] or null
   int32_t* dev_status;
   int N, n_q, Hq, Hkv, G, D, C, priv_len, n_blocks, block_size, num_splits;
   int rows_per_head;      // N * n_q * G
   int n_prefix_tiles;     // ceil(C / BN)
   float scale_log2;       // sm_scale * log2(e)
-  int rope;
-  int delta;
   int q_tma;              // Q tile by TMA (G divides 128)
-  unsigned long long rope_turns[64];  // theta^(-2d/D) / (2*pi) as a 0.64 fixed-point fraction
+};
+
+// Rotation of the cached prefix keys before attention (RoPE at k_pos - delta).
+struct RopeParams {
+  const void* k;          // bf16 [Hkv, stride, D], rows [0, C) rotated
+  void* out;              // bf16 [Hkv, C, D]
+  const int32_t* k_pos;   // [C] or null (position = key index)
+  int Hkv, C, D, delta;
+  long long stride;
+  unsigned long long turns[64];  // theta^(-2d/D) / (2*pi) as a 0.64 fixed-point fraction
 };
 
 struct AttnMaps {
@@ -65,6 +72,7 @@ struct AttnMaps {
 
 int attn_smem_bytes(int D);
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream);
+cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- vocab reductions
 

@@ -83,7 +83,10 @@ typedef enum bd_status {
  * With enabled != 0, cached prefix key s is rotated at position k_pos[s] - delta
  * before Q·Kᵀ, rotate-half over the pairs (d, d + D/2) with frequency
  * theta^(-2d/D).  The rotated key enters the bf16 product as bf16.  Queries and
- * the active positions' own keys must already be rotated by the caller.
+ * the active positions' own keys must already be rotated by the caller.  The
+ * cache itself is never modified: the call rotates the prefix keys once into
+ * its workspace (Hkv * C * D * 2 bytes more, counted by bd_*_workspace_size)
+ * and every row tile reads that copy.
  *   k_pos  device int32 [C], or NULL for k_pos[s] = s
  * ---------------------------------------------------------------------------*/
 typedef struct bd_rope {
@@ -119,7 +122,9 @@ typedef struct bd_rope {
  *   sm_scale     0 -> D^-1/2
  *   num_splits   KV splits (1..16): the CTAs of one thread-block cluster, whose
  *                partial rows meet in the workspace (in L2); 0 -> chosen by the
- *                library.  With one split no workspace is needed (NULL is fine)
+ *                library, which may also run the call as two launches (whole
+ *                waves of unsplit row tiles, then the rest split wide).  With
+ *                one split and no RoPE no workspace is needed (NULL is fine)
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= n_q; 0 <= C; kv_stride >= C + n_q.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_attn_args {
