@@ -340,6 +340,352 @@ def run_wam_sweep(args, device):
         torch.cuda.empty_cache()
 
 
+# ------------------------------------------------------------------------------ the other workloads
+
+def _graph(fn):
+    """fn's launches captured as one CUDA graph (fn runs once first, outside the
+    capture, to size workspaces and set kernel attributes)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def _replay_ms(g, reps: int, flush, before=None):
+    """Median CUDA-event time of `reps` replays, L2 flushed (and `before` run)
+    outside the timed region before each."""
+    import torch
+    ms = []
+    for _ in range(reps):
+        if before is not None:
+            before()
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms)
+
+
+def _copies(bytes_per_call: int) -> int:
+    """Independent input copies for timing a vocabulary kernel back to back:
+    enough that the copies together exceed L2, at most 16, at most ~2 GB."""
+    return int(max(1, min(16, (2 << 30) // max(1, bytes_per_call))))
+
+
+def _attn_visible(C: int, block_start, causal: bool = False) -> int:
+    """Visible keys summed over the active positions (block-causal, or causal)."""
+    n_q = int(block_start[-1])
+    if causal:
+        return sum(C + i + 1 for i in range(n_q))
+    tot = 0
+    for b in range(len(block_start) - 1):
+        lo, hi = int(block_start[b]), int(block_start[b + 1])
+        tot += (hi - lo) * (C + hi)
+    return tot
+
+
+def _attn_roof(us: float, nbytes: float, flops: float, peaks, sustained: bool):
+    """Roofline entry of one attention launch: HBM or tensor bound, whichever
+    bound is slower at the measured peaks."""
+    hbm = peaks["hbm_gbs"] if peaks else 6800.0
+    tf = (peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") if peaks else None) or \
+        (1700.0 if sustained else 1900.0)
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (tf * 1e12)
+    if t_tc > t_hbm:
+        ach = flops / (us * 1e-6) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s", "frac": ach / tf,
+                "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes, "avg_launch_us": us}
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes, "avg_launch_us": us}
+
+
+def _vocab_roof(us: float, nbytes: float, peaks):
+    hbm = peaks["hbm_gbs"] if peaks else 6800.0
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "alg_bytes_per_launch": nbytes, "avg_launch_us": us}
+
+
+def _extra_line(workload: str, tokens_per_step: float, step_ms: float, args, kernels: dict, extra: dict):
+    line = {"metric": METRIC, "value": tokens_per_step / step_ms * 1e3, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload, "l2": "flushed (256 MiB write) before every timed step",
+                       "timing": "median of CUDA-event timed graph replays"},
+            "committed_per_step": tokens_per_step, "roofline": kernels}
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+class _Window:
+    """State and tokens of one decode window on the device, `copies` times
+    (independent copies for timing a vocabulary kernel back to back), reset to
+    their initial values outside timed regions."""
+
+    def __init__(self, state0: np.ndarray, tokens0: np.ndarray, copies: int, dev):
+        import torch
+        self.s0 = torch.from_numpy(np.ascontiguousarray(state0, dtype=np.uint8)).to(dev)
+        self.t0 = torch.from_numpy(np.ascontiguousarray(tokens0, dtype=np.int32)).to(dev)
+        self.state = [self.s0.clone() for _ in range(copies)]
+        self.tokens = [self.t0.clone() for _ in range(copies)]
+
+    def reset(self):
+        for s, t in zip(self.state, self.tokens):
+            s.copy_(self.s0)
+            t.copy_(self.t0)
+
+
+def _unmask_outs(n_pos: int, n_blocks: int, dev):
+    import torch
+    return dict(commit=torch.empty(n_pos, dtype=torch.uint8, device=dev),
+                n_committed=torch.empty(n_blocks, dtype=torch.int32, device=dev),
+                status=torch.empty(n_blocks, dtype=torch.int32, device=dev),
+                pred=torch.empty(n_pos, dtype=torch.int32, device=dev),
+                conf=torch.empty(n_pos, dtype=torch.float32, device=dev),
+                lse=torch.empty(n_pos, dtype=torch.float32, device=dev))
+
+
+def _per_launch_us(calls, reset, flush, reps: int) -> float:
+    """Per-launch time of `calls` (independent launches, own inputs and outputs
+    each) captured back to back in one graph."""
+    def run():
+        for c in calls:
+            c()
+    g = _graph(run)
+    return _replay_ms(g, reps, flush, before=reset) * 1e3 / len(calls)
+
+
+def run_tiny(args, dev):
+    """Tiny workload, one round: block-causal attention (1 layer, 4/2 heads,
+    head dim 64, prefix 256, two blocks of 8 with 3 scaffold each), unmask of the
+    16 positions (fp32 logits [16, 1024] ~ N(0, 2), tau 0.9, at least 1/4 of the
+    remaining per block, draft of the rest), causal AR attention, verify of the
+    draft against AR rows [11, 1024] that agree with it on a seeded prefix."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    T = synth.TINY
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    lay = synth.uniform_layout(16, 8, scaffold_per_block=3, seed=T.seed)
+    bs = [0, 8, 16]
+    a = synth.attn_case(T.seed, 0, C=T.prefix, block_start=bs, Hq=T.Hq, Hkv=T.Hkv, D=T.D)
+    q_ar = synth.attn_case(T.seed, 1000, C=0, block_start=bs, Hq=T.Hq, Hkv=1, D=T.D).q
+    logits = synth.normal_logits(T.seed, 1, 16, T.V, sigma=2.0, bf16=False)
+    edit = np.flatnonzero(lay.scaffold == 0)
+    E = len(edit)
+    g = synth.rng(T.seed, 77)
+    k = int(g.integers(0, E + 1))
+    want = g.integers(0, T.V, size=E + 1)
+    want[:k] = np.argmax(logits[edit], axis=1)[:k]          # the draft's tokens on a seeded prefix
+    if k < E:
+        want[k] = (np.argmax(logits[edit[k]]) + 1) % T.V
+    ar, _, _ = synth.planted_logits(T.seed, 2, E + 1, T.V, sigma=2.0, tokens=want, bf16=False)
+    state0 = np.where(lay.scaffold == 1, synth.SCAFFOLD, synth.MASKED)
+    tokens0 = np.where(lay.scaffold == 1, 11, -1)
+    t = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(dt)  # noqa: E731
+    bf = torch.bfloat16
+    q, k_, v, qa = t(a.q, bf), t(a.k, bf), t(a.v, bf), t(q_ar, bf)
+    lg, arl = t(logits, torch.float32), t(ar[None], torch.float32)
+    blk = torch.tensor(bs, dtype=torch.int32, device=dev)
+    row = torch.arange(16, dtype=torch.int32, device=dev)
+    copies = 16
+    win = _Window(state0, tokens0, copies, dev)
+    outs = [_unmask_outs(16, 2, dev) for _ in range(copies)]
+    acc = [torch.empty(1, dtype=torch.int32, device=dev) for _ in range(copies)]
+    o = torch.empty((16, T.Hq, T.D), dtype=bf, device=dev)
+    lse = torch.empty((T.Hq, 16), dtype=torch.float32, device=dev)
+    kw = dict(tau_full=0.9, tau_half=0.9, min_frac=(1, 4), k_fixed=0, add_thr=(0, 1), act_thr=(0, 1),
+              write_draft=True)
+
+    def attn_mdm():
+        bd.bd_block_causal_attn(q, k_, v, T.prefix, block_start=blk, o=o, lse=lse)
+
+    def attn_ar():
+        bd.bd_block_causal_attn(qa, k_, v, T.prefix, block_size=1, o=o, lse=lse)
+
+    def unmask(i=0):
+        bd.bd_unmask_step(lg, row, blk, win.state[i], win.tokens[i], **kw, **outs[i])
+
+    def verify(i=0):
+        bd.bd_spec_verify(win.tokens[i].view(1, -1), win.state[i].view(1, -1), arl, accepted_len=acc[i])
+
+    round_g = _graph(lambda: (attn_mdm(), unmask(), attn_ar(), verify()))
+    for _ in range(args.warmup):
+        win.reset()
+        round_g.replay()
+    step_ms = _replay_ms(round_g, args.steps, flush, before=win.reset)
+    committed = int(outs[0]["n_committed"].sum()) + int(acc[0][0])
+    attn_us = _replay_ms(_graph(lambda: (attn_mdm(), attn_ar())), args.steps, flush) * 1e3 / 2
+    um_us = _per_launch_us([lambda i=i: unmask(i) for i in range(copies)], win.reset, flush, args.steps)
+    vf_us = _per_launch_us([lambda i=i: verify(i) for i in range(copies)], win.reset, flush, args.steps)
+    peaks = measured_peaks()
+    vis = (_attn_visible(T.prefix, bs) + _attn_visible(T.prefix, bs, causal=True)) / 2
+    nbytes = 2 * T.Hkv * (T.prefix + 16) * T.D * 2 + 2 * 16 * T.Hq * T.D * 2 + 16 * T.Hq * 4
+    n_masked = int((state0 == synth.MASKED).sum())
+    kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * T.D * T.Hq * vis, peaks, False),
+               "unmask_kernel": _vocab_roof(um_us, n_masked * T.V * 4, peaks),
+               "verify_kernel": _vocab_roof(vf_us, (E + 1) * T.V * 4, peaks)}
+    _extra_line("tiny: 1 layer, 4/2 heads, head dim 64, prefix 256, 2 blocks of 8 (3 scaffold each), "
+                "fp32 logits [16, 1024]; one round (attention, unmask tau 0.9 + 1/4 + draft, causal AR "
+                "attention, verify)", committed, step_ms, args, kernels, {"gpu_launches_per_step": 4})
+
+
+def run_fast_dvla(args, dev):
+    """Fast-dVLA pipelined decode, one denoise step of the 3-block window:
+    36 x attention (16/2 heads, head dim 128, prefix 512 image + 88 instruction
+    + the 14 action tokens of the two finished blocks, window of three 7-token
+    blocks) and one unmask over the window's masked positions (masked ratios
+    2/7, 4/7, 7/7; half activation at 1/2 with tau 0.9, full at 0.85 with tau
+    0.9 and at least 1/4 of the remaining)."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    F = synth.FAST_DVLA
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    C, bs, n_q = F.prefix + 14, [0, 7, 14, 21], 21
+    g0 = synth.rng(F.seed, 7)
+    state0 = np.zeros(n_q, np.int64)
+    state0[g0.choice(7, 5, replace=False)] = synth.COMMITTED
+    state0[7 + g0.choice(7, 3, replace=False)] = synth.COMMITTED
+    tokens0 = np.where(state0 == synth.COMMITTED, 5, -1)
+    masked = np.flatnonzero(state0 == synth.MASKED)
+    logit_row = np.full(n_q, -1, np.int32)
+    logit_row[masked] = np.arange(len(masked))
+    logits, _, _ = synth.planted_logits(F.seed, 1, len(masked), F.V)
+    bf = torch.bfloat16
+    t = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(dt)  # noqa: E731
+    layers = []
+    for l in range(F.layers):
+        a = synth.attn_case(F.seed, l, C=C, block_start=bs, Hq=F.Hq, Hkv=F.Hkv, D=F.D, text_from=512)
+        layers.append((t(a.q, bf), t(a.k, bf), t(a.v, bf)))
+    copies = _copies(len(masked) * F.V * 2)
+    lg = [t(logits, bf) for _ in range(copies)]
+    row = t(logit_row, torch.int32)
+    blk = torch.tensor(bs, dtype=torch.int32, device=dev)
+    win = _Window(state0, tokens0, copies, dev)
+    outs = [_unmask_outs(n_q, 3, dev) for _ in range(copies)]
+    o = torch.empty((n_q, F.Hq, F.D), dtype=bf, device=dev)
+    lse = torch.empty((F.Hq, n_q), dtype=torch.float32, device=dev)
+    kw = dict(tau_full=0.9, tau_half=0.9, min_frac=(1, 4), k_fixed=0, add_thr=(1, 2), act_thr=(17, 20))
+
+    def attn():
+        for q, k, v in layers:
+            bd.bd_block_causal_attn(q, k, v, C, block_start=blk, o=o, lse=lse)
+
+    def unmask(i=0):
+        bd.bd_unmask_step(lg[i], row, blk, win.state[i], win.tokens[i], **kw, **outs[i])
+
+    step_g = _graph(lambda: (attn(), unmask()))
+    for _ in range(args.warmup):
+        win.reset()
+        step_g.replay()
+    step_ms = _replay_ms(step_g, args.steps, flush, before=win.reset)
+    committed = int(outs[0]["n_committed"].sum())
+    attn_us = _replay_ms(_graph(attn), args.steps, flush) * 1e3 / F.layers
+    um_us = _per_launch_us([lambda i=i: unmask(i) for i in range(copies)], win.reset, flush, args.steps)
+    peaks = measured_peaks()
+    nbytes = 2 * F.Hkv * (C + n_q) * F.D * 2 + 2 * n_q * F.Hq * F.D * 2 + n_q * F.Hq * 4
+    kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * F.D * F.Hq * _attn_visible(C, bs), peaks, True),
+               "unmask_kernel": _vocab_roof(um_us, len(masked) * F.V * 2, peaks)}
+    _extra_line(f"fast_dvla: 16/2 heads, head dim 128, 36 layers, prefix {C} keys, window of 3 blocks x 7 "
+                f"({len(masked)} masked), vocab 151936; one denoise step (36 attention layers + unmask)",
+                committed, step_ms, args, kernels,
+                {"gpu_launches_per_step": F.layers + 1, "block_status": outs[0]["status"].tolist()})
+
+
+def run_fork(args, dev):
+    """Shared-prefix fork + streaming cache, one scaffold-speculative round of
+    the second trajectory block for N = 1, 8, 32 rollouts: 36 x
+    bd_fork_rollouts (MDM pass, the 39-position block bidirectional; 41 private
+    rows of the first trajectory block before it; 4,306 pre-RoPE prefix keys in
+    view-major order rotated at k_pos - 256), 36 x bd_fork_rollouts (AR pass,
+    causal), then the sampled verifier over the N rollouts (AR rows [N, 33,
+    151936] bf16 with Gumbel noise fp32).  Inputs are drawn on the device from
+    a seeded generator; every rollout's AR rows agree with its draft on a
+    seeded number of slots."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    S = synth.FORK_STREAM
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    C, n_q, priv_len, L, E = S.prefix, 39, 41, 39, 32
+    k_pos = torch.from_numpy(synth.streaming_prefix_positions()).to(dev)
+    rope = dict(k_pos=k_pos, delta=256, theta=1e4)
+    bf = torch.bfloat16
+    for N in (1, 8, 32):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(S.seed * 1000 + N)
+        rn = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(bf)  # noqa: E731
+        layers = [(rn(N, n_q, S.Hq, S.D), rn(N, n_q, S.Hq, S.D), rn(S.Hkv, C, S.D), rn(S.Hkv, C, S.D),
+                   rn(N, S.Hkv, priv_len + n_q, S.D), rn(N, S.Hkv, priv_len + n_q, S.D)) for _ in range(S.layers)]
+        blk = torch.tensor([0, n_q], dtype=torch.int32, device=dev)
+        o = torch.empty((N, n_q, S.Hq, S.D), dtype=bf, device=dev)
+        lse = torch.empty((N, S.Hq, n_q), dtype=torch.float32, device=dev)
+        # verify inputs: scaffold slots, drafts, AR rows planted to agree on k_r slots, uniforms
+        g = synth.rng(S.seed, 999, N)
+        scaf = np.zeros(L, np.int64)
+        scaf[g.choice(L, L - E, replace=False)] = 1
+        state0 = np.tile(np.where(scaf == 1, synth.SCAFFOLD, synth.MASKED), (N, 1))
+        drafts = g.integers(0, S.V, size=(N, L))
+        kr = g.integers(0, E + 1, size=N)
+        ar = (torch.randn((N, E + 1, S.V), generator=gen, device=dev) * 3.0)
+        ed = np.flatnonzero(scaf == 0)
+        for r in range(N):
+            for e in range(int(kr[r])):
+                ar[r, e, int(drafts[r, ed[e]])] = 60.0
+            if kr[r] < E:
+                ar[r, int(kr[r]), (int(drafts[r, ed[kr[r]]]) + 1) % S.V] = 60.0
+        ar = ar.to(bf)
+        u = torch.rand((N, E + 1, S.V), generator=gen, device=dev).clamp_(2.0 ** -24, 1.0 - 2.0 ** -24)
+        copies = _copies(N * (E + 1) * S.V * 6)
+        ars = [ar] + [ar.clone() for _ in range(copies - 1)]
+        us = [u] + [u.clone() for _ in range(copies - 1)]
+        win = _Window(state0, drafts, copies, dev)
+        accs = [torch.empty(N, dtype=torch.int32, device=dev) for _ in range(copies)]
+        acc = accs[0]
+
+        def mdm():
+            for q, _, pk, pv, rk, rv in layers:
+                bd.bd_fork_rollouts(q, pk, pv, rk, rv, priv_len, C, block_start=blk, o=o, lse=lse, rope=rope)
+
+        def ar_pass():
+            for _, q, pk, pv, rk, rv in layers:
+                bd.bd_fork_rollouts(q, pk, pv, rk, rv, priv_len, C, block_size=1, o=o, lse=lse, rope=rope)
+
+        def verify(i=0):
+            bd.bd_spec_verify(win.tokens[i], win.state[i], ars[i], us[i], 1.0, accepted_len=accs[i])
+
+        round_g = _graph(lambda: (mdm(), ar_pass(), verify()))
+        reps = max(3, args.steps // (1 + N // 4))
+        for _ in range(args.warmup):
+            win.reset()
+            round_g.replay()
+        step_ms = _replay_ms(round_g, reps, flush, before=win.reset)
+        committed = int(acc.sum())
+        attn_us = _replay_ms(_graph(lambda: (mdm(), ar_pass())), reps, flush) * 1e3 / (2 * S.layers)
+        vf_us = _per_launch_us([lambda i=i: verify(i) for i in range(copies)], win.reset, flush, reps)
+        peaks = measured_peaks()
+        vis = N * (_attn_visible(C + priv_len, [0, n_q]) + _attn_visible(C + priv_len, [0, n_q], causal=True)) / 2
+        nbytes = (2 * S.Hkv * C * S.D * 2 + N * 2 * S.Hkv * (priv_len + n_q) * S.D * 2
+                  + 2 * N * n_q * S.Hq * S.D * 2 + N * n_q * S.Hq * 4)
+        kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * S.D * S.Hq * vis, peaks, True),
+                   "verify_kernel": _vocab_roof(vf_us, N * (E + 1) * S.V * (2 + 4), peaks)}
+        _extra_line(f"fork_streaming N={N}: 16/2 heads, head dim 128, 36 layers, 4306 pre-RoPE prefix keys "
+                    f"(RoPE at k_pos - 256), trajectory block of 39 positions after 41 private rows per rollout; "
+                    f"one round (MDM fork, causal AR fork, sampled verify of {N} rollouts)",
+                    committed, step_ms, args, kernels,
+                    {"gpu_launches_per_step": "2 x 36 x (RoPE pass + attention) + 1", "rollouts": N})
+        del layers, ar, u, ars, us
+        torch.cuda.empty_cache()
+
+
 def algorithmic(inp):
     """Bytes (and FLOPs) the round must move: visible K/V, Q, O, LSE per layer;
     logits rows of masked editable positions; AR rows."""
@@ -525,6 +871,31 @@ def aggregate(seconds: float, tokens: float, world: int, device="cpu"):
     return float(t[0]), float(c[0])
 
 
+def vocab_times(rd, inp, device, reps: int):
+    """Per-launch us of the round's unmask and verify calls, each timed as 16
+    independent calls (own logits copy, state and tokens) in one graph."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    copies = 16
+    n_q = inp["n_q"]
+    win = _Window(inp["state"], inp["tokens"], copies, device)
+    lgs = [rd.logits] + [rd.logits.clone() for _ in range(copies - 1)]
+    ars = [rd.ar_logits] + [rd.ar_logits.clone() for _ in range(copies - 1)]
+    outs = [_unmask_outs(n_q, 1, device) for _ in range(copies)]
+    accs = [torch.empty(1, dtype=torch.int32, device=device) for _ in range(copies)]
+
+    def unmask(i):
+        bd.bd_unmask_step(lgs[i], rd.logit_row, rd.block, win.state[i], win.tokens[i], tau_full=TAU, tau_half=TAU,
+                          min_frac=(0, 1), k_fixed=0, write_draft=True, **outs[i])
+
+    def verify(i):
+        bd.bd_spec_verify(win.tokens[i].view(1, -1), win.state[i].view(1, -1), ars[i], accepted_len=accs[i])
+
+    um = _per_launch_us([lambda i=i: unmask(i) for i in range(copies)], win.reset, rd.flush, reps)
+    vf = _per_launch_us([lambda i=i: verify(i) for i in range(copies)], win.reset, rd.flush, reps)
+    return um, vf
+
+
 def replica_seed(rank: int) -> int:
     """Seed of the request rank `rank` decodes (independent inputs per replica)."""
     return W.seed + 100 * rank
@@ -550,12 +921,15 @@ def run_gpu(args, rank, world, local_rank):
         steps_ms.append(rd.timed_step())
         committed += rd.committed()
     torch.cuda.synchronize()
-    # per-kernel times for the roofline: the same round as four graphs
-    attn_ms, unmask_ms = [], []
-    for _ in range(max(3, min(50, args.steps // 4))):
-        _, a, u = rd.timed_parts()
+    # per-kernel times for the roofline: the attention from the round replayed
+    # as four graphs (72 launches in its two attention parts); the vocabulary
+    # kernels from 16 independent calls back to back (own logits copies)
+    attn_ms = []
+    reps = max(3, min(50, args.steps // 4))
+    for _ in range(reps):
+        _, a, _ = rd.timed_parts()
         attn_ms.append(a)
-        unmask_ms.append(u)
+    unmask_us, verify_us = vocab_times(rd, inp, device, reps)
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_s = sum(steps_ms) / 1e3
@@ -569,7 +943,7 @@ def run_gpu(args, rank, world, local_rank):
     attn_bytes = (alg["attn_bytes"][0] + alg["attn_bytes"][1]) / 2
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
     achieved = attn_bytes / attn_launch_s / 1e9
-    unmask_s = (sum(unmask_ms) / len(unmask_ms)) / 1e3
+    unmask_s = unmask_us / 1e6
     splits = rd.attn_splits()
     launches_per_step = 2 * W.layers + 2
     line = {
@@ -592,7 +966,10 @@ def run_gpu(args, rank, world, local_rank):
                      "alg_bytes_per_launch": attn_bytes, "avg_launch_us": attn_launch_s * 1e6,
                      "unmask": {"alg_bytes": alg["unmask_bytes"], "us": unmask_s * 1e6,
                                 "achieved_gbs": alg["unmask_bytes"] / unmask_s / 1e9,
-                                "frac": alg["unmask_bytes"] / unmask_s / 1e9 / hbm}},
+                                "frac": alg["unmask_bytes"] / unmask_s / 1e9 / hbm},
+                     "verify": {"alg_bytes": alg["verify_bytes"], "us": verify_us,
+                                "achieved_gbs": alg["verify_bytes"] / verify_us / 1e3,
+                                "frac": alg["verify_bytes"] / verify_us / 1e3 / hbm}},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -626,16 +1003,22 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep"], default="fast_ddrive",
-                    help="wam_sweep: the whole WAM-Diff2 decode per block size as one CUDA graph (extra lines)")
+    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork"],
+                    default="fast_ddrive",
+                    help="fast_ddrive: the contract's line; the others print extra lines: wam_sweep (the whole "
+                         "WAM-Diff2 decode per block size as one CUDA graph), tiny, fast_dvla (one denoise step of "
+                         "the 3-block window), fork (one round for N = 1, 8, 32 rollouts)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.workload == "wam_sweep":
-        run_wam_sweep(args, int(os.environ.get("LOCAL_RANK", "0")))
+    extra = {"wam_sweep": run_wam_sweep, "tiny": run_tiny, "fast_dvla": run_fast_dvla, "fork": run_fork}
+    if args.workload in extra:
+        import torch
+        torch.cuda.set_device(local_rank)
+        extra[args.workload](args, f"cuda:{local_rank}")
         return 0
     if args.impl == "reference":
         if rank == 0:
