@@ -9,7 +9,9 @@ explanation block of the 404-position scaffolded output (33 positions: 32
 editable + 1 scaffold); vocabulary 151,936.
 
 One step = one scaffold-speculative round on the active block, all through the
-library's C ABI:
+library's C ABI (the attention calls declare the cached prefix ready, so each
+launch starts fetching it while the previous kernel finishes: the KV cache is
+written before a round, never inside it):
   36 x bd_block_causal_attn   (MDM forward, the block bidirectional)
   1  x bd_unmask_step         (argmax / confidence of the 32 editable rows, tau =
                                0.9 commits, draft of the rest)
@@ -128,7 +130,7 @@ class GpuRound:
     def mdm(self):
         for l in range(W.layers):
             self.bd.bd_block_causal_attn(self.q[l], self.k[l], self.v[l], self.inp["C"], block_start=self.block,
-                                         o=self.o, lse=self.lse)
+                                         o=self.o, lse=self.lse, prefix_ready=True)
 
     def unmask(self):
         self.bd.bd_unmask_step(self.logits, self.logit_row, self.block, self.state, self.tokens, tau_full=TAU,
@@ -137,7 +139,7 @@ class GpuRound:
     def ar(self):
         for l in range(W.layers):
             self.bd.bd_block_causal_attn(self.q_ar[l], self.k[l], self.v[l], self.inp["C"], block_size=1,
-                                         o=self.o, lse=self.lse)
+                                         o=self.o, lse=self.lse, prefix_ready=True)
 
     def verify(self):
         self.bd.bd_spec_verify(self.tokens.view(1, -1), self.state.view(1, -1), self.ar_logits,
@@ -273,7 +275,8 @@ class WamDecode:
         C = WAM.prefix + b * B
         for l in range(self.layers):
             bd.bd_block_causal_attn(self.q[l], self.kk[l], self.vv[l], C, block_start=self.block, o=self.o,
-                                    lse=self.lse, num_splits=self.num_splits, dev_status=self.dev_status)
+                                    lse=self.lse, num_splits=self.num_splits, dev_status=self.dev_status,
+                                    prefix_ready=True)
         bd.bd_unmask_step(self.logits[b, s], self.logit_row, self.block, self.state[b * B:(b + 1) * B],
                           self.tokens[b * B:(b + 1) * B], tau_full=2.0, tau_half=2.0, min_frac=(0, 1),
                           k_fixed=self.k, add_thr=(1, 2), act_thr=(17, 20), dev_status=self.dev_status, **self.um)
@@ -507,10 +510,10 @@ def run_tiny(args, dev):
               write_draft=True)
 
     def attn_mdm():
-        bd.bd_block_causal_attn(q, k_, v, T.prefix, block_start=blk, o=o, lse=lse)
+        bd.bd_block_causal_attn(q, k_, v, T.prefix, block_start=blk, o=o, lse=lse, prefix_ready=True)
 
     def attn_ar():
-        bd.bd_block_causal_attn(qa, k_, v, T.prefix, block_size=1, o=o, lse=lse)
+        bd.bd_block_causal_attn(qa, k_, v, T.prefix, block_size=1, o=o, lse=lse, prefix_ready=True)
 
     def unmask(i=0):
         bd.bd_unmask_step(lg, row, blk, win.state[i], win.tokens[i], **kw, **outs[i])
@@ -578,7 +581,7 @@ def run_fast_dvla(args, dev):
 
     def attn():
         for q, k, v in layers:
-            bd.bd_block_causal_attn(q, k, v, C, block_start=blk, o=o, lse=lse)
+            bd.bd_block_causal_attn(q, k, v, C, block_start=blk, o=o, lse=lse, prefix_ready=True)
 
     def unmask(i=0):
         bd.bd_unmask_step(lg[i], row, blk, win.state[i], win.tokens[i], **kw, **outs[i])

@@ -43,7 +43,7 @@ class bd_attn_args(ct.Structure):
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("kv_stride", ct.c_int32), ("sm_scale", ct.c_float), ("rope", bd_rope),
                 ("num_splits", ct.c_int32), ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t),
-                ("dev_status", ct.c_void_p)]
+                ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32)]
 
 
 class bd_fork_args(ct.Structure):
@@ -53,7 +53,8 @@ class bd_fork_args(ct.Structure):
                 ("block_start", ct.c_void_p), ("n_blocks", ct.c_int32), ("block_size", ct.c_int32),
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("sm_scale", ct.c_float), ("rope", bd_rope), ("num_splits", ct.c_int32),
-                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
+                ("prefix_ready", ct.c_int32)]
 
 
 class bd_unmask_args(ct.Structure):
@@ -168,7 +169,7 @@ def _bs(block_start):
 
 def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0, o=None, lse=None,
                          sm_scale: float = 0.0, rope=None, num_splits: int = 0, workspace=None,
-                         dev_status=None, stream=None):
+                         dev_status=None, stream=None, prefix_ready: bool = False):
     """Block-causal attention of the active positions.  q [n_q, Hq, D] bf16;
     k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after).
     Returns (o [n_q, Hq, D] bf16, lse [Hq, n_q] fp32)."""
@@ -191,13 +192,14 @@ def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0,
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    a.prefix_ready = 1 if prefix_ready else 0
     _check("bd_block_causal_attn", lib().bd_block_causal_attn(a, _stream(stream)))
     return o, lse
 
 
 def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: int, block_start=None,
                      block_size: int = 0, o=None, lse=None, sm_scale: float = 0.0, rope=None, num_splits: int = 0,
-                     workspace=None, dev_status=None, stream=None):
+                     workspace=None, dev_status=None, stream=None, prefix_ready: bool = False):
     """N rollouts over one shared prefix.  q [N, n_q, Hq, D]; prefix_k/v [Hkv, prefix_stride, D];
     priv_k/v [N, Hkv, priv_stride, D].  Returns (o [N, n_q, Hq, D], lse [N, Hq, n_q])."""
     N, n_q, Hq, D = q.shape
@@ -223,6 +225,7 @@ def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: in
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    a.prefix_ready = 1 if prefix_ready else 0
     _check("bd_fork_rollouts", lib().bd_fork_rollouts(a, _stream(stream)))
     return o, lse
 

@@ -99,6 +99,7 @@ struct AttnDesc {
   void* ws;
   size_t ws_bytes;
   int32_t* ds;
+  int prefix_ready;
 };
 
 // One call runs as one launch, or as two when its (row tile, KV head) groups
@@ -217,6 +218,8 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.num_splits = pl.part[0].splits;
   p.rows_per_head = pl.rows_per_head;
   p.n_prefix_tiles = pl.n_prefix_tiles;
+  // the rotated copy of a RoPE call is written by the kernel just before
+  p.prefix_early = d.prefix_ready && !(d.rope.enabled && d.C > 0) ? 1 : 0;
   const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
   p.scale_log2 = scale * 1.4426950408889634f;
   // RoPE: the pre-RoPE prefix keys are rotated once for the whole call into
@@ -311,6 +314,7 @@ AttnDesc desc_of(const bd_attn_args* a) {
   d.ws = a->workspace;
   d.ws_bytes = a->workspace_bytes;
   d.ds = a->dev_status;
+  d.prefix_ready = a->prefix_ready;
   return d;
 }
 
@@ -342,6 +346,7 @@ AttnDesc desc_of(const bd_fork_args* a) {
   d.ws = a->workspace;
   d.ws_bytes = a->workspace_bytes;
   d.ds = a->dev_status;
+  d.prefix_ready = a->prefix_ready;
   return d;
 }
 

@@ -345,6 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  // The first K/V loads (K 0, V 0, K 1, V 1, K 2 -- K runs one tile ahead of
+  // V): with early = true only the leading prefix tiles among them, issued
+  // before the dependency wait; with early = false the rest.
+  auto issue_initial = [&](bool early) {
+    for (int u = 0; u < 5; ++u) {
+      const int t = u >> 1;
+      const bool is_v = (u & 1) != 0;
+      if (t >= nt) break;
+      const bool prefix = tr.lo + t < p.n_prefix_tiles;
+      if (early ? (prefix && p.prefix_early) : !(prefix && p.prefix_early)) issue_tile(t, is_v);
+    }
+  };
+
   if (threadIdx.x == 0) {
     if (p.q_tma) tma_prefetch_desc(&maps.q);
     if (p.n_prefix_tiles > 0) {
@@ -370,14 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[MERGE_O], 1);
     misc[1] = 0;
     fence_mbar_init();
+    // cached prefix tiles the caller declared complete before the previous
+    // kernel of the stream started may be fetched before the dependency wait
+    if (p.prefix_early) issue_initial(true);
   }
   if (warp == 1) {
     tmem_alloc(&misc[0], L::kTmemCols);
     tmem_relinquish();
   }
-  // Everything above touches only shared memory, TMEM and the kernel's own
-  // parameters; from here on this thread reads or writes global memory, which
-  // the previous kernel in the stream may still be producing.
+  // Everything above touches only shared memory, TMEM, the kernel's own
+  // parameters and (prefix_early) cached prefix rows; from here on this thread
+  // reads or writes global memory that the previous kernel in the stream may
+  // still be producing.
   pdl_wait();
   if (threadIdx.x == 0) {
     // the first loads leave before the rest of the CTA is set up
@@ -388,12 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < D / 64; ++hh)
           tma_load_4d(smem + L::kQ + hh * BM * 128, &maps.q, hh * 64, 0, kvh, m0 / p.G, &bars[QFULL]);
       }
-      // K runs one tile ahead of V: K 0, V 0, K 1, V 1, K 2
-      for (int t = 0; t < 2 && t < nt; ++t) {
-        issue_tile(t, false);
-        issue_tile(t, true);
-      }
-      if (nt > 2) issue_tile(2, false);
+      issue_initial(false);
     }
   }
   tc_fence_before();

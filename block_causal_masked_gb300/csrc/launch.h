@@ -52,6 +52,7 @@ struct AttnParams {
   int n_prefix_tiles;     // ceil(C / BN)
   float scale_log2;       // sm_scale * log2(e)
   int q_tma;              // Q tile by TMA (G divides 128)
+  int prefix_early;       // prefix K/V tiles may be loaded before the dependency wait
 };
 
 // Rotation of the cached prefix keys before attention (RoPE at k_pos - delta).

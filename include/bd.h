@@ -125,6 +125,14 @@ typedef struct bd_rope {
  *                library, which may also run the call as two launches (whole
  *                waves of unsplit row tiles, then the rest split wide).  With
  *                one split and no RoPE no workspace is needed (NULL is fine)
+ *   prefix_ready 0, or 1 to declare that the cached prefix rows [0, C) of k and v
+ *                were complete before the kernel that precedes this call on
+ *                `stream` started (true of a decode step's KV cache, which the
+ *                previous kernel -- the QKV projection of this layer -- does not
+ *                write).  The call may then start fetching those rows while
+ *                that kernel is still running (programmatic dependent launch);
+ *                q, the active rows and every output are touched only after it
+ *                has completed.  Ignored with RoPE.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= n_q; 0 <= C; kv_stride >= C + n_q.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_attn_args {
@@ -148,6 +156,7 @@ typedef struct bd_attn_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  int32_t prefix_ready;
 } bd_attn_args;
 
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream);
@@ -169,8 +178,8 @@ size_t bd_attn_workspace_size(const bd_attn_args* a);
  *   priv_k/v          bf16 [N, Hkv, priv_stride, D], rows [0, priv_len + n_q) used
  *   o                 bf16 [N, n_q, Hq, D]
  *   lse               fp32 [N, Hq, n_q] or NULL
- *   block_start, n_blocks, block_size, sm_scale, rope, num_splits: as in
- *   bd_attn_args (rope applies to the shared prefix keys only)
+ *   block_start, n_blocks, block_size, sm_scale, rope, num_splits, prefix_ready:
+ *   as in bd_attn_args (rope and prefix_ready concern the shared prefix only)
  * ---------------------------------------------------------------------------*/
 typedef struct bd_fork_args {
   int32_t N;
@@ -198,6 +207,7 @@ typedef struct bd_fork_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  int32_t prefix_ready;
 } bd_fork_args;
 
 bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream);

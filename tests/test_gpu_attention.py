@@ -172,3 +172,48 @@ def test_fork_with_rope_matches_oracle():
     o_ref, lse_ref = oracle.fork_attention(f.q, f.prefix_k, f.prefix_v, f.priv_k, f.priv_v, f.priv_len,
                                            f.block_start, k_pos=f.k_pos, delta=f.delta, theta=f.theta, rope=True)
     assert_attn_close(o, lse, o_ref, lse_ref, "fork rope")
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_prefix_ready_matches_default_in_a_graph(rope):
+    """prefix_ready = 1 (prefix tiles fetched before the dependency wait) gives
+    bitwise the results of the default, for launches chained in one CUDA graph
+    where each launch's queries are written by the kernel just before it; with
+    RoPE the flag is ignored.  The last launch also matches the oracle."""
+    C, bs, n = 1500, [0, 33], 4
+    case = synth.attn_case(12, 0, C=C, block_start=bs, Hq=16, Hkv=2, D=128)
+    k, v = bf16(case.k), bf16(case.v)
+    q0 = bf16(case.q)
+    blk = i32(bs)
+    kp = torch.arange(C, dtype=torch.int32, device=DEV) + 7
+    rp = dict(k_pos=kp, delta=7, theta=1e4) if rope else None
+
+    def chain(flag):
+        qs = [torch.empty_like(q0) for _ in range(n)]
+        outs = [torch.empty_like(q0) for _ in range(n)]
+        lses = [torch.empty((16, 33), dtype=torch.float32, device=DEV) for _ in range(n)]
+
+        def run():
+            for i in range(n):
+                qs[i].copy_(q0 if i == 0 else outs[i - 1])          # q written by the kernel before
+                bd.bd_block_causal_attn(qs[i], k, v, C, block_start=blk, o=outs[i], lse=lses[i], rope=rp,
+                                        prefix_ready=flag)
+        run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            run()
+        for x in outs:
+            x.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        return [host(x) for x in outs], [host(x) for x in lses], host(qs[-1])
+
+    o1, l1, q_last = chain(True)
+    o0, l0, _ = chain(False)
+    for a, b in zip(o1 + l1, o0 + l0):
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a, b.view(np.uint32)
+                              if b.dtype == np.float32 else b)
+    kw = dict(k_pos=host(kp), delta=7, theta=1e4, rope=True) if rope else {}
+    o_ref, lse_ref = oracle.block_causal_attention(q_last, case.k, case.v, C, bs, **kw)
+    assert_attn_close(torch.from_numpy(o1[-1]), torch.from_numpy(l1[-1]), o_ref, lse_ref)
