@@ -79,6 +79,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Waits for the phase of parity `parity` of `bar` with no abort flag: gives up
+// after the time limit, OR-ing BD_DEV_TIMEOUT into *dev_status (if given).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // 2^x on the MUFU unit: PTX ex2.approx.ftz.f32 (relative error below 2^-22 per
 // the PTX ISA; results below 2^-126 flush to zero; 2^-inf = +0).
 __device__ __forceinline__ float fast_exp2(float x) {

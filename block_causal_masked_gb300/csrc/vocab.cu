@@ -64,23 +64,6 @@ __device__ __forceinline__ void acc_vec(Acc& a, const float (&x)[N], int i0, boo
   }
 }
 
-__device__ __forceinline__ void load_vec8(const void* base, int dtype, long long off, float (&x)[8]) {
-  if (dtype == BD_BF16) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[2 * k] = __uint_as_float(ws[k] << 16);
-      x[2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
-    }
-  } else {
-    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-    const float4 a = __ldg(f), b = __ldg(f + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
-}
-
 __device__ __forceinline__ float load_one(const void* base, int dtype, long long off) {
   if (dtype == BD_BF16) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + off);
@@ -114,42 +97,94 @@ __device__ Acc block_reduce(Acc a, Acc* sh) {
   return a;
 }
 
+// Pieces of a chunk are staged in shared memory by bulk copies (the copy
+// engine keeps far more bytes in flight per SM than per-thread loads can), two
+// pieces at a time: while one is reduced the next is landing.
+constexpr int kPiece = 8192;   // elements per piece (a multiple of 8)
+constexpr int kPieceStages = 2;
+
+// Dynamic shared memory of a streaming CTA: kPieceStages pieces of logits (and
+// of noise, when sampled).
+__host__ __device__ constexpr int stream_smem_bytes(int elem_bytes, bool noise) {
+  return kPieceStages * kPiece * (elem_bytes + (noise ? 4 : 0));
+}
+
+struct Stream {
+  uint8_t* buf;     // dynamic shared memory
+  uint64_t* bars;   // kPieceStages mbarriers
+  int32_t* dev_status;
+};
+
 // Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed
-// scores).  Each thread keeps U 8-element vectors in flight, so a chunk of up
-// to U * 8 * 256 elements costs one memory round trip.
-template <int U>
-__device__ Acc reduce_chunk(const void* logits, int dtype, long long row_off, const float* noise, long long noise_off,
-                            float inv_temp, int lo, int hi, bool need_sum) {
+// scores).  Elements [lo, lo + 8 floor((hi - lo) / 8)) arrive by bulk copies
+// into shared memory; a ragged tail of fewer than 8 is read directly.  Every
+// copy issued has landed when this returns (the shared memory stays valid).
+__device__ Acc reduce_chunk(const Stream& st, const void* logits, int dtype, long long row_off, const float* noise,
+                            long long noise_off, float inv_temp, int lo, int hi, bool need_sum) {
   Acc a{-INFINITY, 0.f, 0x7fffffff};
-  const int vlo = lo / 8, vhi = hi / 8;  // whole 8-element vectors (lo is a multiple of 8)
-  for (int v0 = vlo; v0 < vhi; v0 += U * kThreads) {
-    float x[U][8];
+  const int esz = dtype == BD_BF16 ? 2 : 4;
+  const int stage_bytes = kPiece * (esz + (noise ? 4 : 0));
+  const int vend = lo + (hi - lo) / 8 * 8;
+  const int npieces = (vend - lo + kPiece - 1) / kPiece;
+  int issued = 0;  // pieces issued (thread 0)
+  auto issue = [&](int k) {
+    ++issued;
+    const int b = k % kPieceStages;
+    const int e0 = lo + k * kPiece;
+    const int n = min(kPiece, vend - e0);
+    uint8_t* dst = st.buf + b * stage_bytes;
+    mbar_arrive_expect_tx(&st.bars[b], static_cast<uint32_t>(n * (esz + (noise ? 4 : 0))));
+    bulk_load(dst, static_cast<const uint8_t*>(logits) + (row_off + e0) * esz, n * esz, &st.bars[b]);
+    if (noise) bulk_load(dst + kPiece * esz, noise + noise_off + e0, n * 4, &st.bars[b]);
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < kPieceStages && k < npieces; ++k) issue(k);
+  bool ok = true;
+  for (int k = 0; k < npieces; ++k) {
+    const int b = k % kPieceStages;
+    const int e0 = lo + k * kPiece;
+    const int nv = min(kPiece, vend - e0) / 8;
+    if (ok) ok = mbar_wait_bounded(&st.bars[b], (k / kPieceStages) & 1, st.dev_status);
+    if (ok) {
+      const uint8_t* piece = st.buf + b * stage_bytes;
+      for (int v = threadIdx.x; v < nv; v += kThreads) {
+        float x[8];
+        if (dtype == BD_BF16) {
+          const uint4 w = *reinterpret_cast<const uint4*>(piece + 16 * v);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * kThreads + threadIdx.x;
-      if (v < vhi) load_vec8(logits, dtype, row_off + 8ll * v, x[u]);
-    }
-    if (noise) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * kThreads + threadIdx.x;
-        if (v < vhi) {
-          const float4* np4 = reinterpret_cast<const float4*>(noise + noise_off + 8ll * v);
-          const float4 n0 = __ldg(np4), n1 = __ldg(np4 + 1);
+          for (int q = 0; q < 4; ++q) {
+            x[2 * q] = __uint_as_float(ws[q] << 16);
+            x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
+          }
+        } else {
+          const float4 f0 = *reinterpret_cast<const float4*>(piece + 32 * v);
+          const float4 f1 = *reinterpret_cast<const float4*>(piece + 32 * v + 16);
+          x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
+          x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+        }
+        if (noise) {
+          const float4* np4 = reinterpret_cast<const float4*>(piece + kPiece * esz + 32 * v);
+          const float4 n0 = np4[0], n1 = np4[1];
           const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
-          for (int k = 0; k < 8; ++k) x[u][k] = gumbel_score(x[u][k], nn[k], inv_temp);
+          for (int q = 0; q < 8; ++q) x[q] = gumbel_score(x[q], nn[q], inv_temp);
         }
+        acc_vec<8>(a, x, e0 + 8 * v, need_sum);
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * kThreads + threadIdx.x;
-      if (v < vhi) acc_vec<8>(a, x[u], 8 * v, need_sum);
+    __syncthreads();  // the stage is read: it may be refilled
+    if (threadIdx.x == 0 && k + kPieceStages < npieces) {
+      if (ok) issue(k + kPieceStages);
     }
   }
+  if (threadIdx.x == 0 && !ok) {
+    // a wait gave up: let the copies still in flight land before the CTA ends
+    for (int k = issued > kPieceStages ? issued - kPieceStages : 0; k < issued; ++k)
+      mbar_wait_bounded(&st.bars[k % kPieceStages], (k / kPieceStages) & 1, nullptr);
+  }
   // ragged tail of the row (only when the row length is not a multiple of 8)
-  for (int i = vhi * 8 + threadIdx.x; i < hi; i += kThreads) {
+  for (int i = vend + threadIdx.x; i < hi; i += kThreads) {
     float x[1] = {load_one(logits, dtype, row_off + i)};
     if (noise) x[0] = gumbel_score(x[0], __ldg(noise + noise_off + i), inv_temp);
     acc_vec<1>(a, x, i, need_sum);
@@ -351,6 +386,13 @@ __device__ void unmask_select(const UnmaskParams& p) {
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
   __shared__ Acc red[kThreads / 32];
   __shared__ int last;
+  __shared__ __align__(8) uint64_t bars[kPieceStages];
+  extern __shared__ __align__(128) uint8_t dyn[];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPieceStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_trigger();  // the next kernel may start its own set-up
   // one CTA per (chunk, logits row): every row is streamed, whichever position
@@ -362,7 +404,8 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
     const int hi = min(p.V, lo + p.chunk_elems);
     Acc a{-INFINITY, 0.f, 0x7fffffff};
     if (lo < hi)
-      a = reduce_chunk<8>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
+      a = reduce_chunk(Stream{dyn, bars, p.dev_status}, p.logits, p.dtype, static_cast<long long>(row) * p.ld,
+                       nullptr, 0, 1.f, lo, hi, true);
     a = block_reduce(a, red);
     if (threadIdx.x == 0)
       p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
@@ -476,6 +519,13 @@ __device__ void verify_match(const VerifyParams& p, int s) {
 __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
   __shared__ Acc red[kThreads / 32];
   __shared__ int last;
+  __shared__ __align__(8) uint64_t bars[kPieceStages];
+  extern __shared__ __align__(128) uint8_t dyn[];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPieceStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.y;  // sequence * n_rows + e
@@ -485,9 +535,8 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
   const int hi = min(p.V, lo + p.chunk_elems);
   Acc a{-INFINITY, 0.f, 0x7fffffff};
   if (lo < hi)
-    a = p.noise ? reduce_chunk<4>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise,
-                                  static_cast<long long>(row) * p.ld, p.inv_temp, lo, hi, false)
-                : reduce_chunk<8>(p.logits, p.dtype, static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, false);
+    a = reduce_chunk(Stream{dyn, bars, p.dev_status}, p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise,
+                     static_cast<long long>(row) * p.ld, p.inv_temp, lo, hi, false);
   a = block_reduce(a, red);
   if (threadIdx.x == 0) {
     p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, 0.f, __int_as_float(a.idx), 0.f);
@@ -538,8 +587,16 @@ size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
 // overlap the tail of the previous kernel (each kernel waits for it with
 // griddepcontrol.wait before touching global memory).
 template <typename P>
-static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, cudaStream_t stream) {
+static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, int smem, cudaStream_t stream) {
+  static bool configured = false;  // one instantiation per kernel
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem_bytes(4, true));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   cudaLaunchConfig_t cfg = {};
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -553,11 +610,13 @@ static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, cudaStre
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
-  return launch_pdl(unmask_kernel, dim3(p.chunks, p.R), p, stream);
+  return launch_pdl(unmask_kernel, dim3(p.chunks, p.R), p, stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, false),
+                    stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
-  return launch_pdl(verify_kernel, dim3(p.chunks, p.n_seq * p.n_rows), p, stream);
+  return launch_pdl(verify_kernel, dim3(p.chunks, p.n_seq * p.n_rows), p,
+                    stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, p.noise != nullptr), stream);
 }
 
 }  // namespace bd
