@@ -103,13 +103,7 @@ __device__ __forceinline__ bool all_lanes(bool v) { return __all_sync(0xffffffff
 // Same as mbar_wait but ignores the abort flag: used to let copies and MMAs in
 // flight finish before the CTA releases its shared memory and TMEM.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int32_t* dev_status) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
-      return;
-    }
-  }
+  (void)mbar_wait_bounded(bar, parity, dev_status);
 }
 
 // End (exclusive) of the block that holds active position i, clamped to [1, n_q].

@@ -59,19 +59,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of parity `parity` of `bar` to complete.  Returns false
-// (after setting *abort_flag and OR-ing BD_DEV_TIMEOUT into *dev_status) if the
-// limit expires, or at once if another thread of the CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The spinning part of the waits below, kept out of line: it is cold (most
+// waits succeed at the first try_wait, which itself suspends the thread for a
+// while), and one shared copy keeps the kernels' code small enough for the
+// instruction caches.
+static __device__ __noinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* dev_status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
+      if (abort_flag && *abort_flag) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
+        if (abort_flag) *abort_flag = 1;
         if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
         return false;
       }
@@ -79,18 +79,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Waits for the phase of parity `parity` of `bar` to complete.  Returns false
+// (after setting *abort_flag and OR-ing BD_DEV_TIMEOUT into *dev_status) if the
+// limit expires, or at once if another thread of the CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_spin(bar, parity, abort_flag, dev_status);
+}
+
 // Waits for the phase of parity `parity` of `bar` with no abort flag: gives up
 // after the time limit, OR-ing BD_DEV_TIMEOUT into *dev_status (if given).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* dev_status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
-      return false;
-    }
-  }
+  return mbar_spin(bar, parity, nullptr, dev_status);
 }
 
 // 2^x on the MUFU unit: PTX ex2.approx.ftz.f32 (relative error below 2^-22 per

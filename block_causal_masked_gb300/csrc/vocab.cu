@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxBlock = 1024;   // positions of one block
 constexpr int kMaxVerifyL = 1024; // slots of one verified block
 
@@ -212,6 +213,7 @@ __device__ void stage_partials(const float4* src, int n, float4* dst) {
 // Merge of one row's chunk partials (staged in shared memory), in chunk order.
 __device__ Acc merge_staged(const float4* part, int chunks) {
   Acc a{-INFINITY, 0.f, 0x7fffffff};
+#pragma unroll 1
   for (int c = 0; c < chunks; ++c) {
     const float4 q = part[c];
     acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
@@ -224,7 +226,6 @@ constexpr int kStageF4 = 512;  // chunk partials staged at a time by the decidin
 // ======================================================================= unmask
 
 __device__ void unmask_select(const UnmaskParams& p) {
-  constexpr int kPer = kMaxPos / kThreads;  // positions per thread
   __shared__ uint8_t st0[kMaxPos];
   __shared__ float conf_s[kMaxPos];
   __shared__ int pred_s[kMaxPos];
@@ -235,43 +236,30 @@ __device__ void unmask_select(const UnmaskParams& p) {
   const int tid = threadIdx.x;
   const int per_batch = max(1, kStageF4 / p.chunks);  // logits rows whose partials are staged at once
   {
-    // one memory round trip: every load is issued before the first is used
-    uint8_t stv[kPer];
-    int rv[kPer], bv[kPer + 1];
+    // The loads of a thread are all issued before any is used (one memory
+    // round trip when n_pos <= 256).  The loops are kept rolled: this code runs
+    // once per call in one CTA, so its size (instruction fetch) costs more than
+    // its instruction count.
     float4 q[kStageF4 / kThreads];
     const int n0 = min(per_batch, p.R) * p.chunks;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int j = u * kThreads + tid;
-      if (j < p.n_pos) {
-        stv[u] = p.state[j];
-        rv[u] = __ldg(p.logit_row + j);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u <= kPer; ++u) {
-      const int b = u * kThreads + tid;
-      if (b <= p.n_blocks) bv[u] = __ldg(p.block_start + b);
-    }
 #pragma unroll
     for (int u = 0; u < kStageF4 / kThreads; ++u) {
       const int i = u * kThreads + tid;
       if (i < n0) q[u] = __ldcg(p.chunk_part + i);
     }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int j = u * kThreads + tid;
+    const int n_items = max(p.n_pos, p.n_blocks + 1);
+#pragma unroll 1
+    for (int j = tid; j < n_items; j += kThreads) {
+      const uint8_t sv = j < p.n_pos ? p.state[j] : 0;
+      const int rv = j < p.n_pos ? __ldg(p.logit_row + j) : 0;
+      const int bv = j <= p.n_blocks ? __ldg(p.block_start + j) : 0;
       if (j < p.n_pos) {
-        st0[j] = stv[u];
-        row_s[j] = rv[u];
+        st0[j] = sv;
+        row_s[j] = rv;
         conf_s[j] = 0.f;
         pred_s[j] = -1;
       }
-    }
-#pragma unroll
-    for (int u = 0; u <= kPer; ++u) {
-      const int b = u * kThreads + tid;
-      if (b <= p.n_blocks) bs_s[b] = bv[u];
+      if (j <= p.n_blocks) bs_s[j] = bv;
     }
 #pragma unroll
     for (int u = 0; u < kStageF4 / kThreads; ++u) {
@@ -280,21 +268,24 @@ __device__ void unmask_select(const UnmaskParams& p) {
     }
   }
   // every masked position with a logits row: merge that row's chunk partials
+  #pragma unroll 1
   for (int r0 = 0; r0 < p.R; r0 += per_batch) {
     const int nb = min(per_batch, p.R - r0);
     if (r0 > 0) stage_partials(p.chunk_part + static_cast<size_t>(r0) * p.chunks, nb * p.chunks, stage);
     __syncthreads();
+    #pragma unroll 1
     for (int j = tid; j < p.n_pos; j += kThreads) {
       const int row = row_s[j];
       if (row < r0 || row >= r0 + nb || st0[j] != BD_MASKED) continue;
       const Acc a = merge_staged(stage + (row - r0) * p.chunks, p.chunks);
-      conf_s[j] = 1.f / a.s;
+      conf_s[j] = fast_rcp(a.s);
       pred_s[j] = a.idx;
-      if (p.lse) p.lse[j] = a.m + logf(a.s);
+      if (p.lse) p.lse[j] = a.m + fast_log2(a.s) * kLn2;
     }
     __syncthreads();
   }
   int ok_local = 1;
+  #pragma unroll 1
   for (int j = tid; j < p.n_pos; j += kThreads) {
     const int pred = pred_s[j];
     if (p.pred) p.pred[j] = pred;
@@ -302,6 +293,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
     if (p.lse && pred < 0) p.lse[j] = 0.f;
     p.commit[j] = 0;
   }
+  #pragma unroll 1
   for (int b = tid; b < p.n_blocks; b += kThreads) {
     const int lo = bs_s[b], hi = bs_s[b + 1];
     ok_local &= lo < hi && hi - lo <= kMaxBlock;
@@ -311,17 +303,20 @@ __device__ void unmask_select(const UnmaskParams& p) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, BD_DEV_BAD_INPUT);
     return;
   }
+  #pragma unroll 1
   for (int b = 0; b < p.n_blocks; ++b) {
     const int lo = bs_s[b], hi = bs_s[b + 1];
     if (tid < 4) cnt[tid] = 0;
     __syncthreads();
     int masked = 0, cand = 0, prev_done = 0;
+    #pragma unroll 1
     for (int j = lo + tid; j < hi; j += kThreads) {
       masked += st0[j] == BD_MASKED;
       cand += pred_s[j] >= 0;
     }
     if (b > 0) {
       const int plo = bs_s[b - 1];
+      #pragma unroll 1
       for (int j = plo + tid; j < lo; j += kThreads) prev_done += st0[j] != BD_MASKED;
     }
     if (masked) atomicAdd(&cnt[0], masked);
@@ -345,6 +340,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
     const int n_min = min(rem, max(p.k_fixed, frac));
     int ncom = 0;
     if (status == BD_FULL || status == BD_HALF) {
+      #pragma unroll 1
       for (int j = lo + tid; j < hi; j += kThreads) {
         if (pred_s[j] < 0) continue;
         const float c = conf_s[j];
@@ -355,6 +351,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
           take = c >= p.tau_full;
           if (!take) {
             int rank = 0;
+            #pragma unroll 1
             for (int k = lo; k < hi && rank < n_min; ++k)
               if (pred_s[k] >= 0 && (conf_s[k] > c || (conf_s[k] == c && k < j))) ++rank;
             take = rank < n_min;
@@ -370,6 +367,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
         }
       }
     } else if (p.write_draft) {
+      #pragma unroll 1
       for (int j = lo + tid; j < hi; j += kThreads)
         if (pred_s[j] >= 0) p.tokens[j] = pred_s[j];
     }
@@ -424,7 +422,6 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
 // ======================================================================= verify
 
 __device__ void verify_match(const VerifyParams& p, int s) {
-  constexpr int kPer = kMaxVerifyL / kThreads;
   __shared__ uint8_t st[kMaxVerifyL];
   __shared__ int tok[kMaxVerifyL];
   __shared__ int arg[kMaxVerifyL + 1];
@@ -433,31 +430,21 @@ __device__ void verify_match(const VerifyParams& p, int s) {
   const int per_batch = max(1, kStageF4 / p.chunks);  // rows whose partials are staged at once
   const float4* part = p.chunk_part + static_cast<size_t>(s) * p.n_rows * p.chunks;
   {
-    // one memory round trip: every load is issued before the first is used
-    uint8_t sv[kPer];
-    int tv[kPer];
+    // the loads of a thread are all issued before any is used (one memory
+    // round trip when L <= 256); loops kept rolled (see unmask_select)
     float4 q[kStageF4 / kThreads];
     const int n0 = min(per_batch, p.n_rows) * p.chunks;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int j = u * kThreads + threadIdx.x;
-      if (j < L) {
-        sv[u] = p.state[static_cast<size_t>(s) * L + j];
-        tv[u] = p.tokens[static_cast<size_t>(s) * L + j];
-      }
-    }
 #pragma unroll
     for (int u = 0; u < kStageF4 / kThreads; ++u) {
       const int i = u * kThreads + threadIdx.x;
       if (i < n0) q[u] = __ldcg(part + i);
     }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int j = u * kThreads + threadIdx.x;
-      if (j < L) {
-        st[j] = sv[u];
-        tok[j] = tv[u];
-      }
+#pragma unroll 1
+    for (int j = threadIdx.x; j < L; j += kThreads) {
+      const uint8_t sv = p.state[static_cast<size_t>(s) * L + j];
+      const int tv = p.tokens[static_cast<size_t>(s) * L + j];
+      st[j] = sv;
+      tok[j] = tv;
     }
 #pragma unroll
     for (int u = 0; u < kStageF4 / kThreads; ++u) {
@@ -466,10 +453,12 @@ __device__ void verify_match(const VerifyParams& p, int s) {
     }
   }
   // the rows' chunk partials, staged in batches: one thread per row
+  #pragma unroll 1
   for (int e0 = 0; e0 < p.n_rows; e0 += per_batch) {
     const int nb = min(per_batch, p.n_rows - e0);
     if (e0 > 0) stage_partials(part + static_cast<size_t>(e0) * p.chunks, nb * p.chunks, stage);
     __syncthreads();
+    #pragma unroll 1
     for (int ee = threadIdx.x; ee < nb; ee += kThreads) {
       const Acc a = merge_staged(stage + ee * p.chunks, p.chunks);
       arg[e0 + ee] = a.idx == 0x7fffffff ? -1 : a.idx;
@@ -479,6 +468,7 @@ __device__ void verify_match(const VerifyParams& p, int s) {
   if (threadIdx.x == 0) {
     int e = 0, n_acc = 0, bonus = -1, bonus_pos = -1;
     bool mismatch = false;
+    #pragma unroll 1
     for (int j = 0; j < L; ++j) {
       if (st[j] == BD_SCAFFOLD) continue;
       if (st[j] == BD_MASKED) {
@@ -510,6 +500,7 @@ __device__ void verify_match(const VerifyParams& p, int s) {
     p.bonus_pos[s] = bonus_pos;
   }
   __syncthreads();
+  #pragma unroll 1
   for (int j = threadIdx.x; j < L; j += kThreads) {
     p.state[static_cast<size_t>(s) * L + j] = st[j];
     p.tokens[static_cast<size_t>(s) * L + j] = tok[j];
