@@ -59,10 +59,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The spinning part of the waits below, kept out of line: it is cold (most
-// waits succeed at the first try_wait, which itself suspends the thread for a
-// while), and one shared copy keeps the kernels' code small enough for the
-// instruction caches.
+// The spinning part of mbar_wait_bounded, kept out of line: those waits are
+// few and cold (the vocabulary kernels' piece arrivals, end-of-CTA drains), so
+// one shared copy keeps the code small.  mbar_wait, on the attention kernel's
+// pipeline, spins inline: a call on the wake-up path measured slower there.
 static __device__ __noinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* dev_status) {
   const uint64_t t0 = globaltimer();
@@ -85,7 +85,18 @@ static __device__ __noinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, vo
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* dev_status) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_spin(bar, parity, abort_flag, dev_status);
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 
 // Waits for the phase of parity `parity` of `bar` with no abort flag: gives up
