@@ -14,15 +14,18 @@ fusion or reordering beyond that definition:
                  per-block commit rule (scaffold frozen, threshold, minimum
                  fraction, half/full activation from the predecessor's completion).
 * ``verify``     scaffold-speculative verification (greedy or Gumbel-max sampled).
+* ``stream``     the streaming cache: a new frame written into every view's frame
+                 slot, and the streaming (position-causal) attention mask.
 
 Where the pages leave a step open, the docstrings name the reading taken.
 Parity of every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` (closed forms, special cases, invariants, brute force
 and the pages' printed section table); none is unpinned.
 """
-from . import attention, unmask, verify  # noqa: F401
+from . import attention, stream, unmask, verify  # noqa: F401
 from .attention import (block_causal_attention, fork_attention, rope_rotate,  # noqa: F401
                         round_bf16, visibility_mask)
+from .stream import stream_attention, stream_insert, streaming_mask  # noqa: F401
 from .unmask import row_stats, unmask_step  # noqa: F401
 from .verify import gumbel_scores, spec_verify  # noqa: F401
 
