@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 __all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_unmask_step_noalloc",
-           "bd_spec_verify", "bd_check",
+           "bd_spec_verify", "bd_stream_insert", "bd_check",
            "bd_status_string", "lib", "BdError", "Workspace", "MASKED", "COMMITTED", "SCAFFOLD",
            "INACTIVE", "HALF", "FULL", "DONE"]
 
@@ -43,7 +43,7 @@ class bd_attn_args(ct.Structure):
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("kv_stride", ct.c_int32), ("sm_scale", ct.c_float), ("rope", bd_rope),
                 ("num_splits", ct.c_int32), ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t),
-                ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32)]
+                ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32), ("q_pos", ct.c_void_p)]
 
 
 class bd_fork_args(ct.Structure):
@@ -55,6 +55,13 @@ class bd_fork_args(ct.Structure):
                 ("sm_scale", ct.c_float), ("rope", bd_rope), ("num_splits", ct.c_int32),
                 ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
                 ("prefix_ready", ct.c_int32)]
+
+
+class bd_stream_insert_args(ct.Structure):
+    _fields_ = [("k_cache", ct.c_void_p), ("v_cache", ct.c_void_p), ("k_pos", ct.c_void_p), ("new_k", ct.c_void_p),
+                ("new_v", ct.c_void_p), ("new_pos", ct.c_void_p), ("views", ct.c_int32), ("frames", ct.c_int32),
+                ("per_frame", ct.c_int32), ("slot", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
+                ("cache_stride", ct.c_int32)]
 
 
 class bd_unmask_args(ct.Structure):
@@ -89,7 +96,8 @@ def lib() -> ct.CDLL:
             path = _build.build()
             L = ct.CDLL(path)
             for name, argt in (("bd_block_causal_attn", bd_attn_args), ("bd_fork_rollouts", bd_fork_args),
-                               ("bd_unmask_step", bd_unmask_args), ("bd_spec_verify", bd_verify_args)):
+                               ("bd_unmask_step", bd_unmask_args), ("bd_spec_verify", bd_verify_args),
+                               ("bd_stream_insert", bd_stream_insert_args)):
                 fn = getattr(L, name)
                 fn.argtypes = [ct.POINTER(argt), ct.c_void_p]
                 fn.restype = ct.c_int
@@ -150,9 +158,11 @@ _WS = {"attn": Workspace(), "unmask": Workspace(), "verify": Workspace()}
 
 
 def _rope(rope) -> bd_rope:
+    """dict(k_pos=int32 tensor or None, delta, theta, enabled=True); enabled=False
+    passes the positions (for the streaming mask) without rotating the keys."""
     r = bd_rope()
     if rope:
-        r.enabled = 1
+        r.enabled = 1 if rope.get("enabled", True) else 0
         kp = rope.get("k_pos")
         r.k_pos = None if kp is None else kp.data_ptr()
         r.delta = int(rope.get("delta", 0))
@@ -169,9 +179,11 @@ def _bs(block_start):
 
 def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0, o=None, lse=None,
                          sm_scale: float = 0.0, rope=None, num_splits: int = 0, workspace=None,
-                         dev_status=None, stream=None, prefix_ready: bool = False):
+                         dev_status=None, stream=None, prefix_ready: bool = False, q_pos=None):
     """Block-causal attention of the active positions.  q [n_q, Hq, D] bf16;
     k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after).
+    With q_pos (int32 [n_q]) the streaming mask instead: queries over rows
+    [0, C) only, key j visible iff rope k_pos[j] - delta <= q_pos[i].
     Returns (o [n_q, Hq, D] bf16, lse [Hq, n_q] fp32)."""
     n_q, Hq, D = q.shape
     Hkv, kv_stride, _ = k.shape
@@ -187,12 +199,15 @@ def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0,
     a.sm_scale = float(sm_scale)
     a.rope = _rope(rope)
     a.num_splits = int(num_splits)
+    a.prefix_ready = 1 if prefix_ready else 0
+    if q_pos is not None:  # part of the plan: set before the workspace is sized
+        assert q_pos.dtype == torch.int32 and q_pos.is_cuda and q_pos.numel() == n_q
+        a.q_pos = q_pos.data_ptr()
     need = lib().bd_attn_workspace_size(a)
     ws = workspace if workspace is not None else _WS["attn"].get(need, q.device)
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
-    a.prefix_ready = 1 if prefix_ready else 0
     _check("bd_block_causal_attn", lib().bd_block_causal_attn(a, _stream(stream)))
     return o, lse
 
@@ -306,6 +321,21 @@ def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
     _check("bd_spec_verify", lib().bd_spec_verify(a, _stream(stream)))
     return accepted_len, bonus, bonus_pos
+
+
+def bd_stream_insert(k_cache, v_cache, k_pos, new_k, new_v, new_pos, views: int, frames: int, per_frame: int,
+                     slot: int, stream=None) -> None:
+    """Writes the new frame (new_k/new_v bf16 [views * per_frame, Hkv, D], view by
+    view; new_pos int32 [views * per_frame]) into frame slot ``slot`` of every view
+    of the view-major cache (k_cache/v_cache bf16 [Hkv, cache_stride, D]) and its
+    positions into k_pos (int32 [views * frames * per_frame])."""
+    Hkv, stride, D = k_cache.shape
+    a = bd_stream_insert_args()
+    a.k_cache, a.v_cache, a.k_pos = k_cache.data_ptr(), v_cache.data_ptr(), k_pos.data_ptr()
+    a.new_k, a.new_v, a.new_pos = new_k.data_ptr(), new_v.data_ptr(), new_pos.data_ptr()
+    a.views, a.frames, a.per_frame, a.slot = int(views), int(frames), int(per_frame), int(slot)
+    a.Hkv, a.D, a.cache_stride = Hkv, D, stride
+    _check("bd_stream_insert", lib().bd_stream_insert(a, _stream(stream)))
 
 
 def bd_check(dev_status, stream=None) -> int:

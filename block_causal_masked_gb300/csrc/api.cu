@@ -100,6 +100,7 @@ struct AttnDesc {
   size_t ws_bytes;
   int32_t* ds;
   int prefix_ready;
+  const int32_t* q_pos;  // streaming mask (plain attention only)
 };
 
 // One call runs as one launch, or as two when its (row tile, KV head) groups
@@ -132,7 +133,9 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   if (d.N < 1 || d.n_q < 1 || d.C < 0 || d.Hq < 1 || d.Hkv < 1 || d.priv_len < 0) return BD_ERR_INVALID_ARG;
   if (d.D != 64 && d.D != 128) return BD_ERR_UNSUPPORTED;
   if (d.Hq % d.Hkv != 0) return BD_ERR_UNSUPPORTED;
-  if (d.block_start == nullptr) {
+  if (d.q_pos != nullptr) {
+    if (d.N != 1) return BD_ERR_INVALID_ARG;
+  } else if (d.block_start == nullptr) {
     if (d.block_size < 1) return BD_ERR_INVALID_ARG;
   } else if (d.n_blocks < 1 || d.n_blocks > d.n_q) {
     return BD_ERR_INVALID_ARG;
@@ -147,7 +150,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   pl->rows_per_head = static_cast<int>(rows);
   pl->m_tiles = static_cast<int>((rows + kAttnBM - 1) / kAttnBM);
   pl->n_prefix_tiles = (d.C + kAttnBN - 1) / kAttnBN;
-  const long long priv_tiles = (d.priv_len + d.n_q + kAttnBN - 1) / kAttnBN;
+  // with the streaming mask the queries have no keys of their own
+  const long long priv_tiles = d.q_pos ? 0 : (d.priv_len + d.n_q + kAttnBN - 1) / kAttnBN;
   const long long rolls_per_tile = (kAttnBM - 1) / per_roll + 2 < d.N ? (kAttnBM - 1) / per_roll + 2 : d.N;
   const long long max_tiles = pl->n_prefix_tiles + rolls_per_tile * priv_tiles;
   if (max_tiles > kAttnMaxTiles) return BD_ERR_UNSUPPORTED;
@@ -220,6 +224,9 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.n_prefix_tiles = pl.n_prefix_tiles;
   // the rotated copy of a RoPE call is written by the kernel just before
   p.prefix_early = d.prefix_ready && !(d.rope.enabled && d.C > 0) ? 1 : 0;
+  p.q_pos = d.q_pos;
+  p.kpos = d.rope.k_pos;
+  p.kdelta = d.rope.delta;
   const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
   p.scale_log2 = scale * 1.4426950408889634f;
   // RoPE: the pre-RoPE prefix keys are rotated once for the whole call into
@@ -315,6 +322,11 @@ AttnDesc desc_of(const bd_attn_args* a) {
   d.ws_bytes = a->workspace_bytes;
   d.ds = a->dev_status;
   d.prefix_ready = a->prefix_ready;
+  d.q_pos = a->q_pos;
+  if (d.q_pos) {  // no active rows are read: point the private map at the cache itself
+    d.rk = a->k;
+    d.rv = a->v;
+  }
   return d;
 }
 
@@ -400,7 +412,8 @@ size_t bd_fork_workspace_size(const bd_fork_args* a) {
 
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream) {
   if (!a || !a->q || !a->k || !a->v || !a->o) return BD_ERR_INVALID_ARG;
-  if (a->kv_stride < static_cast<long long>(a->C) + a->n_q) return BD_ERR_INVALID_ARG;
+  if (a->kv_stride < static_cast<long long>(a->C) + (a->q_pos ? 0 : a->n_q)) return BD_ERR_INVALID_ARG;
+  if (a->q_pos && !aligned(a->q_pos, 4)) return BD_ERR_UNSUPPORTED;
   return run_attention(desc_of(a), static_cast<cudaStream_t>(stream));
 }
 
@@ -409,6 +422,36 @@ bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream) {
   if (a->C > 0 && a->prefix_stride < a->C) return BD_ERR_INVALID_ARG;
   if (a->priv_stride < static_cast<long long>(a->priv_len) + a->n_q) return BD_ERR_INVALID_ARG;
   return run_attention(desc_of(a), static_cast<cudaStream_t>(stream));
+}
+
+bd_status bd_stream_insert(const bd_stream_insert_args* a, void* stream) {
+  if (!a || !a->k_cache || !a->v_cache || !a->k_pos || !a->new_k || !a->new_v || !a->new_pos)
+    return BD_ERR_INVALID_ARG;
+  if (a->views < 1 || a->frames < 1 || a->per_frame < 1 || a->Hkv < 1 || a->slot < 0 || a->slot >= a->frames)
+    return BD_ERR_INVALID_ARG;
+  if (a->D != 64 && a->D != 128) return BD_ERR_UNSUPPORTED;
+  const long long window = static_cast<long long>(a->views) * a->frames * a->per_frame;
+  if (window > (1ll << 30) || a->cache_stride < window) return BD_ERR_INVALID_ARG;
+  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->new_k, 16) || !aligned(a->new_v, 16) ||
+      !aligned(a->k_pos, 4) || !aligned(a->new_pos, 4))
+    return BD_ERR_UNSUPPORTED;
+  bd_status st = check_device();
+  if (st != BD_OK) return st;
+  StreamInsertParams p;
+  p.k_cache = a->k_cache;
+  p.v_cache = a->v_cache;
+  p.k_pos = a->k_pos;
+  p.new_k = a->new_k;
+  p.new_v = a->new_v;
+  p.new_pos = a->new_pos;
+  p.views = a->views;
+  p.frames = a->frames;
+  p.per_frame = a->per_frame;
+  p.slot = a->slot;
+  p.Hkv = a->Hkv;
+  p.D = a->D;
+  p.stride = a->cache_stride;
+  return launch_stream_insert(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 size_t bd_unmask_workspace_size(const bd_unmask_args* a) {

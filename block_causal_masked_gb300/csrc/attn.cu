@@ -36,6 +36,7 @@
 // path.
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <cmath>
 
 #include "launch.h"
@@ -134,12 +135,15 @@ __device__ __forceinline__ void bf16x2_unpack(uint32_t w, float& lo, float& hi) 
 
 // cos/sin of pos * freq_d with freq_d / (2 pi) given as a 0.64 fixed-point
 // fraction: the product modulo 2^64 is the fractional turn, so the reduction
-// to [-pi, pi) is exact up to the 2^-32 truncation of its top word.
+// to [-pi, pi) is exact up to the 2^-32 truncation of its top word; the turn is
+// scaled to radians in double (an int32 does not fit a float's significand)
+// and sin / cos are the accurate single-precision functions, so the rotated
+// key is within ~3e-7 of its exact value before the bf16 rounding.
 __device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long turns, float& c, float& s) {
   const unsigned long long prod = static_cast<unsigned long long>(static_cast<long long>(pos)) * turns;
   const int top = static_cast<int>(prod >> 32);
-  const float ang = static_cast<float>(top) * (6.283185307179586f / 4294967296.0f);
-  __sincosf(ang, &s, &c);
+  const float ang = static_cast<float>(static_cast<double>(top) * (6.283185307179586 / 4294967296.0));
+  sincosf(ang, &s, &c);
 }
 
 // The K/V tiles of one CTA: the shared prefix tiles, then the private tiles of
@@ -157,7 +161,7 @@ __device__ __forceinline__ TileRange tile_range(const AttnParams& p, int m0, int
   TileRange tr;
   tr.r_first = m0 / per_roll;
   const int r_last = (row_end - 1) / per_roll;
-  tr.n_priv = (p.priv_len + p.n_q + BN - 1) / BN;
+  tr.n_priv = p.q_pos ? 0 : (p.priv_len + p.n_q + BN - 1) / BN;  // streaming mask: no own keys
   const int total = p.n_prefix_tiles + (r_last - tr.r_first + 1) * tr.n_priv;
   tr.lo = static_cast<int>(static_cast<long long>(split) * total / p.num_splits);
   tr.hi = static_cast<int>(static_cast<long long>(split + 1) * total / p.num_splits);
@@ -520,7 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[QFULL]);
     }
 
-    const int lim_priv = valid ? p.priv_len + block_end_of(p, i_row) : 0;
+    const int lim_priv = valid && !p.q_pos ? p.priv_len + block_end_of(p, i_row) : 0;
+    // streaming mask: this row's query position (nothing is visible to a padding row)
+    const int qpos_row = valid && p.q_pos ? __ldg(p.q_pos + i_row) : INT_MIN;
     const bool warp_active = __any_sync(0xffffffffu, valid);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* xch = reinterpret_cast<float*>(smem + L::kXch);
@@ -543,7 +549,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         nv = max(0, min(BN, lim - te.key0));
         if (warp_active) {
           tmem_ld64(lane_base + s * BN + c0, sv);
-          if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
+          if (p.q_pos) {
+            // key j is visible iff its re-based position is at most the query's
+            const int kb = te.key0 + c0;
+#pragma unroll
+            for (int j = 0; j < BN / 2; ++j) {
+              const int key = kb + j;
+              const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) - p.kdelta : INT_MAX;
+              if (kp > qpos_row) sv[j] = -INFINITY;
+            }
+          } else if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
 #pragma unroll
             for (int j = 0; j < BN / 2; ++j)
               if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0

@@ -53,6 +53,23 @@ struct AttnParams {
   float scale_log2;       // sm_scale * log2(e)
   int q_tma;              // Q tile by TMA (G divides 128)
   int prefix_early;       // prefix K/V tiles may be loaded before the dependency wait
+  // streaming mask (q_pos != null): queries over the prefix only, key j visible
+  // iff (kpos ? kpos[j] : j) - kdelta <= q_pos[i]
+  const int32_t* q_pos;
+  const int32_t* kpos;
+  int kdelta;
+};
+
+// New frame of the streaming cache written into every view's frame slot.
+struct StreamInsertParams {
+  void* k_cache;          // bf16 [Hkv, stride, D]
+  void* v_cache;
+  int32_t* k_pos;         // [views * frames * per_frame]
+  const void* new_k;      // bf16 [views * per_frame, Hkv, D]
+  const void* new_v;
+  const int32_t* new_pos; // [views * per_frame]
+  int views, frames, per_frame, slot, Hkv, D;
+  long long stride;
 };
 
 // Rotation of the cached prefix keys before attention (RoPE at k_pos - delta).
@@ -74,6 +91,7 @@ struct AttnMaps {
 int attn_smem_bytes(int D);
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream);
 cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream);
+cudaError_t launch_stream_insert(const StreamInsertParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- vocab reductions
 

@@ -133,6 +133,16 @@ typedef struct bd_rope {
  *                that kernel is still running (programmatic dependent launch);
  *                q, the active rows and every output are touched only after it
  *                has completed.  Ignored with RoPE.
+ *   q_pos        NULL, or device int32 [n_q] for the streaming mask (FlashDrive
+ *                tutorial, "流式推理": the new frame's tokens are queries over the
+ *                cached window, causally in the view-major positions).  Then
+ *                the queries attend to the cached rows [0, C) only -- the new
+ *                frame's own keys are among them, written by bd_stream_insert
+ *                -- and key j is visible to query i iff
+ *                pos(j) - rope.delta <= q_pos[i], pos(j) = rope.k_pos[j] (j when
+ *                k_pos is NULL), whether or not RoPE is enabled.  block_start /
+ *                block_size are ignored; kv_stride >= C suffices.  A query that
+ *                sees no key gets o = 0 and lse = -inf.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= n_q; 0 <= C; kv_stride >= C + n_q.
  * ---------------------------------------------------------------------------*/
 typedef struct bd_attn_args {
@@ -157,6 +167,7 @@ typedef struct bd_attn_args {
   size_t workspace_bytes;
   int32_t* dev_status;
   int32_t prefix_ready;
+  const int32_t* q_pos;
 } bd_attn_args;
 
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream);
@@ -212,6 +223,48 @@ typedef struct bd_fork_args {
 
 bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream);
 size_t bd_fork_workspace_size(const bd_fork_args* a);
+
+/* -----------------------------------------------------------------------------
+ * bd_stream_insert
+ *
+ * FlashDrive tutorial (agifrontier.github.io), "流式推理": each control step
+ * encodes only the newest camera frame; the history frames' K/V stay in the
+ * cache, which is laid out view-major (all frames of one camera, then the
+ * next), and the new frame's tokens are written into each view's own frame
+ * slot -- not appended at the end -- as pre-RoPE keys.
+ *
+ * The window holds `frames` frame slots of `per_frame` tokens for each of
+ * `views` cameras: slot s of view w is cache rows [(w * frames + s) * per_frame,
+ * + per_frame).  The call writes the new frame into slot `slot` (the caller's
+ * ring index of the oldest frame) of every view, and its positions into k_pos:
+ *   k_cache[h, (w*frames + slot)*per_frame + t, :] = new_k[w*per_frame + t, h, :]
+ *   v_cache likewise;  k_pos[(w*frames + slot)*per_frame + t] = new_pos[w*per_frame + t]
+ * Keys are copied bit for bit (pre-RoPE; attention rotates them at k_pos - delta).
+ *
+ *   k_cache, v_cache  bf16 [Hkv, cache_stride, D], rows [0, views*frames*per_frame)
+ *   k_pos             device int32 [views * frames * per_frame], updated
+ *   new_k, new_v      bf16 [views * per_frame, Hkv, D] (the new frame's tokens,
+ *                     view by view, as the projection writes them)
+ *   new_pos           device int32 [views * per_frame]
+ * Supported: D in {64, 128}; 0 <= slot < frames; cache_stride >= views*frames*per_frame.
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_stream_insert_args {
+  void* k_cache;
+  void* v_cache;
+  int32_t* k_pos;
+  const void* new_k;
+  const void* new_v;
+  const int32_t* new_pos;
+  int32_t views;
+  int32_t frames;
+  int32_t per_frame;
+  int32_t slot;
+  int32_t Hkv;
+  int32_t D;
+  int32_t cache_stride;
+} bd_stream_insert_args;
+
+bd_status bd_stream_insert(const bd_stream_insert_args* a, void* stream);
 
 /* -----------------------------------------------------------------------------
  * bd_unmask_step

@@ -10,6 +10,9 @@ that the tests assert (see the ``margins`` returned by the oracle).
 import numpy as np
 import torch
 
+import oracle
+import synth
+
 DEV = "cuda:0"
 O_ATOL, O_RTOL = 1e-2, 1e-2
 LSE_RTOL = 1e-5
@@ -52,3 +55,37 @@ def assert_attn_close(o, lse, o_ref, lse_ref, what=""):
 
 def status_word() -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def bf16_midpoint_distance(x) -> np.ndarray:
+    """Distance of each float64 value to the nearest midpoint between two bf16
+    values (where rounding to bf16 changes its result); +inf for 0."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    m, e = np.frexp(x)                       # x = m * 2**e, 0.5 <= m < 1
+    scaled = m * 256.0                       # bf16 values are the integers here
+    d = np.abs(scaled - np.floor(scaled) - 0.5) * np.ldexp(1.0, e - 8)
+    return np.where(x == 0.0, np.inf, d)
+
+
+ROPE_MARGIN = 2e-6
+
+
+def condition_rope_keys(k, pos, delta: int, theta: float, seed: int, C: int | None = None,
+                        margin: float = ROPE_MARGIN):
+    """Redraws (in place, seeded) the pre-RoPE prefix key rows [0, C) of k [Hkv, S, D]
+    whose rotated elements lie within `margin` of a bf16 rounding midpoint.
+
+    The bf16 rounding of a rotated key is a decision taken in floating point: the
+    kernel rotates in fp32 (error ~3e-7), the oracle in float64; inputs are kept
+    where no fp32 error can change that rounding, as for every other decision."""
+    C = k.shape[1] if C is None else C
+    p = np.asarray(pos, dtype=np.int64)[:C] - int(delta)
+    for attempt in range(100):
+        r = oracle.rope_rotate(k[:, :C], p, theta)
+        bad = np.argwhere((bf16_midpoint_distance(r) < margin).any(axis=-1))
+        if bad.size == 0:
+            return k
+        g = synth.rng(seed, 990, attempt)
+        for h, j in bad:
+            k[h, j] = synth.to_bf16(g.standard_normal(k.shape[-1]).astype(np.float32))
+    raise AssertionError("rope keys could not be conditioned")

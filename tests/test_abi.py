@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol():
     assert set(_declared()) <= exported
 
 
-STRUCTS = ["bd_rope", "bd_attn_args", "bd_fork_args", "bd_unmask_args", "bd_verify_args"]
+STRUCTS = ["bd_rope", "bd_attn_args", "bd_fork_args", "bd_unmask_args", "bd_verify_args", "bd_stream_insert_args"]
 
 
 def test_ctypes_structs_match_c_layout(tmp_path):
@@ -122,3 +122,24 @@ def test_vocab_argument_errors_on_host():
     v = bd.bd_verify_args()
     v.n_seq, v.L, v.n_rows, v.V, v.logits_ld = 1, 4, 9, 100, 104
     assert bd.lib().bd_spec_verify(v, None) == 1          # n_rows > L + 1
+
+
+def test_stream_insert_argument_errors_on_host():
+    a = bd.bd_stream_insert_args()
+    a.k_cache = a.v_cache = a.k_pos = a.new_k = a.new_v = a.new_pos = FAKE
+    a.views, a.frames, a.per_frame, a.slot, a.Hkv, a.D, a.cache_stride = 4, 4, 256, 0, 2, 128, 4096
+    for kw, want in ((dict(slot=4), 1), (dict(slot=-1), 1), (dict(views=0), 1), (dict(cache_stride=4095), 1),
+                     (dict(D=96), 2), (dict(new_k=FAKE + 8), 2), (dict(k_pos=None), 1)):
+        b = bd.bd_stream_insert_args.from_buffer_copy(a)
+        for k, v in kw.items():
+            setattr(b, k, v)
+        assert bd.lib().bd_stream_insert(b, None) == want, kw
+
+
+def test_streaming_mask_argument_errors_on_host():
+    """With q_pos the active rows are not read (kv_stride >= C suffices), the block
+    partition is not needed, and a misaligned q_pos is refused."""
+    a = _attn(kv_stride=100, block_size=0, q_pos=FAKE + 2)
+    assert bd.lib().bd_block_causal_attn(a, None) == 2
+    a = _attn(kv_stride=99, block_size=0, q_pos=FAKE)
+    assert bd.lib().bd_block_causal_attn(a, None) == 1

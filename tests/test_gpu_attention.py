@@ -12,7 +12,7 @@ import torch
 import block_causal_masked_gb300 as bd
 import oracle
 import synth
-from helpers import DEV, assert_attn_close, bf16, host, i32, status_word
+from helpers import DEV, assert_attn_close, bf16, condition_rope_keys, host, i32, status_word
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +89,7 @@ def test_in_kernel_rope_matches_oracle(D):
     C = 600
     case = synth.attn_case(14, D, C=C, block_start=[0, 12, 20], Hq=16, Hkv=2, D=D)
     k_pos = (np.arange(C) * 3 + 256).astype(np.int32)
+    condition_rope_keys(case.k, k_pos, 256, 10000.0, 14, C=C)
     rope = dict(k_pos=i32(k_pos), delta=256, theta=10000.0)
     o, lse = _run(case, 0, rope=rope)
     o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, C, case.block_start, k_pos=k_pos,
@@ -102,6 +103,7 @@ def test_in_kernel_rope_equals_prerotated_keys():
     C = 4096 + 210
     case = synth.attn_case(15, 0, C=C, block_start=[0, 39], Hq=16, Hkv=2, D=128)
     k_pos = synth.streaming_prefix_positions()
+    condition_rope_keys(case.k, k_pos, 256, 1e4, 15, C=C)
     o, lse = _run(case, 0, rope=dict(k_pos=i32(k_pos), delta=256, theta=1e4))
     k2 = case.k.copy()
     k2[:, :C] = oracle.round_bf16(oracle.rope_rotate(case.k[:, :C], k_pos.astype(np.int64) - 256, 1e4))
@@ -117,8 +119,11 @@ def _fork(seed, N, C, n_q, priv_len, bs, D=128, rope=False):
     k_pos = synth.streaming_prefix_positions(sections=C - 4096) if rope and C > 4096 else None
     if rope and k_pos is None:
         k_pos = (np.arange(C) + 256).astype(np.int32)
-    return synth.fork_case(seed, 0, N=N, C=C, n_q=n_q, priv_len=priv_len, block_start=bs, Hq=16, Hkv=2, D=D,
-                           k_pos=k_pos, delta=256 if rope else 0, theta=1e4)
+    f = synth.fork_case(seed, 0, N=N, C=C, n_q=n_q, priv_len=priv_len, block_start=bs, Hq=16, Hkv=2, D=D,
+                        k_pos=k_pos, delta=256 if rope else 0, theta=1e4)
+    if rope:
+        condition_rope_keys(f.prefix_k, k_pos, 256, 1e4, seed)
+    return f
 
 
 def _run_fork(f, splits=0, rope=False):
@@ -182,6 +187,8 @@ def test_prefix_ready_matches_default_in_a_graph(rope):
     RoPE the flag is ignored.  The last launch also matches the oracle."""
     C, bs, n = 1500, [0, 33], 4
     case = synth.attn_case(12, 0, C=C, block_start=bs, Hq=16, Hkv=2, D=128)
+    if rope:
+        condition_rope_keys(case.k, np.arange(C) + 7, 7, 1e4, 12, C=C)
     k, v = bf16(case.k), bf16(case.v)
     q0 = bf16(case.q)
     blk = i32(bs)

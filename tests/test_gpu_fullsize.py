@@ -13,7 +13,7 @@ import bench
 import block_causal_masked_gb300 as bd
 import oracle
 import synth
-from helpers import CONF_RTOL, DEV, assert_attn_close, bf16, f32, host, i32, status_word, u8
+from helpers import CONF_RTOL, DEV, assert_attn_close, bf16, condition_rope_keys, f32, host, i32, status_word, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +75,7 @@ def test_fork_streaming_full_size(N):
     k_pos = synth.streaming_prefix_positions()
     f = synth.fork_case(4, N, N=N, C=C, n_q=39, priv_len=41, block_start=[0, 39], Hq=16, Hkv=2, D=128,
                         k_pos=k_pos, delta=256, theta=1e4)
+    condition_rope_keys(f.prefix_k, k_pos, 256, 1e4, 4)
     ds = status_word()
     o, lse = bd.bd_fork_rollouts(bf16(f.q), bf16(f.prefix_k), bf16(f.prefix_v), bf16(f.priv_k), bf16(f.priv_v),
                                  f.priv_len, C, block_start=i32(f.block_start),

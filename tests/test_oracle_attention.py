@@ -264,3 +264,19 @@ def test_fork_rollouts_are_independent():
     pk2[1] += 5.0
     o2, _ = oracle.fork_attention(q, f.prefix_k, f.prefix_v, pk2, pv, f.priv_len, f.block_start)
     assert np.array_equal(o[[0, 2]], o2[[0, 2]]) and not np.array_equal(o[1], o2[1])
+
+
+def test_rope_key_conditioning_margin():
+    """The helper that keeps RoPE test inputs away from bf16 rounding midpoints:
+    hand values (bf16 spacing is 2^-7 on [1, 2): 1 + 2^-8 is a midpoint, 1 and
+    1 + 2^-7 are bf16 values half a spacing from one; spacing 2^-6 at 3), and
+    conditioned keys keep the margin."""
+    import helpers
+    d = helpers.bf16_midpoint_distance(np.array([1.0, 1.0 + 2 ** -8, 1.0 + 2 ** -7, 0.0, -3.0]))
+    assert d[0] == 2 ** -8 and d[1] == 0.0 and d[2] == 2 ** -8
+    assert np.isinf(d[3]) and d[4] == 2 ** -7
+    k = synth.attn_case(30, 0, C=200, block_start=[0, 4], Hq=4, Hkv=2, D=16).k
+    pos = np.arange(200) * 5
+    helpers.condition_rope_keys(k, pos, 3, 1e4, 30, C=200)
+    r = oracle.rope_rotate(k[:, :200], pos - 3, 1e4)
+    assert (helpers.bf16_midpoint_distance(r) >= helpers.ROPE_MARGIN).all()
