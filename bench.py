@@ -689,6 +689,86 @@ def run_fork(args, dev):
         torch.cuda.empty_cache()
 
 
+def run_stream(args, dev):
+    """FlashDrive streaming step: a new camera frame (4 views x 256 tokens) enters
+    the view-major pre-RoPE window of 4 frames per view (4,096 keys, 16/2 heads,
+    head dim 128), 36 layers of bd_stream_insert (the frame's K/V into every
+    view's ring slot) + bd_block_causal_attn with the streaming mask (the
+    frame's 1,024 queries over the window, RoPE at k_pos - delta).  Value: new
+    frame tokens per second."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    S = synth.FORK_STREAM
+    views, frames, per, Hq, Hkv, D, L = 4, 4, 256, S.Hq, S.Hkv, S.D, S.layers
+    C = views * frames * per
+    n = views * per
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(S.seed * 1000 + 7)
+    bf = torch.bfloat16
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(bf)  # noqa: E731
+    kc = [rn(Hkv, C, D) for _ in range(L)]
+    vc = [rn(Hkv, C, D) for _ in range(L)]
+    nk = [rn(n, Hkv, D) for _ in range(L)]
+    nv = [rn(n, Hkv, D) for _ in range(L)]
+    q = [rn(n, Hq, D) for _ in range(L)]
+    # window of frame times 1..4 after one slide (delta = one frame); the new
+    # frame (time 4) goes into slot 0, where frame 0 was
+    w = np.arange(views)[:, None, None]
+    f = np.arange(frames)[None, :, None]
+    t = np.arange(per)[None, None, :]
+    slot_time = np.array([4, 1, 2, 3])[None, :, None]                     # frame time held by each slot
+    pos0 = ((w * frames + slot_time) * per + t).reshape(-1).astype(np.int32)
+    kpos = torch.from_numpy(pos0).to(dev)
+    delta = per
+    new_pos = torch.from_numpy(((np.arange(views)[:, None] * frames + 4) * per
+                                + np.arange(per)[None, :]).reshape(-1).astype(np.int32)).to(dev)
+    qpos = (new_pos - delta).contiguous()
+    o = torch.empty((n, Hq, D), dtype=bf, device=dev)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=dev)
+    rope = dict(k_pos=kpos, delta=delta, theta=1e4)
+
+    def step():
+        for l in range(L):
+            bd.bd_stream_insert(kc[l], vc[l], kpos, nk[l], nv[l], new_pos, views, frames, per, 0)
+            bd.bd_block_causal_attn(q[l], kc[l], vc[l], C, q_pos=qpos, rope=rope, o=o, lse=lse)
+
+    def attn_only():
+        for l in range(L):
+            bd.bd_block_causal_attn(q[l], kc[l], vc[l], C, q_pos=qpos, rope=rope, o=o, lse=lse)
+
+    def insert_only():
+        for l in range(L):
+            bd.bd_stream_insert(kc[l], vc[l], kpos, nk[l], nv[l], new_pos, views, frames, per, 0)
+
+    g = _graph(step)
+    for _ in range(args.warmup):
+        g.replay()
+    step_ms = _replay_ms(g, args.steps, flush)
+    attn_us = _replay_ms(_graph(attn_only), args.steps, flush) * 1e3 / L
+    ins_us = _replay_ms(_graph(insert_only), args.steps, flush) * 1e3 / L
+    peaks = measured_peaks()
+    # visible keys per query: every earlier view, its own view's history, its frame up to itself
+    pos_np = pos0.astype(np.int64) - delta
+    qp = (new_pos.cpu().numpy().astype(np.int64) - delta)
+    vis = int((pos_np[None, :] <= qp[:, None]).sum())
+    flops = 4 * D * Hq * vis
+    nbytes = 2 * Hkv * C * D * 2 + 2 * n * Hq * D * 2 + n * Hq * 4 + C * 4
+    kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, flops, peaks, True),
+               "stream_insert_kernel": _vocab_roof(ins_us, 2 * 2 * n * Hkv * D * 2 + 2 * n * 4, peaks),
+               "rope_prefix_kernel": "inside attn_kernel's time (one launch per attention call)"}
+    line = {"metric": "new-frame tokens/s (streaming step: insert + streaming-mask attention, 36 layers)",
+            "value": n / step_ms * 1e3, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"stream: 4 views x 4 frames x 256 tokens view-major pre-RoPE window, new "
+                                   f"frame of {n} tokens, 16/2 heads, head dim 128, 36 layers, RoPE at k_pos - "
+                                   f"{delta}", "l2": "flushed (256 MiB write) before every timed step",
+                       "visible_keys_per_query": vis / n},
+            "roofline": kernels}
+    print(json.dumps(line), flush=True)
+
+
 def algorithmic(inp):
     """Bytes (and FLOPs) the round must move: visible K/V, Q, O, LSE per layer;
     logits rows of masked editable positions; AR rows."""
@@ -1006,18 +1086,20 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork"],
+    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork", "stream"],
                     default="fast_ddrive",
                     help="fast_ddrive: the contract's line; the others print extra lines: wam_sweep (the whole "
                          "WAM-Diff2 decode per block size as one CUDA graph), tiny, fast_dvla (one denoise step of "
-                         "the 3-block window), fork (one round for N = 1, 8, 32 rollouts)")
+                         "the 3-block window), fork (one round for N = 1, 8, 32 rollouts), stream (one new camera frame "
+                         "into the streaming window: insert + streaming-mask attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    extra = {"wam_sweep": run_wam_sweep, "tiny": run_tiny, "fast_dvla": run_fast_dvla, "fork": run_fork}
+    extra = {"wam_sweep": run_wam_sweep, "tiny": run_tiny, "fast_dvla": run_fast_dvla, "fork": run_fork,
+             "stream": run_stream}
     if args.workload in extra:
         import torch
         torch.cuda.set_device(local_rank)

@@ -413,7 +413,7 @@ size_t bd_fork_workspace_size(const bd_fork_args* a) {
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream) {
   if (!a || !a->q || !a->k || !a->v || !a->o) return BD_ERR_INVALID_ARG;
   if (a->kv_stride < static_cast<long long>(a->C) + (a->q_pos ? 0 : a->n_q)) return BD_ERR_INVALID_ARG;
-  if (a->q_pos && !aligned(a->q_pos, 4)) return BD_ERR_UNSUPPORTED;
+  if (a->q_pos && (!aligned(a->q_pos, 4) || (a->rope.k_pos && !aligned(a->rope.k_pos, 16)))) return BD_ERR_UNSUPPORTED;
   return run_attention(desc_of(a), static_cast<cudaStream_t>(stream));
 }
 

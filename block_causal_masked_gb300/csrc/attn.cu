@@ -135,14 +135,15 @@ __device__ __forceinline__ void bf16x2_unpack(uint32_t w, float& lo, float& hi) 
 
 // cos/sin of pos * freq_d with freq_d / (2 pi) given as a 0.64 fixed-point
 // fraction: the product modulo 2^64 is the fractional turn, so the reduction
-// to [-pi, pi) is exact up to the 2^-32 truncation of its top word; the turn is
-// scaled to radians in double (an int32 does not fit a float's significand)
-// and sin / cos are the accurate single-precision functions, so the rotated
-// key is within ~3e-7 of its exact value before the bf16 rounding.
+// to [-pi, pi) is exact up to the 2^-32 truncation of its top word; the turn
+// becomes an fp32 angle (error below 1e-7 rad) and sin / cos are the accurate
+// single-precision functions, so a rotated key is within ~1e-6 of its exact
+// value before the bf16 rounding.  (Scaling the turn in double measured 6 us
+// slower per call: fp64 is slow on this part.)
 __device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long turns, float& c, float& s) {
   const unsigned long long prod = static_cast<unsigned long long>(static_cast<long long>(pos)) * turns;
   const int top = static_cast<int>(prod >> 32);
-  const float ang = static_cast<float>(static_cast<double>(top) * (6.283185307179586 / 4294967296.0));
+  const float ang = static_cast<float>(top) * (6.283185307179586f / 4294967296.0f);
   sincosf(ang, &s, &c);
 }
 
@@ -305,7 +306,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   }
 }
 
-template <int D>
+// STREAM: the streaming mask (q_pos), compiled apart so that the block-causal
+// path carries none of its code.
+template <int D, bool STREAM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   using L = Layout<D>;
@@ -524,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[QFULL]);
     }
 
-    const int lim_priv = valid && !p.q_pos ? p.priv_len + block_end_of(p, i_row) : 0;
+    const int lim_priv = valid && !STREAM ? p.priv_len + block_end_of(p, i_row) : 0;
     // streaming mask: this row's query position (nothing is visible to a padding row)
-    const int qpos_row = valid && p.q_pos ? __ldg(p.q_pos + i_row) : INT_MIN;
+    const int qpos_row = valid && STREAM ? __ldg(p.q_pos + i_row) : INT_MIN;
     const bool warp_active = __any_sync(0xffffffffu, valid);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* xch = reinterpret_cast<float*>(smem + L::kXch);
@@ -549,14 +552,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         nv = max(0, min(BN, lim - te.key0));
         if (warp_active) {
           tmem_ld64(lane_base + s * BN + c0, sv);
-          if (p.q_pos) {
-            // key j is visible iff its re-based position is at most the query's
+          if constexpr (STREAM) {
+            // key j is visible iff its re-based position is at most the query's;
+            // the positions of this half of the tile are read 16 bytes at a time,
+            // 32 keys per batch with every load issued before the first is used
             const int kb = te.key0 + c0;
+            const long long lim_q = static_cast<long long>(qpos_row) + p.kdelta;  // stored positions <= lim_q
 #pragma unroll
-            for (int j = 0; j < BN / 2; ++j) {
-              const int key = kb + j;
-              const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) - p.kdelta : INT_MAX;
-              if (kp > qpos_row) sv[j] = -INFINITY;
+            for (int b = 0; b < BN / 64; ++b) {
+              const int k0 = kb + 32 * b;
+              if (p.kpos != nullptr && k0 + 32 <= p.C) {
+                int4 kp4[8];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) kp4[j4] = __ldg(reinterpret_cast<const int4*>(p.kpos + k0) + j4);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                  if (kp4[j4].x > lim_q) sv[32 * b + 4 * j4 + 0] = -INFINITY;
+                  if (kp4[j4].y > lim_q) sv[32 * b + 4 * j4 + 1] = -INFINITY;
+                  if (kp4[j4].z > lim_q) sv[32 * b + 4 * j4 + 2] = -INFINITY;
+                  if (kp4[j4].w > lim_q) sv[32 * b + 4 * j4 + 3] = -INFINITY;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int key = k0 + j;
+                  const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) : INT_MAX;
+                  if (key >= p.C || kp > lim_q) sv[32 * b + j] = -INFINITY;
+                }
+              }
             }
           } else if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
 #pragma unroll
@@ -675,11 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool STREAM>
 cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
   static bool configured = false;
   const int smem = attn_smem_bytes(D);
-  auto kernel = attn_kernel<D>;
+  auto kernel = attn_kernel<D, STREAM>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -775,7 +798,11 @@ int attn_smem_bytes(int D) {
 }
 
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
-  return p.D == 128 ? launch_attn_t<128>(p, maps, m_tiles, stream) : launch_attn_t<64>(p, maps, m_tiles, stream);
+  if (p.q_pos)
+    return p.D == 128 ? launch_attn_t<128, true>(p, maps, m_tiles, stream)
+                      : launch_attn_t<64, true>(p, maps, m_tiles, stream);
+  return p.D == 128 ? launch_attn_t<128, false>(p, maps, m_tiles, stream)
+                    : launch_attn_t<64, false>(p, maps, m_tiles, stream);
 }
 
 cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream) {

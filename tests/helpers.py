@@ -76,8 +76,10 @@ def condition_rope_keys(k, pos, delta: int, theta: float, seed: int, C: int | No
     whose rotated elements lie within `margin` of a bf16 rounding midpoint.
 
     The bf16 rounding of a rotated key is a decision taken in floating point: the
-    kernel rotates in fp32 (error ~3e-7), the oracle in float64; inputs are kept
-    where no fp32 error can change that rounding, as for every other decision."""
+    kernel rotates in fp32 (angle within 1e-7 rad, sin / cos within an ulp, so a
+    rotated element of keys below 8 in magnitude is within ~1.2e-6), the oracle
+    in float64; inputs are kept where no such error can change that rounding, as
+    for every other decision."""
     C = k.shape[1] if C is None else C
     p = np.asarray(pos, dtype=np.int64)[:C] - int(delta)
     for attempt in range(100):
