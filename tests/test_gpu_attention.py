@@ -224,3 +224,16 @@ def test_prefix_ready_matches_default_in_a_graph(rope):
     kw = dict(k_pos=host(kp), delta=7, theta=1e4, rope=True) if rope else {}
     o_ref, lse_ref = oracle.block_causal_attention(q_last, case.k, case.v, C, bs, **kw)
     assert_attn_close(torch.from_numpy(o1[-1]), torch.from_numpy(l1[-1]), o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_two_launch_plan_matches_oracle(D):
+    """More (row tile, KV head) groups than one wave of SMs: 2,500 positions x 8
+    query heads on one KV head = 157 row tiles, run as a bulk launch of 152
+    unsplit row tiles and a tail of 5 split wide; block size 100."""
+    n_q, C = 2500, 200
+    bs = list(range(0, n_q, 100)) + [n_q]
+    case = synth.attn_case(40, D, C=C, block_start=bs, Hq=8, Hkv=1, D=D)
+    o, lse = _run(case, 0)
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, C, bs)
+    assert_attn_close(o, lse, o_ref, lse_ref, f"two-launch D={D}")

@@ -322,3 +322,47 @@ def test_unmask_draft_mode_matches_oracle():
     g = {k: host(v) for k, v in r.items()} | dict(state=host(st), tokens=host(tk))
     _compare_unmask(g, o)
     assert (g["state"] == synth.MASKED).any() and (g["tokens"][scaf == 0] >= 0).all()
+
+
+def test_unmask_maximum_window():
+    """The largest window the library takes (2,048 positions): 64 blocks of 32
+    with 3 scaffold slots each, the first 20 blocks partly committed, Fast-dVLA
+    activation thresholds, bf16 logits [masked rows, 4,096] with planted peaks."""
+    n_pos, Bsz, Vv = 2048, 32, 4096
+    lay = synth.uniform_layout(n_pos, Bsz, scaffold_per_block=3, seed=50)
+    g0 = synth.rng(50, 1)
+    state = np.where(lay.scaffold == 1, synth.SCAFFOLD, synth.MASKED).astype(np.int64)
+    for b in range(20):
+        ed = np.flatnonzero(state[b * Bsz:(b + 1) * Bsz] == synth.MASKED) + b * Bsz
+        state[g0.choice(ed, size=int(g0.integers(len(ed) // 2, len(ed) + 1)), replace=False)] = synth.COMMITTED
+    tokens = np.where(state == synth.MASKED, -1, 7)
+    masked = np.flatnonzero(state == synth.MASKED)
+    logit_row = np.full(n_pos, -1)
+    logit_row[masked] = np.arange(len(masked))
+    kw = dict(tau_full=0.9, tau_half=0.9, min_frac=Fraction(1, 4), k_fixed=0, add_thr=Fraction(1, 2),
+              act_thr=Fraction(17, 20))
+    for attempt in range(20):
+        x, _, _ = synth.planted_logits(50, 100 + attempt, len(masked), Vv)
+        g, o = _step_both(x, logit_row, lay.block_start, state, tokens, True, **kw)
+        if g is not None:
+            break
+    assert g is not None
+    assert {bd.FULL, bd.HALF, bd.INACTIVE} <= set(int(s) for s in o["status"])
+
+
+def test_verify_maximum_block():
+    """The longest verified block (1,024 slots, 1/8 scaffold) for two sequences,
+    one matching its draft to the end (bonus after the block), one diverging
+    at slot 700; V = 2,048 fp32."""
+    L, Vv, n_seq = 1024, 2048, 2
+    g = synth.rng(51, 0)
+    scaf = np.zeros(L, np.int64)
+    scaf[g.choice(L, L // 8, replace=False)] = 1
+    E = int((scaf == 0).sum())
+    state = np.tile(np.where(scaf == 1, synth.SCAFFOLD, synth.MASKED), (n_seq, 1))
+    drafts = g.integers(0, Vv, size=(n_seq, L))
+    ar = np.stack([_plant_ar(51, s, drafts[s][scaf == 0], k, Vv, False) for s, k in enumerate((E, 700))])
+    o = oracle.spec_verify(drafts, state, ar)
+    gg = _gpu_verify(drafts, state, ar, False)
+    _compare_verify(gg, o)
+    assert list(o["accepted_len"]) == [E + 1, 701] and o["bonus_pos"][0] == L
