@@ -62,8 +62,10 @@ struct TileEntry {
 
 
 enum Bar : int {
-  KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 13, QFULL = 14,
-  DRAIN = 15, MERGE_O = 16, NUM_BARS = 17
+  // PFULL / ODONE: two each, by tile parity (tile t uses PFULL + t % 2 and
+  // ODONE + t % 2), so that the softmax may run one tile ahead of P.V
+  KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 14, QFULL = 16,
+  DRAIN = 17, MERGE_O = 18, NUM_BARS = 19
 };
 
 template <int D>
@@ -377,8 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars[SFULL + 0], 1);
     mbar_init(&bars[SFULL + 1], 1);
-    mbar_init(&bars[PFULL], 32 * kSmWarps);
-    mbar_init(&bars[ODONE], 1);
+    mbar_init(&bars[PFULL + 0], 32 * kSmWarps);
+    mbar_init(&bars[PFULL + 1], 32 * kSmWarps);
+    mbar_init(&bars[ODONE + 0], 1);
+    mbar_init(&bars[ODONE + 1], 1);
     mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
     mbar_init(&bars[DRAIN], 1);
     mbar_init(&bars[MERGE_O], 1);
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int t = 0; ok && t < nt; ++t) {
         if (t + 1 < nt && !issue_s(t + 1)) break;
-        if (!mbar_wait(&bars[PFULL], t & 1, abort_flag, ds)) break;
+        if (!mbar_wait(&bars[PFULL + (t & 1)], (t >> 1) & 1, abort_flag, ds)) break;
         if (!mbar_wait(&bars[VFULL + t % kVStages], (t / kVStages) & 1, abort_flag, ds)) break;
         tc_fence_after();
         const uint32_t va = smem_addr(smem + L::kV + (t % kVStages) * L::kKVBytes);
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + 2 * BN, pt + acol, sw128_desc(va + voff, BN * 128, 1024), kIdPV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars[ODONE]);
+        mma_commit(&bars[ODONE + (t & 1)]);
         mma_commit(&bars[VEMPTY + t % kVStages]);
       }
       mma_commit(&bars[DRAIN]);
@@ -610,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O must be rescaled (rare once the running max has settled): that needs
       // the previous tile's P.V to have finished first
       const bool rescale = warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      if (rescale) {
-        ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
+      if (rescale) {  // P.V(t - 1) must have finished updating O
+        ok = all_lanes(mbar_wait(&bars[ODONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag, ds));
         if (!ok) continue;
         tc_fence_after();
 #pragma unroll
@@ -645,15 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
       }
-      if (t > 0 && !rescale) {  // keeps the wait on every P.V phase in order
-        ok = all_lanes(mbar_wait(&bars[ODONE], (t - 1) & 1, abort_flag, ds));
+      // P(t) does not wait for P.V(t - 1): it goes into the other S buffer.
+      // The wait on P.V(t - 2) -- already done, since S(t) was issued after it
+      // and tcgen05.mma runs in issue order -- only keeps this thread's view of
+      // each ODONE barrier within one phase (no parity aliasing later).
+      if (t >= 2) {
+        ok = all_lanes(mbar_wait(&bars[ODONE + (t & 1)], ((t - 2) >> 1) & 1, abort_flag, ds));
         if (!ok) continue;
       }
       tc_fence_before();
-      mbar_arrive(&bars[PFULL]);
+      mbar_arrive(&bars[PFULL + (t & 1)]);
     }
-    if (ok && nt > 0) {
-      ok = all_lanes(mbar_wait(&bars[ODONE], (nt - 1) & 1, abort_flag, ds));
+    if (ok && nt > 0) {  // the last P.V (and, in issue order, every earlier one)
+      ok = all_lanes(mbar_wait(&bars[ODONE + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag, ds));
       tc_fence_after();
     }
     have_o = ok && nt > 0;
