@@ -166,8 +166,11 @@ __device__ __forceinline__ TileRange tile_range(const AttnParams& p, int m0, int
   const int r_last = (row_end - 1) / per_roll;
   tr.n_priv = p.q_pos ? 0 : (p.priv_len + p.n_q + BN - 1) / BN;  // streaming mask: no own keys
   const int total = p.n_prefix_tiles + (r_last - tr.r_first + 1) * tr.n_priv;
-  tr.lo = static_cast<int>(static_cast<long long>(split) * total / p.num_splits);
-  tr.hi = static_cast<int>(static_cast<long long>(split + 1) * total / p.num_splits);
+  // ceil boundaries: when the splits cannot all take the same number of
+  // tiles, the last split (which holds the diagonal tiles of the active
+  // block, the slowest to process) is among those that take fewer
+  tr.lo = static_cast<int>((static_cast<long long>(split) * total + p.num_splits - 1) / p.num_splits);
+  tr.hi = static_cast<int>((static_cast<long long>(split + 1) * total + p.num_splits - 1) / p.num_splits);
   return tr;
 }
 
@@ -185,7 +188,7 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 //      (running max m, sum l) straight into that CTA's shared memory;
 //   2. cluster barrier (release / acquire): every split's rows are written;
 //   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S O slices
-//      into shared memory with bulk copies on one mbarrier; meanwhile the
+//      (contiguous) into shared memory with one bulk copy; meanwhile the
 //      softmax threads form the weights l_s 2^(m_s - M) / L once per row
 //      (M = max m_s, L = sum l_s 2^(m_s - M)), then store O = sum w_s O_s in
 //      bf16 and LSE = (M + log2 L) ln 2.
@@ -203,7 +206,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   int32_t* ds = p.dev_status;
   uint4* part_o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.part) +
                                            (static_cast<size_t>(blockIdx.z) * p.m_tiles + p.m_tile0 + blockIdx.y) *
-                                               attn_part_bytes(S, D));  // [S][S][kCh][rpc]
+                                               attn_part_bytes(S, D));  // [owner][split][kCh][rpc]
   float2* recv_ml = reinterpret_cast<float2*>(smem + L::kMLRecv);         // [S][rpc]
   if (is_sm) {
     const int quad = warp & 3;
@@ -212,7 +215,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
       const int q = rl / rpc;
       const int r = rl - q * rpc;
-      uint4* dst = part_o + static_cast<size_t>(split * S + q) * kCh * rpc + r;
+      uint4* dst = part_o + static_cast<size_t>(q * S + split) * kCh * rpc + r;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + 2 * BN + half * (D / 2);
       const float inv_l = have_o && l_tot > 0.f ? 1.f / l_tot : 0.f;
       float v[32];
@@ -246,9 +249,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   if (threadIdx.x == 0) {
     fence_proxy_async_global();
     mbar_arrive_expect_tx(&bars[MERGE_O], static_cast<uint32_t>(S * kCh * rpc * 16));
-    for (int s2 = 0; s2 < S; ++s2)
-      bulk_load(recv_o + s2 * kCh * rpc, part_o + static_cast<size_t>(s2 * S + split) * kCh * rpc, kCh * rpc * 16,
-                &bars[MERGE_O]);
+    // the S slices of this owner are contiguous: one copy (measured faster
+    // than one copy per slice)
+    bulk_load(recv_o, part_o + static_cast<size_t>(split * S) * kCh * rpc, S * kCh * rpc * 16, &bars[MERGE_O]);
     // the copies land before this thread reaches the CTA's final barrier
     mbar_drain(&bars[MERGE_O], 0, ds);
   }

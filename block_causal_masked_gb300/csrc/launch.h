@@ -28,8 +28,8 @@ __host__ __device__ constexpr int attn_resident_clusters(int S) {
 // of the tile, r = ceil(128 / S) rounded up to even.
 __host__ __device__ constexpr int attn_merge_rows(int S) { return ((kAttnBM + S - 1) / S + 1) & ~1; }
 // Partial O of one (KV head, row tile) in the slices that one split hands one
-// owner, contiguous: [S splits][S owners][D / 8][r] bf16x8 chunks of the
-// split's normalised O.  (The splits' running max and sum travel through
+// owner: [S owners][S splits][D / 8][r] bf16x8 chunks of the splits'
+// normalised O, so that an owner's slices are one contiguous range.  (The splits' running max and sum travel through
 // distributed shared memory.)
 __host__ __device__ constexpr long long attn_part_bytes(int S, int D) {
   return static_cast<long long>(S) * S * attn_merge_rows(S) * 2 * D;
