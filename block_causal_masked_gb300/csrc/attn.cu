@@ -86,11 +86,9 @@ struct Layout {
   static constexpr int kMLRecv = kXch + 6 * BM * 4;
   static constexpr int kEnd = kMLRecv + (BM + 2 * kAttnMaxSplits) * 8;
   // split-KV merge, over the K / V rings (idle by then): the S bf16 O
-  // slices of this CTA's rows (S * r <= BM + 2 * S rows), then the weights
-  // [S][r] and LSE [r] of those rows
+  // slices of this CTA's rows (S * r <= BM + 2 * S rows)
   static constexpr int kRecv = kK;
-  static constexpr int kWts = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
-  static_assert(kWts + (BM / 2 + 2) * (kAttnMaxSplits + 1) * 4 <= kRingEnd, "merge buffers must fit");
+  static_assert(kRecv + (BM + 2 * kAttnMaxSplits) * D * 2 <= kRingEnd, "merge slices must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
@@ -188,10 +186,11 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 //      (running max m, sum l) straight into that CTA's shared memory;
 //   2. cluster barrier (release / acquire): every split's rows are written;
 //   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S O slices
-//      (contiguous) into shared memory with one bulk copy; meanwhile the
-//      softmax threads form the weights l_s 2^(m_s - M) / L once per row
-//      (M = max m_s, L = sum l_s 2^(m_s - M)), then store O = sum w_s O_s in
-//      bf16 and LSE = (M + log2 L) ln 2.
+//      (contiguous) into shared memory with one bulk copy; meanwhile each
+//      softmax thread takes a (row, 8 columns) item and forms its row's
+//      weights l_s 2^(m_s - M) / L (M = max m_s, L = sum l_s 2^(m_s - M)),
+//      then stores O = sum w_s O_s in bf16 and, for the first 8 columns,
+//      LSE = (M + log2 L) ln 2.
 template <int D>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
                               float l_tot, uint64_t* bars, volatile int* abort_flag) {
@@ -259,55 +258,55 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int t = threadIdx.x - 64;
   const int per_roll = p.n_q * p.G;
   const int kvh = blockIdx.z;
-  float* wts = reinterpret_cast<float*>(smem + L::kWts);  // [S][rpc] weights of the splits
-  float* lse_row = wts + S * rpc;                        // [rpc]
-  {
-    // one half-warp per row, lane s2 = split s2 (S <= 16)
-    const int s2 = lane & 15;
-    for (int j = (warp - 2) * 2 + (lane >> 4); j < mine; j += 2 * kSmWarps) {
-      const float2 ml = s2 < S ? recv_ml[s2 * rpc + j] : make_float2(-INFINITY, 0.f);
-      float M = ml.y > 0.f ? ml.x : -INFINITY;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float wl = ml.y > 0.f ? ml.y * fast_exp2(ml.x - M) : 0.f;
-      float Ls = wl;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-      if (s2 < S) wts[s2 * rpc + j] = Ls > 0.f ? wl * fast_rcp(Ls) : 0.f;
-      if (s2 == 0) lse_row[j] = Ls > 0.f ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
-    }
-  }
-  named_sync(1, kThreads);
-  if (!all_lanes(mbar_wait(&bars[MERGE_O], 0, abort_flag, ds))) return;
   for (int it = t; it < mine * kCh; it += kThreads) {
     const int ch = it / mine;  // consecutive threads: consecutive rows of one chunk
     const int j = it - ch * mine;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-      if (s2 < S) {
-        const float w = wts[s2 * rpc + j];
-        const uint4 x = recv_o[(s2 * kCh + ch) * rpc + j];
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float a, b;
-          bf16x2_unpack(xw[e], a, b);
-          acc[2 * e] = fmaf(w, a, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(w, b, acc[2 * e + 1]);
-        }
-      }
-    }
     const int grow = m0 + r0 + j;
     const int r_row = grow / per_roll;
     const int rem = grow - r_row * per_roll;
     const int i_row = rem / p.G;
     const int qhead = kvh * p.G + (rem - i_row * p.G);
     const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
+    // the splits' weights l_s 2^(m_s - M) for row j, while the slices are in
+    // flight; every load is issued unconditionally (indices clamped to the S
+    // splits, the surplus weighted 0) so that none waits for another
+    float2 ml[kAttnMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) ml[s2] = recv_ml[min(s2, S - 1) * rpc + j];
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+      if (s2 < S && ml[s2].y > 0.f) M = fmaxf(M, ml[s2].x);
+    float Ls = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+      ml[s2].y = s2 < S && ml[s2].y > 0.f ? ml[s2].y * fast_exp2(ml[s2].x - M) : 0.f;
+      Ls += ml[s2].y;
+    }
+    const float inv = Ls > 0.f ? fast_rcp(Ls) : 0.f;
+    if (it == t && !mbar_wait(&bars[MERGE_O], 0, abort_flag, ds)) return;
+    uint4 x[kAttnMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) x[s2] = recv_o[(min(s2, S - 1) * kCh + ch) * rpc + j];
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+      const float w = ml[s2].y * inv;
+      const uint32_t xw[4] = {x[s2].x, x[s2].y, x[s2].z, x[s2].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a, b;
+        bf16x2_unpack(xw[e], a, b);
+        acc[2 * e] = fmaf(w, a, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, b, acc[2 * e + 1]);
+      }
+    }
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 8) =
         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                    pack_bf16x2(acc[6], acc[7]));
-    if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] = lse_row[j];
+    if (ch == 0 && p.lse)
+      p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
+          Ls > 0.f ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
   }
 }
 
@@ -403,9 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // parameters and (prefix_early) cached prefix rows; from here on this thread
   // reads or writes global memory that the previous kernel in the stream may
   // still be producing.
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, TMEM allocated
+  tc_fence_after();
   pdl_wait();
   if (threadIdx.x == 0) {
-    // the first loads leave before the rest of the CTA is set up
+    // the first loads leave as soon as this thread's wait returns
     if (nt > 0) {
       if (p.q_tma) {
         mbar_arrive_expect_tx(&bars[QFULL], L::kQBytes);
@@ -416,9 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_initial(false);
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   pdl_trigger();  // the next kernel may start its own set-up on free SMs
   const uint32_t tmem = misc[0];
   // softmax state of this thread's packed row (softmax warps), kept for the merge
