@@ -297,8 +297,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       for (int e = 0; e < 4; ++e) {
         float a, b;
         bf16x2_unpack(xw[e], a, b);
-        acc[2 * e] = fmaf(w, a, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(w, b, acc[2 * e + 1]);
+        fma2(acc[2 * e], acc[2 * e + 1], w, w, a, b, acc[2 * e], acc[2 * e + 1]);
       }
     }
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + ch * 8) =
@@ -592,12 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < BN / 2; ++j)
               if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
           }
+          // eight independent chains of three-input maxima
           float m8[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) m8[q] = sv[q];
 #pragma unroll
-          for (int j = 8; j < BN / 2; ++j) m8[j & 7] = fmaxf(m8[j & 7], sv[j]);
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int j = 8; j < BN / 2; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], sv[j], sv[j + 1]);
+          mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
         }
       }
       xch[(s * 2 + half) * BM + rl] = mx;
@@ -641,9 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a = fast_exp2(fmaf(sv[32 * c + 2 * j], p.scale_log2, mneg));
-            const float b = fast_exp2(fmaf(sv[32 * c + 2 * j + 1], p.scale_log2, mneg));
-            ls[j & 7] += a + b;
+            float xa, xb;
+            fma2(xa, xb, sv[32 * c + 2 * j], sv[32 * c + 2 * j + 1], p.scale_log2, p.scale_log2, mneg, mneg);
+            const float a = fast_exp2(xa);
+            const float b = fast_exp2(xb);
+            add2(ls[2 * (j & 3)], ls[2 * (j & 3) + 1], a, b);
             pk[j] = pack_bf16x2(a, b);
           }
           tmem_st16(lane_base + s * BN + c0 + 16 * c, pk);

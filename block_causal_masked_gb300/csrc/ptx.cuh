@@ -126,6 +126,39 @@ __device__ __forceinline__ float fast_rcp(float x) {
   return y;
 }
 
+// Maximum of three (PTX max.f32 with three sources; like fmaxf, a NaN source
+// is ignored).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Paired fp32 arithmetic (PTX .f32x2): two lanes of work per instruction, each
+// lane rounded as its single-precision counterpart (fma.rn / add.rn).
+// (d0, d1) = (a0 b0 + c0, a1 b1 + c1)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 // Programmatic dependent launch.  wait: this thread's global reads and writes
 // may begin (the preceding grid has completed and its writes are visible);
 // launch_dependents: the next grid in the stream may start being scheduled.
