@@ -119,14 +119,47 @@ struct AttnPlan {
   size_t ws_bytes;
 };
 
-// Widest split count (<= 16, <= the tile count) that keeps `groups` clusters
-// of it resident at once, one CTA per SM.
-int one_wave_splits(long long groups, long long max_tiles) {
-  long long s = kPlanSms / groups;
-  if (s > max_tiles) s = max_tiles;
-  if (s > kAttnMaxSplits) s = kAttnMaxSplits;
-  while (s > 1 && groups > attn_resident_clusters(static_cast<int>(s))) --s;
-  return s < 1 ? 1 : static_cast<int>(s);
+// KV split count for a launch of `groups` clusters (one per (row tile, KV
+// head)) whose K/V lists hold up to T tiles of head dim D.  Among the S whose
+// CTAs fit the SMs and whose clusters are all resident at once (one wave), the
+// cheapest by a small model in units of one tile's softmax period, fitted to
+// split sweeps of the workloads' shapes on GB300 (the widest on ties):
+//   * ceil(T / S) tiles on the longest split;
+//   * 1.5 for the cluster merge itself (S > 1), plus 0.7 for each extra pass
+//     of its 256 threads over the r(S) rows x D / 8 chunks an owner merges;
+//   * 0.3 when the split holding the last tile (the active block's diagonal
+//     tile, the slowest kind) is one of the longest;
+//   * 0.3 x the fraction of the next launch's clusters that cannot be resident
+//     beside this launch's (those cannot start their set-up early).
+int choose_splits(long long groups, long long T, int D) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int S = 1; S <= kAttnMaxSplits; ++S) {
+    if (S > 1 && (groups * S > kPlanSms || groups > attn_resident_clusters(S))) continue;
+    const long long c = (T + S - 1) / S;
+    double cost = static_cast<double>(c);
+    if (S > 1) {
+      const long long items = static_cast<long long>(attn_merge_rows(S)) * (D / 8);
+      cost += 1.5 + 0.7 * static_cast<double>((items + 255) / 256 - 1);
+      // the split of tile T - 1 under the ceil boundaries lo(s) = ceil(s T / S)
+      long long lo_last = 0;
+      for (int sp = S - 1; sp >= 0; --sp) {
+        const long long lo = (sp * T + S - 1) / S;
+        if (lo <= T - 1) {
+          lo_last = lo;
+          break;
+        }
+      }
+      if (c >= 2 && T - lo_last == c) cost += 0.3;
+      const long long blocked = 2 * groups - attn_resident_clusters(S);
+      if (blocked > 0) cost += 0.3 * static_cast<double>(blocked < groups ? blocked : groups) / groups;
+    }
+    if (cost <= best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
 }
 
 bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
@@ -159,15 +192,14 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   pl->part[0] = {0, pl->m_tiles, d.num_splits};
   if (d.num_splits == 0) {
     // spread the KV range of every (row tile, KV head) over the SMs as a cluster
-    // of up to 16 CTAs, at least one tile each, and keep every cluster of the
-    // launch resident at once (one wave): the widest split count whose
-    // clusters all fit
+    // of up to 16 CTAs, every cluster of the launch resident at once (one
+    // wave), the split count chosen by choose_splits
     const long long groups = static_cast<long long>(pl->m_tiles) * d.Hkv;
-    pl->part[0].splits = one_wave_splits(groups, max_tiles);
+    pl->part[0].splits = choose_splits(groups, max_tiles, d.D);
     const long long waves = groups / kPlanSms;
     const int bulk = static_cast<int>(waves * kPlanSms / d.Hkv);  // whole waves of row tiles
     if (waves > 0 && bulk > 0 && bulk < pl->m_tiles) {
-      const int tail_splits = one_wave_splits(static_cast<long long>(pl->m_tiles - bulk) * d.Hkv, max_tiles);
+      const int tail_splits = choose_splits(static_cast<long long>(pl->m_tiles - bulk) * d.Hkv, max_tiles, d.D);
       if (tail_splits > 1) {
         pl->n_parts = 2;
         pl->part[0] = {0, bulk, 1};
