@@ -558,31 +558,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp_active) {
           tmem_ld64(lane_base + s * BN + c0, sv);
           if constexpr (STREAM) {
-            // key j is visible iff its re-based position is at most the query's;
-            // the positions of this half of the tile are read 16 bytes at a time,
-            // 32 keys per batch with every load issued before the first is used
+            // key j is visible iff its re-based position is at most the query's.
+            // The range of the positions of this half tile (one 8-byte load per
+            // lane, warp shuffles) settles most rows at once: every key visible
+            // (nothing to mask) or none (the whole half masked); only when some
+            // row's position falls inside the range are the keys compared one
+            // by one, their positions read 16 bytes at a time
             const int kb = te.key0 + c0;
             const long long lim_q = static_cast<long long>(qpos_row) + p.kdelta;  // stored positions <= lim_q
+            int kp_lo, kp_hi;
+            if (p.kpos == nullptr) {
+              kp_lo = kb;
+              kp_hi = min(kb + BN / 2, p.C) - 1;
+            } else {
+              kp_lo = INT_MAX;
+              kp_hi = INT_MIN;
+              const int k2 = kb + 2 * lane;
+              if (k2 + 1 < p.C) {
+                const int2 kv = __ldg(reinterpret_cast<const int2*>(p.kpos + k2));
+                kp_lo = min(kv.x, kv.y);
+                kp_hi = max(kv.x, kv.y);
+              } else if (k2 < p.C) {
+                kp_lo = kp_hi = __ldg(p.kpos + k2);
+              }
 #pragma unroll
-            for (int b = 0; b < BN / 64; ++b) {
-              const int k0 = kb + 32 * b;
-              if (p.kpos != nullptr && k0 + 32 <= p.C) {
-                int4 kp4[8];
+              for (int o = 16; o > 0; o >>= 1) {
+                kp_lo = min(kp_lo, __shfl_xor_sync(0xffffffffu, kp_lo, o));
+                kp_hi = max(kp_hi, __shfl_xor_sync(0xffffffffu, kp_hi, o));
+              }
+            }
+            const bool all_vis = kb + BN / 2 <= p.C && static_cast<long long>(kp_hi) <= lim_q;
+            const bool none_vis = static_cast<long long>(kp_lo) > lim_q;
+            if (__all_sync(0xffffffffu, none_vis)) {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) kp4[j4] = __ldg(reinterpret_cast<const int4*>(p.kpos + k0) + j4);
+              for (int j = 0; j < BN / 2; ++j) sv[j] = -INFINITY;
+            } else if (!__all_sync(0xffffffffu, all_vis)) {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                  if (kp4[j4].x > lim_q) sv[32 * b + 4 * j4 + 0] = -INFINITY;
-                  if (kp4[j4].y > lim_q) sv[32 * b + 4 * j4 + 1] = -INFINITY;
-                  if (kp4[j4].z > lim_q) sv[32 * b + 4 * j4 + 2] = -INFINITY;
-                  if (kp4[j4].w > lim_q) sv[32 * b + 4 * j4 + 3] = -INFINITY;
-                }
-              } else {
+              for (int b = 0; b < BN / 64; ++b) {
+                const int k0 = kb + 32 * b;
+                if (p.kpos != nullptr && k0 + 32 <= p.C) {
+                  int4 kp4[8];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  const int key = k0 + j;
-                  const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) : INT_MAX;
-                  if (key >= p.C || kp > lim_q) sv[32 * b + j] = -INFINITY;
+                  for (int j4 = 0; j4 < 8; ++j4) kp4[j4] = __ldg(reinterpret_cast<const int4*>(p.kpos + k0) + j4);
+#pragma unroll
+                  for (int j4 = 0; j4 < 8; ++j4) {
+                    if (kp4[j4].x > lim_q) sv[32 * b + 4 * j4 + 0] = -INFINITY;
+                    if (kp4[j4].y > lim_q) sv[32 * b + 4 * j4 + 1] = -INFINITY;
+                    if (kp4[j4].z > lim_q) sv[32 * b + 4 * j4 + 2] = -INFINITY;
+                    if (kp4[j4].w > lim_q) sv[32 * b + 4 * j4 + 3] = -INFINITY;
+                  }
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) {
+                    const int key = k0 + j;
+                    const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) : INT_MAX;
+                    if (key >= p.C || kp > lim_q) sv[32 * b + j] = -INFINITY;
+                  }
                 }
               }
             }
