@@ -549,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[BN / 2];
       float mx = -INFINITY;
       int nv = 0;
+      bool dead = false;  // streaming mask: no row of this warp sees a key of this half tile
       if (ok) {
         tc_fence_after();
         const TileEntry te = tile_at(p, tr, t);
@@ -556,7 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid) lim = 0;
         nv = max(0, min(BN, lim - te.key0));
         if (warp_active) {
-          tmem_ld64(lane_base + s * BN + c0, sv);
           if constexpr (STREAM) {
             // key j is visible iff its re-based position is at most the query's.
             // The range of the positions of this half tile (one 8-byte load per
@@ -589,10 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool all_vis = kb + BN / 2 <= p.C && static_cast<long long>(kp_hi) <= lim_q;
             const bool none_vis = static_cast<long long>(kp_lo) > lim_q;
-            if (__all_sync(0xffffffffu, none_vis)) {
-#pragma unroll
-              for (int j = 0; j < BN / 2; ++j) sv[j] = -INFINITY;
-            } else if (!__all_sync(0xffffffffu, all_vis)) {
+            dead = __all_sync(0xffffffffu, none_vis);  // S is then not even loaded
+            if (!dead) tmem_ld64(lane_base + s * BN + c0, sv);
+            if (!dead && !__all_sync(0xffffffffu, all_vis)) {
 #pragma unroll
               for (int b = 0; b < BN / 64; ++b) {
                 const int k0 = kb + 32 * b;
@@ -617,18 +616,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-          } else if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
+          } else {
+            tmem_ld64(lane_base + s * BN + c0, sv);
+            if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
 #pragma unroll
-            for (int j = 0; j < BN / 2; ++j)
-              if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+              for (int j = 0; j < BN / 2; ++j)
+                if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+            }
           }
-          // eight independent chains of three-input maxima
-          float m8[8];
+          if (!dead) {
+            // eight independent chains of three-input maxima
+            float m8[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+            for (int q = 0; q < 8; ++q) m8[q] = sv[q];
 #pragma unroll
-          for (int j = 8; j < BN / 2; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], sv[j], sv[j + 1]);
-          mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+            for (int j = 8; j < BN / 2; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], sv[j], sv[j + 1]);
+            mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+          }
         }
       }
       xch[(s * 2 + half) * BM + rl] = mx;
@@ -663,7 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P of this tile, rounded to bf16, goes into the first half of this
       // half's S columns (S buffer s), while the previous tile's P.V -- which
       // reads the other buffer -- is still running on the tensor pipe
-      if (warp_active) {
+      if (warp_active && dead) {
+        // the half tile is hidden from every row of this warp: P = 0
+        uint32_t zero[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) zero[j] = 0u;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) tmem_st16(lane_base + s * BN + c0 + 16 * c, zero);
+        tmem_wait_st();
+      } else if (warp_active) {
         // masked entries are -inf; a row that has seen no key yet keeps m_run = -inf
         const float mneg = m_run == -INFINITY ? 0.f : -m_run;
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
