@@ -143,3 +143,35 @@ def test_streaming_mask_argument_errors_on_host():
     assert bd.lib().bd_block_causal_attn(a, None) == 2
     a = _attn(kv_stride=99, block_size=0, q_pos=FAKE)
     assert bd.lib().bd_block_causal_attn(a, None) == 1
+
+
+def _planned_splits(**kw):
+    """The KV split count the planner picks, read back from the workspace size
+    (Hkv * row tiles * S * S owner slices of r(S) rows of D bf16 values; none for
+    one split)."""
+    a = _attn(num_splits=0, **kw)
+    ws = bd.lib().bd_attn_workspace_size(a)
+    rows = a.n_q * (a.Hq // a.Hkv)
+    m_tiles = (rows + 127) // 128
+    if ws == 0:
+        return 1
+    for s in range(2, 17):
+        r = ((128 + s - 1) // s + 1) & ~1
+        if ws == a.Hkv * m_tiles * s * s * r * 2 * a.D:
+            return s
+    raise AssertionError(f"unexpected workspace size {ws}")
+
+
+@pytest.mark.parametrize("shape,want", [
+    # Fast-dDrive decode layer: 26 tiles over 6 clusters -> 16 (the diagonal split among the short ones)
+    (dict(C=3124, n_q=33, Hq=16, Hkv=2, kv_stride=3157, block_size=33), 16),
+    # Fast-dVLA window: 6 tiles -> 12 (one merge pass of the 256 threads, not two as at 6)
+    (dict(C=614, n_q=21, Hq=16, Hkv=2, kv_stride=635, block_size=7), 12),
+    # WAM decode, 8 KV heads: 18 tiles over 8 clusters -> 10 (16 would need two waves)
+    (dict(C=2176, n_q=1, Hq=16, Hkv=8, kv_stride=2177, block_size=1), 10),
+    (dict(C=2176, n_q=32, Hq=16, Hkv=8, kv_stride=2208, block_size=32), 10),
+    # a single tile: no split
+    (dict(C=100, n_q=8, Hq=4, Hkv=2, kv_stride=200, block_size=8), 1),
+])
+def test_planner_split_choices(shape, want):
+    assert _planned_splits(**shape) == want
