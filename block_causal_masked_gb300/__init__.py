@@ -43,7 +43,8 @@ class bd_attn_args(ct.Structure):
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("kv_stride", ct.c_int32), ("sm_scale", ct.c_float), ("rope", bd_rope),
                 ("num_splits", ct.c_int32), ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t),
-                ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32), ("q_pos", ct.c_void_p)]
+                ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32), ("q_pos", ct.c_void_p),
+                ("wait_limit_ns", ct.c_uint64)]
 
 
 class bd_fork_args(ct.Structure):
@@ -54,7 +55,7 @@ class bd_fork_args(ct.Structure):
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("sm_scale", ct.c_float), ("rope", bd_rope), ("num_splits", ct.c_int32),
                 ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
-                ("prefix_ready", ct.c_int32)]
+                ("prefix_ready", ct.c_int32), ("wait_limit_ns", ct.c_uint64)]
 
 
 class bd_stream_insert_args(ct.Structure):
@@ -73,7 +74,8 @@ class bd_unmask_args(ct.Structure):
                 ("add_num", ct.c_int32), ("add_den", ct.c_int32), ("act_num", ct.c_int32), ("act_den", ct.c_int32),
                 ("commit", ct.c_void_p), ("n_committed", ct.c_void_p), ("status", ct.c_void_p),
                 ("pred", ct.c_void_p), ("conf", ct.c_void_p), ("lse", ct.c_void_p), ("write_draft", ct.c_int32),
-                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
+                ("wait_limit_ns", ct.c_uint64)]
 
 
 class bd_verify_args(ct.Structure):
@@ -81,7 +83,8 @@ class bd_verify_args(ct.Structure):
                 ("ar_logits", ct.c_void_p), ("logits_dtype", ct.c_int32), ("logits_ld", ct.c_int64),
                 ("n_rows", ct.c_int32), ("V", ct.c_int32), ("noise", ct.c_void_p), ("temperature", ct.c_float),
                 ("accepted_len", ct.c_void_p), ("bonus", ct.c_void_p), ("bonus_pos", ct.c_void_p),
-                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p)]
+                ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
+                ("wait_limit_ns", ct.c_uint64)]
 
 
 _lib = None
@@ -179,7 +182,8 @@ def _bs(block_start):
 
 def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0, o=None, lse=None,
                          sm_scale: float = 0.0, rope=None, num_splits: int = 0, workspace=None,
-                         dev_status=None, stream=None, prefix_ready: bool = False, q_pos=None):
+                         dev_status=None, stream=None, prefix_ready: bool = False, q_pos=None,
+                         wait_limit_ns: int = 0):
     """Block-causal attention of the active positions.  q [n_q, Hq, D] bf16;
     k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after).
     With q_pos (int32 [n_q]) the streaming mask instead: queries over rows
@@ -208,13 +212,15 @@ def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0,
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    a.wait_limit_ns = int(wait_limit_ns)
     _check("bd_block_causal_attn", lib().bd_block_causal_attn(a, _stream(stream)))
     return o, lse
 
 
 def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: int, block_start=None,
                      block_size: int = 0, o=None, lse=None, sm_scale: float = 0.0, rope=None, num_splits: int = 0,
-                     workspace=None, dev_status=None, stream=None, prefix_ready: bool = False):
+                     workspace=None, dev_status=None, stream=None, prefix_ready: bool = False,
+                     wait_limit_ns: int = 0):
     """N rollouts over one shared prefix.  q [N, n_q, Hq, D]; prefix_k/v [Hkv, prefix_stride, D];
     priv_k/v [N, Hkv, priv_stride, D].  Returns (o [N, n_q, Hq, D], lse [N, Hq, n_q])."""
     N, n_q, Hq, D = q.shape
@@ -241,6 +247,7 @@ def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: in
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
     a.prefix_ready = 1 if prefix_ready else 0
+    a.wait_limit_ns = int(wait_limit_ns)
     _check("bd_fork_rollouts", lib().bd_fork_rollouts(a, _stream(stream)))
     return o, lse
 
@@ -249,7 +256,7 @@ def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: f
                    min_frac=(1, 4), k_fixed: int = 0, add_thr=(1, 2), act_thr=(17, 20), write_draft=False,
                    commit=None,
                    n_committed=None, status=None, pred=None, conf=None, lse=None, workspace=None,
-                   dev_status=None, stream=None):
+                   dev_status=None, stream=None, wait_limit_ns: int = 0):
     """One unmask/commit step; updates ``state`` and ``tokens`` in place.
     Returns dict(commit, n_committed, status, pred, conf, lse)."""
     R, V = logits.shape
@@ -283,12 +290,13 @@ def bd_unmask_step(logits, logit_row, block_start, state, tokens, *, tau_full: f
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    a.wait_limit_ns = int(wait_limit_ns)
     _check("bd_unmask_step", lib().bd_unmask_step(a, _stream(stream)))
     return dict(commit=commit, n_committed=n_committed, status=status, pred=pred, conf=conf, lse=lse)
 
 
 def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.0, accepted_len=None, bonus=None,
-                   bonus_pos=None, workspace=None, dev_status=None, stream=None):
+                   bonus_pos=None, workspace=None, dev_status=None, stream=None, wait_limit_ns: int = 0):
     """Scaffold-speculative verify; updates ``tokens``/``state`` [n_seq, L] in place.
     ar_logits [n_seq, n_rows, V]; noise fp32 of the same shape or None.
     Returns (accepted_len, bonus, bonus_pos), int32 [n_seq] each."""
@@ -319,6 +327,7 @@ def bd_spec_verify(tokens, state, ar_logits, noise=None, temperature: float = 1.
     a.workspace = None if ws is None else ws.data_ptr()
     a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     a.dev_status = None if dev_status is None else dev_status.data_ptr()
+    a.wait_limit_ns = int(wait_limit_ns)
     _check("bd_spec_verify", lib().bd_spec_verify(a, _stream(stream)))
     return accepted_len, bonus, bonus_pos
 

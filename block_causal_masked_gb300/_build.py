@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbd.so")
 SOURCES = ["api.cu", "attn.cu", "vocab.cu", "stream.cu"]
-HEADERS = [os.path.join(ROOT, "include", "bd.h"), os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "launch.h")]
+HEADERS = [os.path.join(ROOT, "include", "bd.h"), os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "launch.h"),
+           os.path.join(CSRC, "rope_table.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

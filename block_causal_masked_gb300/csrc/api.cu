@@ -24,6 +24,9 @@ constexpr int kPlanSms = 152;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Limit of a kernel's pipeline waits: the call's, or 1 s.
+unsigned long long wait_limit(uint64_t ns) { return ns ? ns : 1000ull * 1000ull * 1000ull; }
+
 // ------------------------------------------------------------------ device checks
 
 std::mutex g_mu;
@@ -101,6 +104,7 @@ struct AttnDesc {
   int32_t* ds;
   int prefix_ready;
   const int32_t* q_pos;  // streaming mask (plain attention only)
+  uint64_t wait_ns;
 };
 
 // One call runs as one launch, or as two when its (row tile, KV head) groups
@@ -259,6 +263,7 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.q_pos = d.q_pos;
   p.kpos = d.rope.k_pos;
   p.kdelta = d.rope.delta;
+  p.wait_ns = wait_limit(d.wait_ns);
   const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
   p.scale_log2 = scale * 1.4426950408889634f;
   // RoPE: the pre-RoPE prefix keys are rotated once for the whole call into
@@ -283,7 +288,11 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
       double x = f / two_pi;
       x -= std::floor(x);
       rp.turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
+      rp.freq[i] = f;
     }
+    const double c = std::ldexp(two_pi, -64);
+    rp.two_pi_64[0] = static_cast<float>(c);
+    rp.two_pi_64[1] = static_cast<float>(c - static_cast<double>(rp.two_pi_64[0]));
     prefix_k = rp.out;
     prefix_k_stride = d.C;
   }
@@ -355,6 +364,7 @@ AttnDesc desc_of(const bd_attn_args* a) {
   d.ds = a->dev_status;
   d.prefix_ready = a->prefix_ready;
   d.q_pos = a->q_pos;
+  d.wait_ns = a->wait_limit_ns;
   if (d.q_pos) {  // no active rows are read: point the private map at the cache itself
     d.rk = a->k;
     d.rv = a->v;
@@ -391,6 +401,7 @@ AttnDesc desc_of(const bd_fork_args* a) {
   d.ws_bytes = a->workspace_bytes;
   d.ds = a->dev_status;
   d.prefix_ready = a->prefix_ready;
+  d.wait_ns = a->wait_limit_ns;
   return d;
 }
 
@@ -408,7 +419,7 @@ bd_status plan_unmask(const bd_unmask_args* a, int* chunks, int* elems, size_t* 
   if (a->R > kMaxVerifyRows) return BD_ERR_UNSUPPORTED;  // one CTA row per logits row (grid y)
   const int rows = a->R;
   vocab_split(rows, a->V, kPlanSms, chunks, elems);
-  *ws = unmask_workspace_bytes(a->R, *chunks);
+  *ws = unmask_workspace_bytes(a->R);
   return BD_OK;
 }
 
@@ -422,7 +433,7 @@ bd_status plan_verify(const bd_verify_args* a, int* chunks, int* elems, size_t* 
   if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
   if (a->noise && !(a->temperature > 0.f)) return BD_ERR_INVALID_ARG;
   vocab_split(a->n_seq * a->n_rows, a->V, kPlanSms, chunks, elems);
-  *ws = verify_workspace_bytes(a->n_seq, a->n_rows, *chunks);
+  *ws = verify_workspace_bytes(a->n_seq, a->n_rows);
   return BD_OK;
 }
 
@@ -492,7 +503,13 @@ size_t bd_unmask_workspace_size(const bd_unmask_args* a) {
   return plan_unmask(a, &c, &e, &ws) == BD_OK ? ws : 0;
 }
 
-bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Every host-side check of an unmask call (shapes, pointers, alignment,
+// workspace, device), then its kernel parameters; nothing is enqueued.
+bd_status prepare_unmask(const bd_unmask_args* a, UnmaskParams* out) {
   int chunks, elems;
   size_t ws;
   bd_status st = plan_unmask(a, &chunks, &elems, &ws);
@@ -503,7 +520,7 @@ bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
   if (!aligned(a->logits, 16)) return BD_ERR_UNSUPPORTED;
   if (!a->workspace || a->workspace_bytes < ws || !aligned(a->workspace, 256)) return BD_ERR_WORKSPACE;
   if ((st = check_device()) != BD_OK) return st;
-  UnmaskParams p;
+  UnmaskParams& p = *out;
   std::memset(&p, 0, sizeof(p));
   p.logits = a->logits;
   p.dtype = a->logits_dtype;
@@ -533,11 +550,23 @@ bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
   p.lse = a->lse;
   p.write_draft = a->write_draft;
   p.dev_status = a->dev_status;
+  p.wait_ns = wait_limit(a->wait_limit_ns);
   char* w = static_cast<char*>(a->workspace);
   p.grid_ticket = reinterpret_cast<unsigned*>(w);
-  p.chunk_part = reinterpret_cast<float4*>(w + unmask_counter_bytes());
+  p.row_res = reinterpret_cast<float4*>(w + unmask_counter_bytes());
   p.chunks = chunks;
   p.chunk_elems = elems;
+  return BD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bd_status bd_unmask_step(const bd_unmask_args* a, void* stream) {
+  UnmaskParams p;
+  const bd_status st = prepare_unmask(a, &p);
+  if (st != BD_OK) return st;
   return launch_unmask(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
@@ -574,9 +603,10 @@ bd_status bd_spec_verify(const bd_verify_args* a, void* stream) {
   p.bonus = a->bonus;
   p.bonus_pos = a->bonus_pos;
   p.dev_status = a->dev_status;
+  p.wait_ns = wait_limit(a->wait_limit_ns);
   char* w = static_cast<char*>(a->workspace);
   p.seq_ticket = reinterpret_cast<unsigned*>(w);
-  p.chunk_part = reinterpret_cast<float4*>(w + verify_counter_bytes());
+  p.row_res = reinterpret_cast<float4*>(w + verify_counter_bytes());
   p.chunks = chunks;
   p.chunk_elems = elems;
   return launch_verify(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
@@ -645,11 +675,14 @@ extern "C" bd_status bd_unmask_step_noalloc(const bd_unmask_args* a, void* strea
     }
     scratch = g_scratch_addr[dev];
   }
-  // The counter words must start at zero; a call cut short may have left them set.
-  if (cudaMemsetAsync(scratch, 0, unmask_counter_bytes(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return BD_ERR_CUDA;
   bd_unmask_args b = *a;
   b.workspace = scratch;
   b.workspace_bytes = BD_UNMASK_NOALLOC_SCRATCH_BYTES;
-  return bd_unmask_step(&b, stream);
+  // every argument is checked before anything is enqueued
+  UnmaskParams p;
+  if ((st = prepare_unmask(&b, &p)) != BD_OK) return st;
+  // The counter words must start at zero; a call cut short may have left them set.
+  if (cudaMemsetAsync(scratch, 0, unmask_counter_bytes(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BD_ERR_CUDA;
+  return launch_unmask(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

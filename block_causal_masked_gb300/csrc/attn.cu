@@ -29,8 +29,9 @@
 // With RoPE (FlashDrive tutorial, "流式推理"), the cached prefix keys stay
 // pre-RoPE in memory and a small kernel of the same call rotates them at
 // k_pos - delta into a bf16 copy that every row tile then reads -- once per
-// call instead of once per row tile; the angle is reduced exactly in 0.64
-// fixed-point turns.
+// call instead of once per row tile; each rotated element is the bf16 rounding
+// of the rotation formed in float64 (an fp32 rotation with an error bound,
+// recomputed in float64 where that bound leaves the rounding open).
 // Every mbarrier wait is bounded (ptx.cuh); the only cross-CTA waits are the
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
@@ -41,6 +42,7 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "rope_table.h"
 
 namespace bd {
 namespace {
@@ -133,18 +135,206 @@ __device__ __forceinline__ void bf16x2_unpack(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xffff0000u);
 }
 
-// cos/sin of pos * freq_d with freq_d / (2 pi) given as a 0.64 fixed-point
-// fraction: the product modulo 2^64 is the fractional turn, so the reduction
-// to [-pi, pi) is exact up to the 2^-32 truncation of its top word; the turn
-// becomes an fp32 angle (error below 1e-7 rad) and sin / cos are the accurate
-// single-precision functions, so a rotated key is within ~1e-6 of its exact
-// value before the bf16 rounding.  (Scaling the turn in double measured 6 us
-// slower per call: fp64 is slow on this part.)
+// ------------------------------------------------------------------ RoPE rounding
+//
+// The rotated key is an operand of the bf16 Q.K^T product, so it is rounded to
+// bf16 -- and it must be the rounding of the rotation the definition gives:
+// y = a cos(phi) - b sin(phi) (and b cos(phi) + a sin(phi)) at phi = pos * f_d,
+// f_d = theta^(-2d/D), formed in float64 like the definition's arithmetic.  The
+// fast path rotates in fp32 with an error bound E on |y_fp32 - y|; when the
+// interval [y_fp32 - E, y_fp32 + E] holds no bf16 rounding midpoint, every
+// value in it -- y included -- rounds to the same bf16, which is taken.  The
+// few pairs whose interval straddles a midpoint (about 1.6e-3 of them for
+// N(0, 1) keys) are rotated again from the float64 angle with float-float
+// sin / cos (within 2^-46 (|a| + |b|)); only where even that leaves the
+// rounding open is the float64 rotation itself computed.
+//
+// Error bound of the fp32 rotation (per element, |a|, |b| the bf16 inputs):
+//   angle: the fractional turn pos * f_d / (2 pi) is exact modulo 2^64 in 0.64
+//     fixed point; the turn constant carries at most |pos| 2^-51 rad against
+//     the float64 product pos * f_d, which itself is rounded by |pos| 2^-53;
+//   sin / cos: the top 24 bits of the turn go to sincospif exactly (its
+//     documented error is 1 ulp, below 2^-24 for results of magnitude < 1;
+//     2^-23 is assumed), the lower 40 bits (< 3.7e-7 rad) are added by the
+//     first-order angle-sum correction (second-order term < 7e-14, correction
+//     rounded within 2^-24);
+//   so |cos - cos(phi)|, |sin - sin(phi)| <= delta = 3 * 2^-24 + |pos| 2^-50;
+//   the rotation fmaf(a, c, -(b s)) adds |b s| 2^-24 + |y| 2^-24.
+// E = (|a| + |b|) (delta + 2^-24) + |y| 2^-24, computed with a factor of
+// safety (the 2^-22 terms below).
+constexpr float kRopeSinCosErr = 3.0f * 0x1p-24f;
+
+// bf16 bits of the float64 value y, rounded to nearest even without double
+// rounding: the float64 -> fp32 step truncates and records in the last fp32
+// bit whether anything was dropped (round to odd), so the fp32 -> bf16
+// rounding sees every bit below the ones it keeps.
+__device__ __forceinline__ uint32_t bf16_bits_rne(double y) {
+  const float t = __double2float_rz(y);
+  uint32_t u = __float_as_uint(t);
+  if (static_cast<double>(t) != y) u |= 1u;
+  return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&h));
+}
+
+// Does every value within e of x round to the same bf16?
+__device__ __forceinline__ bool bf16_rounding_decided(float x, float e) {
+  return bf16_bits_rn(__fsub_rd(x, e)) == bf16_bits_rn(__fadd_ru(x, e));
+}
+
+// The rotated pair (a cos(phi) - b sin(phi), b cos(phi) + a sin(phi)) at
+// phi = pos * freq in float64, in the definition's order of operations (phi
+// rounded, each product rounded, then the difference / sum), each rounded to
+// bf16: low 16 bits the first, high 16 bits the second.  Kept out of line: it
+// runs only where the float-float rotation leaves the rounding open.
+static __device__ __noinline__ uint32_t rope_pair_f64(int pos, double freq, float a, float b) {
+  const double phi = __dmul_rn(static_cast<double>(pos), freq);
+  double sd, cd;
+  sincos(phi, &sd, &cd);
+  const double ad = a, bd = b;
+  const uint32_t ra = bf16_bits_rne(__dsub_rn(__dmul_rn(ad, cd), __dmul_rn(bd, sd)));
+  const uint32_t rb = bf16_bits_rne(__dadd_rn(__dmul_rn(bd, cd), __dmul_rn(ad, sd)));
+  return ra | (rb << 16);
+}
+
+// ---- second tier: the float64 angle, reduced exactly, and float-float sin / cos
+//
+// Float-float (hi + lo, two fp32 values) carries about 48 bits; float64 runs at
+// a small fraction of the fp32 rate on this part, so the second tier uses one
+// float64 instruction only -- the product phi = pos * f_d, rounded as the
+// definition rounds it -- and does the rest in integer and fp32 arithmetic.
+struct FF {
+  float hi, lo;
+};
+
+// a * b exactly as hi + lo (fma-based two-product).
+__device__ __forceinline__ FF ff_two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, fmaf(a, b, -p)};
+}
+
+// a + b exactly as hi + lo (two-sum).
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ FF ff_mul(FF x, FF y) {
+  FF p = ff_two_prod(x.hi, y.hi);
+  p.lo = fmaf(x.hi, y.lo, fmaf(x.lo, y.hi, p.lo));
+  return ff_two_sum(p.hi, p.lo);
+}
+
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+  FF s = ff_two_sum(x.hi, y.hi);
+  s.lo = __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo));
+  return ff_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ FF ff_neg(FF x) { return {-x.hi, -x.lo}; }
+
+// phi / (2 pi) mod 1 as a 0.64 fixed-point fraction (two's complement for a
+// negative phi), from the exact binary value of phi (m 2^(e - 1075)) and
+// 1 / (2 pi) to 128 bits: floor(2^128 / (2 pi)) = 0x28be60db9391054a_7f09d5f47d4d3770
+// (from pi by Machin's formula, 16 atan(1/5) - 4 atan(1/239), in integer
+// arithmetic).  Exact up to the truncation of that constant, below 2^-90 turn
+// for |phi| < 2^31.
+__device__ __forceinline__ unsigned long long turn_fraction(double phi) {
+  const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(phi));
+  const int ex = static_cast<int>((bits >> 52) & 0x7ffu);
+  if (ex == 0) return 0;  // zero (a subnormal angle is below 1e-307 turn)
+  const unsigned long long m = (bits & ((1ull << 52) - 1)) | (1ull << 52);
+  constexpr unsigned long long kRh = 0x28be60db9391054aull, kRl = 0x7f09d5f47d4d3770ull;
+  // m * R as 192 bits (p2, p1; the lowest limb is never needed)
+  const unsigned long long h0 = __umul64hi(m, kRl);
+  const unsigned long long l1 = m * kRh, h1 = __umul64hi(m, kRh);
+  const unsigned long long p1 = h0 + l1;
+  const unsigned long long p2 = h1 + (p1 < h0 ? 1ull : 0ull);
+  const int sh = 1139 - ex;  // frac(phi / 2 pi) 2^64 = (m R) >> sh, mod 2^64
+  unsigned long long f;
+  if (sh >= 192) f = 0;
+  else if (sh >= 128) f = p2 >> (sh - 128);
+  else if (sh > 64) f = (p1 >> (sh - 64)) | (p2 << (128 - sh));
+  else f = p1;  // sh >= 86 whenever |phi| < 2^31 (a 32-bit position times f_d <= 1)
+  return (bits >> 63) ? 0ull - f : f;
+}
+
+// The rotated pair of rope_pair_f64, from the same float64 angle phi =
+// pos * freq, with sin / cos in float-float: the turn fraction's top 8 bits
+// pick cos / sin(2 pi k / 256) from kRopeTurnTable (float-float, within
+// 2^-50), the remaining t < 2 pi / 256 rad goes through its Taylor
+// series (sin: t - t^3/6 + t^5/120, cos: 1 - t^2/2 + t^4/24 - t^6/720; the
+// first dropped terms are below 2^-49), and the angle sum combines them.
+// Every value is within 2^-46 (|a| + |b|) of the float64 rotation; when the
+// bf16 rounding is still open within that bound (an element within about one
+// fp32 ulp of a rounding midpoint), *decided is false and the caller falls
+// back to the float64 rotation.
+__device__ uint32_t rope_pair_ff(int pos, double freq, float a, float b, float c_hi, float c_lo, bool* decided) {
+  const unsigned long long f = turn_fraction(__dmul_rn(static_cast<double>(pos), freq));
+  const int k = static_cast<int>(f >> 56);
+  const unsigned long long r = f & ((1ull << 56) - 1);
+  // t = 2 pi r / 2^64 = r (c_hi + c_lo) in float-float
+  const float r_hi = static_cast<float>(static_cast<unsigned>(r >> 32)) * 0x1p32f;  // exact
+  const float r_lo = static_cast<float>(static_cast<unsigned>(r & 0xffffffffull));
+  FF t = ff_two_prod(r_hi, c_hi);
+  t.lo = fmaf(r_hi, c_lo, fmaf(r_lo, c_hi, t.lo));
+  t = ff_two_sum(t.hi, t.lo);
+  FF t2 = ff_two_prod(t.hi, t.hi);
+  t2.lo = fmaf(2.f * t.hi, t.lo, t2.lo);
+  FF t3 = ff_two_prod(t2.hi, t.hi);
+  t3.lo = fmaf(t2.hi, t.lo, fmaf(t2.lo, t.hi, t3.lo));
+  // t^3 / 6: quotient rounded, exact remainder
+  const float q = __fdiv_rn(t3.hi, 6.f);
+  const float q_lo = __fdiv_rn(__fadd_rn(fmaf(-q, 6.f, t3.hi), t3.lo), 6.f);
+  const float t4 = __fmul_rn(t2.hi, t2.hi);
+  FF sn = ff_two_sum(t.hi, -q);
+  sn.lo = __fadd_rn(sn.lo, __fsub_rn(t.lo, q_lo) + __fmul_rn(t4, t.hi) * (1.f / 120.f));
+  FF cs = ff_two_sum(1.f, -0.5f * t2.hi);
+  cs.lo = __fadd_rn(cs.lo, -0.5f * t2.lo + t4 * (1.f / 24.f) - __fmul_rn(t4, t2.hi) * (1.f / 720.f));
+  sn = ff_two_sum(sn.hi, sn.lo);
+  cs = ff_two_sum(cs.hi, cs.lo);
+  const float4 kt = __ldg(reinterpret_cast<const float4*>(kRopeTurnTable) + k);
+  const FF kc = {kt.x, kt.y};
+  const FF ks = {kt.z, kt.w};
+  const FF cphi = ff_add(ff_mul(kc, cs), ff_neg(ff_mul(ks, sn)));
+  const FF sphi = ff_add(ff_mul(ks, cs), ff_mul(kc, sn));
+  // y1 = a cos - b sin, y2 = b cos + a sin (a, b exact in fp32)
+  const FF y1 = ff_add(ff_mul({a, 0.f}, cphi), ff_neg(ff_mul({b, 0.f}, sphi)));
+  const FF y2 = ff_add(ff_mul({b, 0.f}, cphi), ff_mul({a, 0.f}, sphi));
+  const float e = (fabsf(a) + fabsf(b)) * 0x1p-44f;
+  uint32_t out = 0;
+  bool ok = true;
+  const FF ys[2] = {y1, y2};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    // [lo_end, hi_end] holds [y - e, y + e]
+    const float lo_end = __fadd_rd(ys[i].hi, __fsub_rd(ys[i].lo, e));
+    const float hi_end = __fadd_ru(ys[i].hi, __fadd_ru(ys[i].lo, e));
+    const uint32_t r0 = bf16_bits_rn(lo_end);
+    ok = ok && r0 == bf16_bits_rn(hi_end);
+    out |= r0 << (16 * i);
+  }
+  *decided = ok;
+  return out;
+}
+
+// cos / sin of 2 pi * (pos * turns mod 2^64) / 2^64 (the turn as a 0.64
+// fixed-point fraction) in fp32, within kRopeSinCosErr of the exact values.
 __device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long turns, float& c, float& s) {
-  const unsigned long long prod = static_cast<unsigned long long>(static_cast<long long>(pos)) * turns;
-  const int top = static_cast<int>(prod >> 32);
-  const float ang = static_cast<float>(top) * (6.283185307179586f / 4294967296.0f);
-  sincosf(ang, &s, &c);
+  const long long prod = static_cast<long long>(static_cast<unsigned long long>(static_cast<long long>(pos)) * turns);
+  // top 24 bits: half-turns in [-1, 1), exact in fp32
+  const float x_hi = static_cast<float>(static_cast<int>(prod >> 40)) * 0x1p-23f;
+  // lower 40 bits: the rest of the angle, below 2 pi 2^-24 rad
+  const float th_lo = static_cast<float>(static_cast<unsigned long long>(prod) & 0xffffffffffull) *
+                      (6.283185307179586f * 0x1p-64f);
+  float sh, ch;
+  sincospif(x_hi, &sh, &ch);
+  c = fmaf(-sh, th_lo, ch);
+  s = fmaf(ch, th_lo, sh);
 }
 
 // The K/V tiles of one CTA: the shared prefix tiles, then the private tiles of
@@ -284,7 +474,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       Ls += ml[s2].y;
     }
     const float inv = Ls > 0.f ? fast_rcp(Ls) : 0.f;
-    if (it == t && !mbar_wait(&bars[MERGE_O], 0, abort_flag, ds)) return;
+    if (it == t && !mbar_wait(&bars[MERGE_O], 0, abort_flag, ds, p.wait_ns)) return;
     uint4 x[kAttnMaxSplits];
 #pragma unroll
     for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) x[s2] = recv_o[(min(s2, S - 1) * kCh + ch) * rpc + j];
@@ -433,11 +623,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk = nt < 3 ? nt : 3, nv = nt < 2 ? nt : 2;  // tiles issued so far
       for (int t = 2; t < nt; ++t) {
         if (t + 1 < nt) {
-          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKStages], ((t + 1) / kKStages - 1) & 1, abort_flag, ds)) break;
+          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKStages], ((t + 1) / kKStages - 1) & 1, abort_flag, ds, p.wait_ns)) break;
           issue_tile(t + 1, false);
           nk = t + 2;
         }
-        if (!mbar_wait(&bars[VEMPTY + t % kVStages], (t / kVStages - 1) & 1, abort_flag, ds)) break;
+        if (!mbar_wait(&bars[VEMPTY + t % kVStages], (t / kVStages - 1) & 1, abort_flag, ds, p.wait_ns)) break;
         issue_tile(t, true);
         nv = t + 1;
       }
@@ -459,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ks = u % kKStages;
         // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
         // point by this thread, and executed in issue order -- has consumed
-        if (!mbar_wait(&bars[KFULL + ks], (u / kKStages) & 1, abort_flag, ds)) return false;
+        if (!mbar_wait(&bars[KFULL + ks], (u / kKStages) & 1, abort_flag, ds, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
 #pragma unroll
@@ -473,15 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[KEMPTY + ks]);  // K tile consumed: the producer may refill the stage
         return true;
       };
-      bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds);
+      bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds, p.wait_ns);
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
       }
       for (int t = 0; ok && t < nt; ++t) {
         if (t + 1 < nt && !issue_s(t + 1)) break;
-        if (!mbar_wait(&bars[PFULL + (t & 1)], (t >> 1) & 1, abort_flag, ds)) break;
-        if (!mbar_wait(&bars[VFULL + t % kVStages], (t / kVStages) & 1, abort_flag, ds)) break;
+        if (!mbar_wait(&bars[PFULL + (t & 1)], (t >> 1) & 1, abort_flag, ds, p.wait_ns)) break;
+        if (!mbar_wait(&bars[VFULL + t % kVStages], (t / kVStages) & 1, abort_flag, ds, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t va = smem_addr(smem + L::kV + (t % kVStages) * L::kKVBytes);
         const uint32_t pt = tmem + (t & 1) * BN;  // P(t), in the S buffer it was formed from
@@ -544,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // number of times (nt + 1), whatever the waits return.
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
-      if (ok) ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds));
+      if (ok) ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds, p.wait_ns));
       // this half of the S row in registers: one TMEM round trip, then S is free again
       float sv[BN / 2];
       float mx = -INFINITY;
@@ -652,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the previous tile's P.V to have finished first
       const bool rescale = warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f);
       if (rescale) {  // P.V(t - 1) must have finished updating O
-        ok = all_lanes(mbar_wait(&bars[ODONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag, ds));
+        ok = all_lanes(mbar_wait(&bars[ODONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag, ds, p.wait_ns));
         if (!ok) continue;
         tc_fence_after();
 #pragma unroll
@@ -701,14 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and tcgen05.mma runs in issue order -- only keeps this thread's view of
       // each ODONE barrier within one phase (no parity aliasing later).
       if (t >= 2) {
-        ok = all_lanes(mbar_wait(&bars[ODONE + (t & 1)], ((t - 2) >> 1) & 1, abort_flag, ds));
+        ok = all_lanes(mbar_wait(&bars[ODONE + (t & 1)], ((t - 2) >> 1) & 1, abort_flag, ds, p.wait_ns));
         if (!ok) continue;
       }
       tc_fence_before();
       mbar_arrive(&bars[PFULL + (t & 1)]);
     }
     if (ok && nt > 0) {  // the last P.V (and, in issue order, every earlier one)
-      ok = all_lanes(mbar_wait(&bars[ODONE + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag, ds));
+      ok = all_lanes(mbar_wait(&bars[ODONE + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag, ds, p.wait_ns));
       tc_fence_after();
     }
     have_o = ok && nt > 0;
@@ -755,15 +945,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool STREAM>
 cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
-  static bool configured = false;
+  static PerDeviceOnce configured;  // one per instantiation
   const int smem = attn_smem_bytes(D);
   auto kernel = attn_kernel<D, STREAM>;
-  if (!configured) {
+  cudaError_t ce = configured.run([&] {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return e;
+  });
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kThreads);
@@ -794,39 +984,102 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
 // a contiguous bf16 copy [Hkv, C, D] (FlashDrive tutorial, "流式推理": the cache
 // stays pre-RoPE; the operator applies the rotation at the re-based
 // positions).  One thread per (KV head, key, 8 rotation pairs): the pairs
-// (d, d + D/2) for d in [8 c, 8 c + 8).
+// (d, d + D/2) for d in [8 c, 8 c + 8).  Each rotated element is the bf16
+// rounding (to nearest even) of the rotation computed in float64; see the
+// error bound above.  The pairs whose rounding the fp32 rotation leaves open
+// are queued in shared memory and redone, one pair per lane of whole warps,
+// after the CTA's fast results are stored: from the float64 angle with
+// float-float sin / cos, and in float64 where that still leaves the rounding
+// open (float64 runs at a small fraction of the fp32 rate on this part).
+constexpr int kRopeThreads = 512;
+constexpr int kRopeQueue = 1024;  // queued pairs per CTA (a thread past it redoes its own)
+
+struct RopeRedo {
+  int pos;      // k_pos - delta
+  int d;        // frequency index
+  float a, b;   // the pair's pre-RoPE elements
+  uint32_t at;  // element offset of the first output in the rotated copy
+};
+
 template <int D>
-__global__ void __launch_bounds__(256) rope_prefix_kernel(const __grid_constant__ RopeParams p) {
+__global__ void __launch_bounds__(kRopeThreads) rope_prefix_kernel(const __grid_constant__ RopeParams p) {
   constexpr int kChunks = D / 16;  // 8-pair chunks of a key row
+  __shared__ RopeRedo queue[kRopeQueue];
+  __shared__ int n_queued;
+  if (threadIdx.x == 0) n_queued = 0;
   pdl_wait();
   pdl_trigger();
+  __syncthreads();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(p.Hkv) * p.C * kChunks;
-  if (i >= total) return;
-  const int c = static_cast<int>(i % kChunks);
-  const long long row = i / kChunks;  // kvh * C + key
-  const int key = static_cast<int>(row % p.C);
-  const int kvh = static_cast<int>(row / p.C);
-  const __nv_bfloat16* src =
-      static_cast<const __nv_bfloat16*>(p.k) + (static_cast<size_t>(kvh) * p.stride + key) * D;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * D;
-  const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
-  uint4 xa = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
-  uint4 xb = __ldg(reinterpret_cast<const uint4*>(src + c * 8 + D / 2));
-  uint32_t* wa = reinterpret_cast<uint32_t*>(&xa);
-  uint32_t* wb = reinterpret_cast<uint32_t*>(&xb);
+  __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(p.out);
+  if (i < total) {
+    const int c = static_cast<int>(i % kChunks);
+    const long long row = i / kChunks;  // kvh * C + key
+    const int key = static_cast<int>(row % p.C);
+    const int kvh = static_cast<int>(row / p.C);
+    const __nv_bfloat16* src =
+        static_cast<const __nv_bfloat16*>(p.k) + (static_cast<size_t>(kvh) * p.stride + key) * D;
+    __nv_bfloat16* dst = out + static_cast<size_t>(row) * D;
+    const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
+    const float delta = kRopeSinCosErr + 0x1p-24f + static_cast<float>(abs(pos)) * 0x1p-50f;
+    uint4 xa = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
+    uint4 xb = __ldg(reinterpret_cast<const uint4*>(src + c * 8 + D / 2));
+    const uint32_t* wa = reinterpret_cast<const uint32_t*>(&xa);
+    const uint32_t* wb = reinterpret_cast<const uint32_t*>(&xb);
+    float a[8], b[8], ya[8], yb[8];
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    float a0, a1, b0, b1, c0, s0, c1, s1;
-    bf16x2_unpack(wa[w], a0, a1);
-    bf16x2_unpack(wb[w], b0, b1);
-    rope_cos_sin(pos, p.turns[c * 8 + 2 * w], c0, s0);
-    rope_cos_sin(pos, p.turns[c * 8 + 2 * w + 1], c1, s1);
-    wa[w] = pack_bf16x2(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-    wb[w] = pack_bf16x2(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+    for (int w = 0; w < 4; ++w) {
+      bf16x2_unpack(wa[w], a[2 * w], a[2 * w + 1]);
+      bf16x2_unpack(wb[w], b[2 * w], b[2 * w + 1]);
+    }
+    unsigned redo = 0;  // pairs whose rounding the fp32 rotation does not settle
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float cs, sn;
+      rope_cos_sin(pos, p.turns[c * 8 + j], cs, sn);
+      ya[j] = fmaf(a[j], cs, -(b[j] * sn));
+      yb[j] = fmaf(b[j], cs, a[j] * sn);
+      const float e0 = (fabsf(a[j]) + fabsf(b[j])) * delta * (1.f + 0x1p-20f);
+      const float ea = fmaf(fabsf(ya[j]), 0x1p-22f, e0);
+      const float eb = fmaf(fabsf(yb[j]), 0x1p-22f, e0);
+      if (!bf16_rounding_decided(ya[j], ea) || !bf16_rounding_decided(yb[j], eb)) redo |= 1u << j;
+    }
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      oa[w] = pack_bf16x2(ya[2 * w], ya[2 * w + 1]);
+      ob[w] = pack_bf16x2(yb[2 * w], yb[2 * w + 1]);
+    }
+    *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(dst + c * 8 + D / 2) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    if (redo) {
+      const uint32_t at = static_cast<uint32_t>(row * D + c * 8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (!((redo >> j) & 1u)) continue;
+        const int q = atomicAdd(&n_queued, 1);
+        if (q < kRopeQueue) {
+          queue[q] = RopeRedo{pos, c * 8 + j, a[j], b[j], at + j};
+        } else {  // the queue is full (never with N(0, 1) keys): this thread redoes the pair itself
+          const uint32_t r = rope_pair_f64(pos, p.freq[c * 8 + j], a[j], b[j]);
+          reinterpret_cast<unsigned short*>(out)[at + j] = static_cast<unsigned short>(r & 0xffffu);
+          reinterpret_cast<unsigned short*>(out)[at + j + D / 2] = static_cast<unsigned short>(r >> 16);
+        }
+      }
+    }
   }
-  *reinterpret_cast<uint4*>(dst + c * 8) = xa;
-  *reinterpret_cast<uint4*>(dst + c * 8 + D / 2) = xb;
+  // the fast results above are stored before the redone elements overwrite them
+  __syncthreads();
+  const int n = min(n_queued, kRopeQueue);
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const RopeRedo it = queue[q];
+    bool decided;
+    uint32_t r = rope_pair_ff(it.pos, p.freq[it.d], it.a, it.b, p.two_pi_64[0], p.two_pi_64[1], &decided);
+    if (!decided) r = rope_pair_f64(it.pos, p.freq[it.d], it.a, it.b);
+    reinterpret_cast<unsigned short*>(out)[it.at] = static_cast<unsigned short>(r & 0xffffu);
+    reinterpret_cast<unsigned short*>(out)[it.at + D / 2] = static_cast<unsigned short>(r >> 16);
+  }
 }
 
 template <int D>
@@ -834,8 +1087,8 @@ cudaError_t launch_rope_t(const RopeParams& p, cudaStream_t stream) {
   const long long total = static_cast<long long>(p.Hkv) * p.C * (D / 16);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(static_cast<unsigned>((total + 255) / 256));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(static_cast<unsigned>((total + kRopeThreads - 1) / kRopeThreads));
+  cfg.blockDim = dim3(kRopeThreads);
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -7,8 +7,33 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace bd {
+
+// Runs a set-up step once per device -- kernel attributes such as the dynamic
+// shared-memory limit belong to the device that is current when they are set
+// -- and again on a device where it failed.  Thread-safe.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_[dev]) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
 
 constexpr int kAttnBM = 128;        // packed query rows per CTA (tcgen05 M)
 constexpr int kAttnBN = 128;        // keys per K/V tile
@@ -58,6 +83,7 @@ struct AttnParams {
   const int32_t* q_pos;
   const int32_t* kpos;
   int kdelta;
+  unsigned long long wait_ns;  // limit of a pipeline wait (drains keep the full limit)
 };
 
 // New frame of the streaming cache written into every view's frame slot.
@@ -80,6 +106,8 @@ struct RopeParams {
   int Hkv, C, D, delta;
   long long stride;
   unsigned long long turns[64];  // theta^(-2d/D) / (2*pi) as a 0.64 fixed-point fraction
+  double freq[64];               // theta^(-2d/D) in float64
+  float two_pi_64[2];            // 2 pi / 2^64 as float-float
 };
 
 struct AttnMaps {
@@ -116,10 +144,11 @@ struct UnmaskParams {
   float* lse;
   int write_draft;
   int32_t* dev_status;
+  unsigned long long wait_ns;  // limit of a wait for a streamed piece
   // workspace carve-up
-  float4* chunk_part;         // [R, chunks]: (max, sum, argmax bits, -)
+  float4* row_res;            // [R]: (max, sum of exp(l - max), argmax bits, -) of each row
   unsigned int* grid_ticket;  // [1]
-  int chunks;                 // CTAs per logits row
+  int chunks;                 // CTAs per logits row (one cluster)
   int chunk_elems;            // elements per chunk (multiple of 8)
 };
 
@@ -137,21 +166,23 @@ struct VerifyParams {
   int32_t* bonus;
   int32_t* bonus_pos;
   int32_t* dev_status;
-  float4* chunk_part;         // [n_seq * n_rows, chunks]: (score, -, argmax bits, -)
+  unsigned long long wait_ns;
+  float4* row_res;            // [n_seq * n_rows]: (best score, -, argmax bits, -) of each row
   unsigned int* seq_ticket;   // [n_seq]
   int chunks;
   int chunk_elems;
 };
 
 constexpr int kMaxPos = 2048;          // positions of one unmask window
+constexpr int kMaxChunks = 16;         // CTAs (chunks) of one logits row = one thread-block cluster
 constexpr int kMaxVerifyRows = 65535;  // n_seq * n_rows of one verify call (grid y)
 constexpr int kMaxVerifySeqs = 1024;   // sequences of one verify call
 
 size_t unmask_counter_bytes();
 size_t verify_counter_bytes();
-size_t unmask_workspace_bytes(int R, int chunks);
-size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks);
-void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems);
+size_t unmask_workspace_bytes(int R);
+size_t verify_workspace_bytes(int n_seq, int n_rows);
+void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems, int max_chunks = kMaxChunks);
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
 

@@ -14,17 +14,21 @@
 
 namespace bd {
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds unless the call sets its
+// own limit (the pipeline waits take the call's wait_limit_ns; the drains that
+// let issued copies and MMAs land before a CTA exits always take this one).
+// Time is counted in SM clock cycles, two per nanosecond (exact at 2 GHz; at
+// the GB300's 2.07 GHz maximum a limit is 3.5 % short, at lower clocks
+// longer): the cycle counter resolves the sub-microsecond limits that a test
+// of the timeout path uses, which %globaltimer's update interval may not.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+__device__ __forceinline__ long long wait_cycles(uint64_t limit_ns) {
+  return limit_ns < (1ull << 61) ? static_cast<long long>(2 * limit_ns) : (1ll << 62);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -59,51 +63,71 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of parity `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A try_wait may put the thread to sleep for a system-dependent time, which
+// can outlast a short limit (a probe of the timeout path): below this limit
+// the waits poll with test_wait instead.
+constexpr uint64_t kShortWaitNs = 100ull * 1000ull;  // 100 us
+
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return limit_ns < kShortWaitNs ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // The spinning part of mbar_wait_bounded, kept out of line: those waits are
 // few and cold (the vocabulary kernels' piece arrivals, end-of-CTA drains), so
 // one shared copy keeps the code small.  mbar_wait, on the attention kernel's
 // pipeline, spins inline: a call on the wake-up path measured slower there.
 static __device__ __noinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* dev_status) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (abort_flag && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        if (abort_flag) *abort_flag = 1;
-        if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
-        return false;
-      }
+                                              int32_t* dev_status, uint64_t limit_ns) {
+  const long long c0 = clock64();
+  for (;;) {
+    if (mbar_poll(bar, parity, limit_ns)) return true;
+    if (abort_flag && *abort_flag) return false;
+    if (clock64() - c0 > wait_cycles(limit_ns)) {
+      if (abort_flag) *abort_flag = 1;
+      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
+      return false;
     }
   }
 }
 
 // Waits for the phase of parity `parity` of `bar` to complete.  Returns false
-// (after setting *abort_flag and OR-ing BD_DEV_TIMEOUT into *dev_status) if the
-// limit expires, or at once if another thread of the CTA has already aborted.
+// (after setting *abort_flag and OR-ing BD_DEV_TIMEOUT into *dev_status) if
+// `limit_ns` expires, or at once if another thread of the CTA has already
+// aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
-        return false;
-      }
+                                          int32_t* dev_status, uint64_t limit_ns) {
+  if (mbar_poll(bar, parity, limit_ns)) return true;
+  const long long c0 = clock64();
+  for (;;) {
+    if (mbar_poll(bar, parity, limit_ns)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - c0 > wait_cycles(limit_ns)) {
+      *abort_flag = 1;
+      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
+      return false;
     }
   }
 }
 
 // Waits for the phase of parity `parity` of `bar` with no abort flag: gives up
-// after the time limit, OR-ing BD_DEV_TIMEOUT into *dev_status (if given).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_spin(bar, parity, nullptr, dev_status);
+// after `limit_ns`, OR-ing BD_DEV_TIMEOUT into *dev_status (if given).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* dev_status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_poll(bar, parity, limit_ns)) return true;
+  return mbar_spin(bar, parity, nullptr, dev_status, limit_ns);
 }
 
 // 2^x on the MUFU unit: PTX ex2.approx.ftz.f32 (relative error below 2^-22 per
@@ -221,6 +245,13 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
 // 8-byte store to a shared::cluster address (possibly another CTA's shared memory).
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// 16-byte store to a shared::cluster address (possibly another CTA's shared memory).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 
 // Cluster-wide barrier, split into arrive and wait (every thread of every CTA

@@ -24,6 +24,7 @@ constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxBlock = 1024;   // positions of one block
+static_assert(kMaxChunks <= 32, "one warp merges a row's chunk partials");
 constexpr int kMaxVerifyL = 1024; // slots of one verified block
 
 // Running (max, sum of exp(x - max), first index of max).
@@ -114,6 +115,7 @@ struct Stream {
   uint8_t* buf;     // dynamic shared memory
   uint64_t* bars;   // kPieceStages mbarriers
   int32_t* dev_status;
+  uint64_t wait_ns; // limit of a wait for a piece
 };
 
 // Reduces elements [lo, hi) of one row (greedy: logits; sampled: perturbed
@@ -145,7 +147,7 @@ __device__ Acc reduce_chunk(const Stream& st, const void* logits, int dtype, lon
     const int b = k % kPieceStages;
     const int e0 = lo + k * kPiece;
     const int nv = min(kPiece, vend - e0) / 8;
-    if (ok) ok = mbar_wait_bounded(&st.bars[b], (k / kPieceStages) & 1, st.dev_status);
+    if (ok) ok = mbar_wait_bounded(&st.bars[b], (k / kPieceStages) & 1, st.dev_status, st.wait_ns);
     if (ok) {
       const uint8_t* piece = st.buf + b * stage_bytes;
       for (int v = threadIdx.x; v < nv; v += kThreads) {
@@ -193,106 +195,99 @@ __device__ Acc reduce_chunk(const Stream& st, const void* logits, int dtype, lon
   return a;
 }
 
-// Copies n chunk partials to shared memory, four loads in flight per thread.
-__device__ void stage_partials(const float4* src, int n, float4* dst) {
-  for (int i0 = 0; i0 < n; i0 += 4 * kThreads) {
-    float4 q[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kThreads + threadIdx.x;
-      if (i < n) q[u] = __ldcg(src + i);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kThreads + threadIdx.x;
-      if (i < n) dst[i] = q[u];
-    }
-  }
-}
-
-// Merge of one row's chunk partials (staged in shared memory), in chunk order.
-__device__ Acc merge_staged(const float4* part, int chunks) {
+// The CTAs of one logits row are one thread-block cluster (one CTA per chunk,
+// the rank = the chunk): each hands its chunk's (max, sum, first argmax) to
+// rank 0 through distributed shared memory, and after one cluster barrier
+// rank 0's first warp merges them, one partial per lane, into the row's result.
+__device__ Acc warp_merge(const float4* parts, int chunks) {
+  const int lane = threadIdx.x & 31;
   Acc a{-INFINITY, 0.f, 0x7fffffff};
-#pragma unroll 1
-  for (int c = 0; c < chunks; ++c) {
-    const float4 q = part[c];
-    acc_merge(a, Acc{q.x, q.y, __float_as_int(q.z)});
+  if (lane < chunks) {
+    const float4 q = parts[lane];
+    a = Acc{q.x, q.y, __float_as_int(q.z)};
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Acc b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    acc_merge(a, b);
   }
   return a;
 }
 
-constexpr int kStageF4 = 512;  // chunk partials staged at a time by the deciding CTA (8 KB)
+// Hands this CTA's partial (valid in thread 0) to rank 0 of the row's cluster
+// and passes the cluster barrier; in rank 0, returns the row's merged result
+// (valid in thread 0).  Every thread of every CTA of the cluster calls it.
+__device__ Acc cluster_row_merge(const Acc& a, float4* parts, int chunks) {
+  if (threadIdx.x == 0)
+    st_cluster_v4(cluster_addr(smem_addr(parts + blockIdx.x), 0), make_float4(a.m, a.s, __int_as_float(a.idx), 0.f));
+  cluster_arrive();  // release: this CTA's partial is written
+  cluster_wait();    // acquire: every partial of the row is in rank 0's shared memory
+  Acc r{-INFINITY, 0.f, 0x7fffffff};
+  if (blockIdx.x == 0 && threadIdx.x < 32) r = warp_merge(parts, chunks);
+  return r;
+}
+
+constexpr int kStageRows = 2048;  // row results the deciding CTA stages in shared memory
 
 // ======================================================================= unmask
 
-__device__ void unmask_select(const UnmaskParams& p) {
+// The commit rule, in the last CTA to finish a row: every row's result is in
+// p.row_res.  `dyn` (the CTA's idle piece buffers, >= 32 KB) stages the row
+// results.
+__device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
   __shared__ uint8_t st0[kMaxPos];
   __shared__ float conf_s[kMaxPos];
   __shared__ int pred_s[kMaxPos];
   __shared__ int row_s[kMaxPos];
   __shared__ int bs_s[kMaxPos + 1];
   __shared__ int cnt[4];
-  __shared__ float4 stage[kStageF4];
+  float4* res_s = reinterpret_cast<float4*>(dyn);
   const int tid = threadIdx.x;
-  const int per_batch = max(1, kStageF4 / p.chunks);  // logits rows whose partials are staged at once
+  const int n_res = min(p.R, kStageRows);
   {
-    // The loads of a thread are all issued before any is used (one memory
-    // round trip when n_pos <= 256).  The loops are kept rolled: this code runs
-    // once per call in one CTA, so its size (instruction fetch) costs more than
-    // its instruction count.
-    float4 q[kStageF4 / kThreads];
-    const int n0 = min(per_batch, p.R) * p.chunks;
-#pragma unroll
-    for (int u = 0; u < kStageF4 / kThreads; ++u) {
-      const int i = u * kThreads + tid;
-      if (i < n0) q[u] = __ldcg(p.chunk_part + i);
-    }
-    const int n_items = max(p.n_pos, p.n_blocks + 1);
+    // Every load of a thread is issued before any is used: one memory round
+    // trip for the window's state, rows, partition and row results.  The
+    // loops are kept rolled: this code runs once per call in one CTA, so its
+    // size (instruction fetch) costs more than its instruction count.
+    const int n_items = max(max(p.n_pos, p.n_blocks + 1), n_res);
 #pragma unroll 1
     for (int j = tid; j < n_items; j += kThreads) {
       const uint8_t sv = j < p.n_pos ? p.state[j] : 0;
-      const int rv = j < p.n_pos ? __ldg(p.logit_row + j) : 0;
+      const int rv = j < p.n_pos ? __ldg(p.logit_row + j) : -1;
       const int bv = j <= p.n_blocks ? __ldg(p.block_start + j) : 0;
+      const float4 q = j < n_res ? __ldcg(p.row_res + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (j < p.n_pos) {
         st0[j] = sv;
         row_s[j] = rv;
-        conf_s[j] = 0.f;
-        pred_s[j] = -1;
       }
       if (j <= p.n_blocks) bs_s[j] = bv;
-    }
-#pragma unroll
-    for (int u = 0; u < kStageF4 / kThreads; ++u) {
-      const int i = u * kThreads + tid;
-      if (i < n0) stage[i] = q[u];
+      if (j < n_res) res_s[j] = q;
     }
   }
-  // every masked position with a logits row: merge that row's chunk partials
-  #pragma unroll 1
-  for (int r0 = 0; r0 < p.R; r0 += per_batch) {
-    const int nb = min(per_batch, p.R - r0);
-    if (r0 > 0) stage_partials(p.chunk_part + static_cast<size_t>(r0) * p.chunks, nb * p.chunks, stage);
-    __syncthreads();
-    #pragma unroll 1
-    for (int j = tid; j < p.n_pos; j += kThreads) {
-      const int row = row_s[j];
-      if (row < r0 || row >= r0 + nb || st0[j] != BD_MASKED) continue;
-      const Acc a = merge_staged(stage + (row - r0) * p.chunks, p.chunks);
-      conf_s[j] = fast_rcp(a.s);
-      pred_s[j] = a.idx;
-      if (p.lse) p.lse[j] = a.m + fast_log2(a.s) * kLn2;
-    }
-    __syncthreads();
-  }
-  int ok_local = 1;
-  #pragma unroll 1
+  __syncthreads();
+  // every masked position with a logits row: prediction, confidence, LSE
+#pragma unroll 1
   for (int j = tid; j < p.n_pos; j += kThreads) {
-    const int pred = pred_s[j];
+    const int row = row_s[j];
+    int pred = -1;
+    float conf = 0.f, lse = 0.f;
+    if (st0[j] == BD_MASKED && row >= 0 && row < p.R) {
+      const float4 q = row < kStageRows ? res_s[row] : __ldcg(p.row_res + row);
+      pred = __float_as_int(q.z);
+      conf = fast_rcp(q.y);
+      lse = q.x + fast_log2(q.y) * kLn2;
+    }
+    pred_s[j] = pred;
+    conf_s[j] = conf;
     if (p.pred) p.pred[j] = pred;
-    if (p.conf) p.conf[j] = conf_s[j];
-    if (p.lse && pred < 0) p.lse[j] = 0.f;
+    if (p.conf) p.conf[j] = conf;
+    if (p.lse) p.lse[j] = lse;
     p.commit[j] = 0;
   }
+  int ok_local = 1;
   #pragma unroll 1
   for (int b = tid; b < p.n_blocks; b += kThreads) {
     const int lo = bs_s[b], hi = bs_s[b + 1];
@@ -383,6 +378,7 @@ __device__ void unmask_select(const UnmaskParams& p) {
 
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
   __shared__ Acc red[kThreads / 32];
+  __shared__ __align__(16) float4 parts[kMaxChunks];
   __shared__ int last;
   __shared__ __align__(8) uint64_t bars[kPieceStages];
   extern __shared__ __align__(128) uint8_t dyn[];
@@ -397,25 +393,24 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
   // it belongs to, so no lookup stands before the first load
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
-  {
-    const int lo = chunk * p.chunk_elems;
-    const int hi = min(p.V, lo + p.chunk_elems);
-    Acc a{-INFINITY, 0.f, 0x7fffffff};
-    if (lo < hi)
-      a = reduce_chunk(Stream{dyn, bars, p.dev_status}, p.logits, p.dtype, static_cast<long long>(row) * p.ld,
-                       nullptr, 0, 1.f, lo, hi, true);
-    a = block_reduce(a, red);
-    if (threadIdx.x == 0)
-      p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, a.s, __int_as_float(a.idx), 0.f);
-  }
+  const int lo = chunk * p.chunk_elems;
+  const int hi = min(p.V, lo + p.chunk_elems);
+  Acc a{-INFINITY, 0.f, 0x7fffffff};
+  if (lo < hi)
+    a = reduce_chunk(Stream{dyn, bars, p.dev_status, p.wait_ns}, p.logits, p.dtype,
+                     static_cast<long long>(row) * p.ld, nullptr, 0, 1.f, lo, hi, true);
+  a = block_reduce(a, red);
+  const Acc r = cluster_row_merge(a, parts, p.chunks);
+  if (chunk != 0) return;
   if (threadIdx.x == 0) {
+    p.row_res[row] = make_float4(r.m, r.s, __int_as_float(r.idx), 0.f);
     __threadfence();
-    last = atomicAdd(p.grid_ticket, 1u) == gridDim.x * gridDim.y - 1;
+    last = atomicAdd(p.grid_ticket, 1u) == static_cast<unsigned>(p.R - 1);
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  unmask_select(p);
+  unmask_select(p, dyn);
   if (threadIdx.x == 0) *p.grid_ticket = 0u;
 }
 
@@ -425,46 +420,23 @@ __device__ void verify_match(const VerifyParams& p, int s) {
   __shared__ uint8_t st[kMaxVerifyL];
   __shared__ int tok[kMaxVerifyL];
   __shared__ int arg[kMaxVerifyL + 1];
-  __shared__ float4 stage[kStageF4];
   const int L = p.L;
-  const int per_batch = max(1, kStageF4 / p.chunks);  // rows whose partials are staged at once
-  const float4* part = p.chunk_part + static_cast<size_t>(s) * p.n_rows * p.chunks;
   {
-    // the loads of a thread are all issued before any is used (one memory
-    // round trip when L <= 256); loops kept rolled (see unmask_select)
-    float4 q[kStageF4 / kThreads];
-    const int n0 = min(per_batch, p.n_rows) * p.chunks;
-#pragma unroll
-    for (int u = 0; u < kStageF4 / kThreads; ++u) {
-      const int i = u * kThreads + threadIdx.x;
-      if (i < n0) q[u] = __ldcg(part + i);
-    }
+    // one memory round trip: the sequence's state, tokens and row results
+    const float4* res = p.row_res + static_cast<size_t>(s) * p.n_rows;
 #pragma unroll 1
-    for (int j = threadIdx.x; j < L; j += kThreads) {
-      const uint8_t sv = p.state[static_cast<size_t>(s) * L + j];
-      const int tv = p.tokens[static_cast<size_t>(s) * L + j];
-      st[j] = sv;
-      tok[j] = tv;
-    }
-#pragma unroll
-    for (int u = 0; u < kStageF4 / kThreads; ++u) {
-      const int i = u * kThreads + threadIdx.x;
-      if (i < n0) stage[i] = q[u];
+    for (int j = threadIdx.x; j < max(L, p.n_rows); j += kThreads) {
+      const uint8_t sv = j < L ? p.state[static_cast<size_t>(s) * L + j] : 0;
+      const int tv = j < L ? p.tokens[static_cast<size_t>(s) * L + j] : 0;
+      const float4 q = j < p.n_rows ? __ldcg(res + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < L) {
+        st[j] = sv;
+        tok[j] = tv;
+      }
+      if (j < p.n_rows) arg[j] = __float_as_int(q.z) == 0x7fffffff ? -1 : __float_as_int(q.z);
     }
   }
-  // the rows' chunk partials, staged in batches: one thread per row
-  #pragma unroll 1
-  for (int e0 = 0; e0 < p.n_rows; e0 += per_batch) {
-    const int nb = min(per_batch, p.n_rows - e0);
-    if (e0 > 0) stage_partials(part + static_cast<size_t>(e0) * p.chunks, nb * p.chunks, stage);
-    __syncthreads();
-    #pragma unroll 1
-    for (int ee = threadIdx.x; ee < nb; ee += kThreads) {
-      const Acc a = merge_staged(stage + ee * p.chunks, p.chunks);
-      arg[e0 + ee] = a.idx == 0x7fffffff ? -1 : a.idx;
-    }
-    __syncthreads();
-  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int e = 0, n_acc = 0, bonus = -1, bonus_pos = -1;
     bool mismatch = false;
@@ -509,6 +481,7 @@ __device__ void verify_match(const VerifyParams& p, int s) {
 
 __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
   __shared__ Acc red[kThreads / 32];
+  __shared__ __align__(16) float4 parts[kMaxChunks];
   __shared__ int last;
   __shared__ __align__(8) uint64_t bars[kPieceStages];
   extern __shared__ __align__(128) uint8_t dyn[];
@@ -526,13 +499,15 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
   const int hi = min(p.V, lo + p.chunk_elems);
   Acc a{-INFINITY, 0.f, 0x7fffffff};
   if (lo < hi)
-    a = reduce_chunk(Stream{dyn, bars, p.dev_status}, p.logits, p.dtype, static_cast<long long>(row) * p.ld, p.noise,
-                     static_cast<long long>(row) * p.ld, p.inv_temp, lo, hi, false);
+    a = reduce_chunk(Stream{dyn, bars, p.dev_status, p.wait_ns}, p.logits, p.dtype, static_cast<long long>(row) * p.ld,
+                     p.noise, static_cast<long long>(row) * p.ld, p.inv_temp, lo, hi, false);
   a = block_reduce(a, red);
+  const Acc r = cluster_row_merge(a, parts, p.chunks);
+  if (chunk != 0) return;
   if (threadIdx.x == 0) {
-    p.chunk_part[static_cast<size_t>(row) * p.chunks + chunk] = make_float4(a.m, 0.f, __int_as_float(a.idx), 0.f);
+    p.row_res[row] = make_float4(r.m, 0.f, __int_as_float(r.idx), 0.f);
     __threadfence();
-    last = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.chunks * p.n_rows - 1);
+    last = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.n_rows - 1);
   }
   __syncthreads();
   if (!last) return;
@@ -543,13 +518,14 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
 
 }  // namespace
 
-void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems) {
-  // about two CTAs per SM over the whole grid, chunks of at least 2048 elements
+void vocab_split(int rows, int V, int num_sms, int* chunks, int* chunk_elems, int max_chunks) {
+  // about two CTAs per SM over the whole grid, chunks of at least 2048
+  // elements, at most one cluster's worth per row
   const int target = 2 * num_sms;
   int c = (target + rows - 1) / rows;
   const int max_c = (V + 2047) / 2048;
   if (c > max_c) c = max_c;
-  if (c > kStageF4) c = kStageF4;  // the deciding CTA stages one row's partials at once
+  if (c > max_chunks) c = max_chunks;
   if (c < 1) c = 1;
   int e = (V + c - 1) / c;
   e = (e + 7) / 8 * 8;
@@ -566,48 +542,60 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 size_t unmask_counter_bytes() { return 256; }
 size_t verify_counter_bytes() { return align256(sizeof(unsigned) * kMaxVerifySeqs); }
 
-size_t unmask_workspace_bytes(int R, int chunks) {
-  return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(R) * chunks);
-}
+size_t unmask_workspace_bytes(int R) { return unmask_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(R)); }
 
-size_t verify_workspace_bytes(int n_seq, int n_rows, int chunks) {
-  return verify_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_seq) * n_rows * chunks);
+size_t verify_workspace_bytes(int n_seq, int n_rows) {
+  return verify_counter_bytes() + align256(sizeof(float4) * static_cast<size_t>(n_seq) * n_rows);
 }
 
 // Launch with programmatic stream serialisation, so that the kernel's set-up can
 // overlap the tail of the previous kernel (each kernel waits for it with
-// griddepcontrol.wait before touching global memory).
+// griddepcontrol.wait before touching global memory), as clusters of the
+// `chunks` CTAs of one logits row.  A cluster wider than the portable 8 needs
+// that many CTAs' room in one GPC; if the device has none, the rows are cut
+// into 8 chunks instead.
 template <typename P>
-static cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, const P& p, int smem, cudaStream_t stream) {
-  static bool configured = false;  // one instantiation per kernel
-  if (!configured) {
-    const cudaError_t e =
+static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem, cudaStream_t stream) {
+  static PerDeviceOnce configured;  // one instantiation per kernel
+  const cudaError_t ce = configured.run([&] {
+    cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem_bytes(4, true));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+  });
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
+  for (;;) {
+    cfg.gridDim = dim3(p.chunks, rows);
+    attr[1].val.clusterDim.x = p.chunks;
+    if (p.chunks <= 8) break;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) break;
+    (void)cudaGetLastError();
+    vocab_split(rows, V, 152, &p.chunks, &p.chunk_elems, 8);
+  }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
-  return launch_pdl(unmask_kernel, dim3(p.chunks, p.R), p, stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, false),
-                    stream);
+  return launch_rows(unmask_kernel, p.R, p, p.V, stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, false), stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
-  return launch_pdl(verify_kernel, dim3(p.chunks, p.n_seq * p.n_rows), p,
-                    stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, p.noise != nullptr), stream);
+  return launch_rows(verify_kernel, p.n_seq * p.n_rows, p, p.V,
+                     stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, p.noise != nullptr), stream);
 }
 
 }  // namespace bd

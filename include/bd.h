@@ -29,6 +29,13 @@
  *   device finds (a bounded wait that expired, an inconsistent block partition)
  *   are OR-ed into the optional `dev_status` word (device int32, may be NULL);
  *   bd_check() reads and maps it.
+ * - Bounded waits: no kernel waits forever.  Each wait of a kernel's pipeline
+ *   (a tile or a piece of logits that has not landed, a stage not yet freed)
+ *   gives up after `wait_limit_ns` nanoseconds (0 -> 1 s), sets BD_DEV_TIMEOUT
+ *   in *dev_status and makes the call's results invalid; the kernel still lets
+ *   every copy and MMA it has issued land (those drains keep the 1 s limit)
+ *   and exits, so the stream and context stay usable.  A small limit is a way
+ *   to exercise that path.
  * - The kernels are built for sm_103a only; on any other device the calls
  *   return BD_ERR_UNSUPPORTED.
  *
@@ -82,7 +89,10 @@ typedef enum bd_status {
  *
  * With enabled != 0, cached prefix key s is rotated at position k_pos[s] - delta
  * before Q·Kᵀ, rotate-half over the pairs (d, d + D/2) with frequency
- * theta^(-2d/D).  The rotated key enters the bf16 product as bf16.  Queries and
+ * theta^(-2d/D).  The rotated key enters the bf16 product as the bf16 rounding
+ * (to nearest, ties to even) of the rotation formed in float64 -- angle
+ * (k_pos[s] - delta) * f_d, then a cos - b sin and b cos + a sin -- exactly,
+ * element by element, for |k_pos[s] - delta| < 2^24.  Queries and
  * the active positions' own keys must already be rotated by the caller.  The
  * cache itself is never modified: the call rotates the prefix keys once into
  * its workspace (Hkv * C * D * 2 bytes more, counted by bd_*_workspace_size)
@@ -168,6 +178,7 @@ typedef struct bd_attn_args {
   int32_t* dev_status;
   int32_t prefix_ready;
   const int32_t* q_pos;
+  uint64_t wait_limit_ns;
 } bd_attn_args;
 
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream);
@@ -219,6 +230,7 @@ typedef struct bd_fork_args {
   size_t workspace_bytes;
   int32_t* dev_status;
   int32_t prefix_ready;
+  uint64_t wait_limit_ns;
 } bd_fork_args;
 
 bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream);
@@ -335,6 +347,7 @@ typedef struct bd_unmask_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  uint64_t wait_limit_ns;
 } bd_unmask_args;
 
 bd_status bd_unmask_step(const bd_unmask_args* a, void* stream);
@@ -414,6 +427,7 @@ typedef struct bd_verify_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  uint64_t wait_limit_ns;
 } bd_verify_args;
 
 bd_status bd_spec_verify(const bd_verify_args* a, void* stream);
