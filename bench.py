@@ -46,301 +46,168 @@ import synth  # noqa: E402
 METRIC = "committed tokens/s per denoise step; attn & unmask % of HBM/tensor roofline"
 UNIT = "tokens/s"
 W = synth.FAST_DDRIVE
-TAU = 0.9
+TAU = synth.DDRIVE_TAU
 L2_FLUSH_BYTES = 256 << 20
-
-
-# ------------------------------------------------------------------------------ inputs
-
-def make_inputs(seed: int):
-    """Seeded host inputs of one round (float32 arrays holding bf16 values)."""
-    lay = synth.section_layout(W.seed)
-    active = 2                                        # second explanation block
-    C = W.prefix + int(lay.block_start[active])       # prompt prefix + the blocks decoded before it
-    lo, hi = int(lay.block_start[active]), int(lay.block_start[active + 1])
-    n_q = hi - lo
-    scaf = lay.scaffold[lo:hi].astype(np.int64)
-    E = int((scaf == 0).sum())
-    layers = []
-    for l in range(W.layers):
-        a = synth.attn_case(seed, l, C=C, block_start=[0, n_q], Hq=W.Hq, Hkv=W.Hkv, D=W.D, text_from=2700)
-        q_ar = synth.attn_case(seed, 1000 + l, C=0, block_start=[0, n_q], Hq=W.Hq, Hkv=1, D=W.D).q
-        layers.append((a.q, q_ar, a.k, a.v))
-    logits, tok, conf = synth.planted_logits(seed, 1, E, W.V)
-    # the draft is the planted token of every editable row; rows at or above tau
-    # commit in the unmask step; the AR rows agree with the draft on the first k
-    # still-masked slots and disagree at the next one
-    g = synth.rng(seed, 77)
-    masked_rows = [e for e in range(E) if conf[e] < TAU]
-    k = int(g.integers(0, len(masked_rows) + 1))
-    want = g.integers(0, W.V, size=E + 1)
-    for e in range(E):
-        if conf[e] >= TAU or e in masked_rows[:k]:
-            want[e] = tok[e]
-    if k < len(masked_rows):
-        e = masked_rows[k]
-        want[e] = (tok[e] + 1) % W.V
-    ar_logits, _, _ = synth.planted_logits(seed, 2, E + 1, W.V, tokens=want)
-    state = np.where(scaf == 1, synth.SCAFFOLD, synth.MASKED).astype(np.uint8)
-    tokens = np.where(scaf == 1, 11, -1).astype(np.int32)
-    logit_row = np.full(n_q, -1, np.int32)
-    logit_row[scaf == 0] = np.arange(E)
-    return dict(C=C, n_q=n_q, E=E, layers=layers, logits=logits, ar_logits=ar_logits, state=state,
-                tokens=tokens, logit_row=logit_row, planted_accept=k)
 
 
 # ------------------------------------------------------------------------------ GPU arm
 
-class GpuRound:
-    def __init__(self, inp, device):
-        import torch
-        import block_causal_masked_gb300 as bd
-        self.torch, self.bd, self.dev = torch, bd, device
-        self.inp = inp
-        t = lambda x, dt: torch.from_numpy(np.array(x, order="C", copy=True)).to(device).to(dt)  # noqa: E731
-        bf = torch.bfloat16
-        self.q = [t(q, bf) for q, _, _, _ in inp["layers"]]
-        self.q_ar = [t(q, bf) for _, q, _, _ in inp["layers"]]
-        self.k = [t(k, bf) for _, _, k, _ in inp["layers"]]
-        self.v = [t(v, bf) for _, _, _, v in inp["layers"]]
-        n_q = inp["n_q"]
-        self.o = torch.empty((n_q, W.Hq, W.D), dtype=bf, device=device)
-        self.lse = torch.empty((W.Hq, n_q), dtype=torch.float32, device=device)
-        self.block = torch.tensor([0, n_q], dtype=torch.int32, device=device)
-        self.logits = t(inp["logits"], bf)
-        self.ar_logits = t(inp["ar_logits"][None], bf)
-        self.logit_row = t(inp["logit_row"], torch.int32)
-        self.state0 = t(inp["state"], torch.uint8)
-        self.tokens0 = t(inp["tokens"], torch.int32)
-        self.state = self.state0.clone()
-        self.tokens = self.tokens0.clone()
-        self.um = dict(commit=torch.empty(n_q, dtype=torch.uint8, device=device),
-                       n_committed=torch.empty(1, dtype=torch.int32, device=device),
-                       status=torch.empty(1, dtype=torch.int32, device=device),
-                       pred=torch.empty(n_q, dtype=torch.int32, device=device),
-                       conf=torch.empty(n_q, dtype=torch.float32, device=device),
-                       lse=torch.empty(n_q, dtype=torch.float32, device=device))
-        self.acc = torch.empty(1, dtype=torch.int32, device=device)
-        self.bonus = torch.empty(1, dtype=torch.int32, device=device)
-        self.bonus_pos = torch.empty(1, dtype=torch.int32, device=device)
-        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.launches = 0
+def make_inputs(seed: int) -> dict:
+    """Seeded host inputs of one Fast-dDrive-shaped round (synth.fast_ddrive_round)."""
+    return synth.fast_ddrive_round(seed)
 
-    # the four parts of a round, each a sequence of C-ABI calls on the current stream
-    def mdm(self):
-        for l in range(W.layers):
-            self.bd.bd_block_causal_attn(self.q[l], self.k[l], self.v[l], self.inp["C"], block_start=self.block,
-                                         o=self.o, lse=self.lse, prefix_ready=True)
 
-    def unmask(self):
-        self.bd.bd_unmask_step(self.logits, self.logit_row, self.block, self.state, self.tokens, tau_full=TAU,
-                               tau_half=TAU, min_frac=(0, 1), k_fixed=0, write_draft=True, **self.um)
+def gpu_round(inp, device):
+    """The library's SpeculativeRound on the workload's inputs, uploaded to the
+    device, with a 256 MiB buffer for flushing L2 between timed steps."""
+    import torch
+    from block_causal_masked_gb300.decode import SpeculativeRound
+    t = lambda x, dt: torch.from_numpy(np.array(x, order="C", copy=True)).to(device).to(dt)  # noqa: E731
+    bf = torch.bfloat16
+    rd = SpeculativeRound([t(q, bf) for q, _, _, _ in inp["layers"]], [t(q, bf) for _, q, _, _ in inp["layers"]],
+                          [t(k, bf) for _, _, k, _ in inp["layers"]], [t(v, bf) for _, _, _, v in inp["layers"]],
+                          inp["C"], t(inp["logits"], bf), t(inp["ar_logits"][None], bf),
+                          t(inp["logit_row"], torch.int32), t(inp["state"], torch.uint8),
+                          t(inp["tokens"], torch.int32), TAU)
+    rd.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    return rd
 
-    def ar(self):
-        for l in range(W.layers):
-            self.bd.bd_block_causal_attn(self.q_ar[l], self.k[l], self.v[l], self.inp["C"], block_size=1,
-                                         o=self.o, lse=self.lse, prefix_ready=True)
 
-    def verify(self):
-        self.bd.bd_spec_verify(self.tokens.view(1, -1), self.state.view(1, -1), self.ar_logits,
-                               accepted_len=self.acc, bonus=self.bonus, bonus_pos=self.bonus_pos)
+def timed_step(rd) -> float:
+    """Replays the round (one graph) after an L2 flush; returns its ms."""
+    import torch
+    rd.reset()
+    rd.flush.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    rd.whole.replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1)
 
-    def reset(self):
-        self.state.copy_(self.state0)
-        self.tokens.copy_(self.tokens0)
 
-    def committed(self) -> int:
-        return int(self.um["n_committed"][0]) + int(self.acc[0])
+def timed_parts(rd):
+    """Replays the round as its four part graphs with events between them,
+    after an L2 flush; returns (step ms, attention ms, unmask ms)."""
+    import torch
+    rd.reset()
+    rd.flush.zero_()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i, g in enumerate(rd.graphs):
+        g.replay()
+        ev[i + 1].record()
+    ev[4].synchronize()
+    tt = [ev[0].elapsed_time(ev[i + 1]) for i in range(4)]
+    return tt[3], tt[0] + (tt[2] - tt[1]), tt[1] - tt[0]
 
-    def capture(self):
-        torch = self.torch
-        self.reset()
-        self.mdm(); self.unmask(); self.ar(); self.verify()          # allocate workspaces, set kernel attributes
-        torch.cuda.synchronize()
-        s = torch.cuda.Stream(self.dev)
-        self.graphs = []
-        for part in (self.mdm, self.unmask, self.ar, self.verify):
-            g = torch.cuda.CUDAGraph()
-            self.reset()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=s):
-                part()
-            self.graphs.append(g)
-        # the whole round as one graph: consecutive launches overlap through
-        # programmatic dependent launch across the part boundaries too
-        self.whole = torch.cuda.CUDAGraph()
-        self.reset()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(self.whole, stream=s):
-            self.mdm(); self.unmask(); self.ar(); self.verify()
-        torch.cuda.synchronize()
 
-    def timed_step(self):
-        """Replays the round (one graph); returns its ms."""
-        torch = self.torch
-        self.reset()
-        self.flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record()
-        self.whole.replay()
-        e1.record()
-        e1.synchronize()
-        return e0.elapsed_time(e1)
-
-    def timed_parts(self):
-        """Replays the round as its four part graphs with events between them;
-        returns (step ms, attention ms, unmask ms)."""
-        torch = self.torch
-        self.reset()
-        self.flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        torch.cuda.synchronize()
-        ev[0].record()
-        for i, g in enumerate(self.graphs):
-            g.replay()
-            ev[i + 1].record()
-        ev[4].synchronize()
-        t = [ev[0].elapsed_time(ev[i + 1]) for i in range(4)]
-        step = t[3]
-        attn = t[0] + (t[2] - t[1])
-        unmask = t[1] - t[0]
-        return step, attn, unmask
-
-    def attn_splits(self) -> int:
-        """KV splits (cluster width) the library plans for this shape."""
-        m_tiles = -(-self.inp["n_q"] * (W.Hq // W.Hkv) // 128)
-        tiles = -(-self.inp["C"] // 128) + -(-self.inp["n_q"] // 128)
-        return max(1, min(152 // (m_tiles * W.Hkv), tiles, 16))
+def planned_splits(C: int, n_q: int, Hq: int, Hkv: int, D: int) -> int:
+    """KV split count the library plans for a plain attention call, read back
+    from its workspace size (Hkv x row tiles x S x S owner slices of r(S) rows
+    of D bf16 values; none for one split)."""
+    import block_causal_masked_gb300 as bd
+    a = bd.bd_attn_args()
+    a.q = a.k = a.v = a.o = 1 << 20
+    a.C, a.n_q, a.Hq, a.Hkv, a.D, a.kv_stride, a.block_size = C, n_q, Hq, Hkv, D, C + n_q, n_q
+    ws = bd.lib().bd_attn_workspace_size(a)
+    m_tiles = -(-n_q * (Hq // Hkv) // 128)
+    for S in range(2, 17):
+        r = ((128 + S - 1) // S + 1) & ~1
+        if ws == Hkv * m_tiles * S * S * r * 2 * D:
+            return S
+    return 1
 
 
 # ------------------------------------------------------------------------------ device-resident decode
 
 WAM = synth.WAM_SWEEP
-WAM_TOKENS = 256
+WAM_TOKENS = synth.WAM_TOKENS
 
 
-def wam_steps(B: int) -> int:
-    """Steps per block of the WAM-Diff2 sweep: top k = max(1, B / 8) commits per
-    step, at most 8 steps, a block ends once complete."""
-    return min(8, -(-B // max(1, B // 8)))
-
-
-class WamDecode:
-    """The whole 256-token WAM-Diff2 decode at block size B as ONE CUDA graph:
-    for every block, wam_steps(B) denoise steps of `layers` x
-    bd_block_causal_attn (16/8 heads, head dim 128, prefix 2,048 + the blocks
-    already decoded) and one bd_unmask_step (top k by confidence).  Block state
-    and tokens stay on the device; nothing returns to the host between steps.
-    logits: float32 host array [n_blocks, steps, B, V] of bf16 values, or None
-    for seeded N(0, 3) rows drawn on the device."""
-
-    def __init__(self, B: int, layers: int, device, logits=None, seed: int = WAM.seed, num_splits: int = 0):
-        import torch
-        import block_causal_masked_gb300 as bd
-        self.torch, self.bd, self.dev = torch, bd, device
-        self.B, self.layers, self.num_splits = B, layers, num_splits
-        self.n_blocks = WAM_TOKENS // B
-        self.steps = wam_steps(B)
-        self.k = max(1, B // 8)
-        g = torch.Generator(device=device)
-        g.manual_seed(seed * 1000 + B)
-        bf = torch.bfloat16
-        kv_len = WAM.prefix + WAM_TOKENS
-        self.q = [torch.randn((B, WAM.Hq, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
-        self.kk = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
-        self.vv = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
-        self.o = torch.empty((B, WAM.Hq, WAM.D), dtype=bf, device=device)
-        self.lse = torch.empty((WAM.Hq, B), dtype=torch.float32, device=device)
-        if logits is None:
-            self.logits = (torch.randn((self.n_blocks, self.steps, B, synth.VOCAB), generator=g, device=device)
-                           * 3.0).to(bf)
-        else:
-            self.logits = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(device).to(bf)
-        self.block = torch.tensor([0, B], dtype=torch.int32, device=device)
-        self.logit_row = torch.arange(B, dtype=torch.int32, device=device)
-        self.state = torch.zeros(WAM_TOKENS, dtype=torch.uint8, device=device)
-        self.tokens = torch.full((WAM_TOKENS,), -1, dtype=torch.int32, device=device)
-        self.um = dict(commit=torch.empty(B, dtype=torch.uint8, device=device),
-                       n_committed=torch.empty(1, dtype=torch.int32, device=device),
-                       status=torch.empty(1, dtype=torch.int32, device=device),
-                       pred=torch.empty(B, dtype=torch.int32, device=device),
-                       conf=torch.empty(B, dtype=torch.float32, device=device),
-                       lse=torch.empty(B, dtype=torch.float32, device=device))
-        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.launches = self.n_blocks * self.steps * (layers + 1)
-
-    def _block_step(self, b: int, s: int):
-        bd, B = self.bd, self.B
-        C = WAM.prefix + b * B
-        for l in range(self.layers):
-            bd.bd_block_causal_attn(self.q[l], self.kk[l], self.vv[l], C, block_start=self.block, o=self.o,
-                                    lse=self.lse, num_splits=self.num_splits, dev_status=self.dev_status,
-                                    prefix_ready=True)
-        bd.bd_unmask_step(self.logits[b, s], self.logit_row, self.block, self.state[b * B:(b + 1) * B],
-                          self.tokens[b * B:(b + 1) * B], tau_full=2.0, tau_half=2.0, min_frac=(0, 1),
-                          k_fixed=self.k, add_thr=(1, 2), act_thr=(17, 20), dev_status=self.dev_status, **self.um)
-
-    def reset(self):
-        self.state.zero_()
-        self.tokens.fill_(-1)
-
-    def capture(self):
-        torch = self.torch
-        self._block_step(0, 0)                    # workspaces and kernel attributes, outside the capture
-        torch.cuda.synchronize()
-        self.reset()
-        stream = torch.cuda.Stream(self.dev)
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=stream):
-            for b in range(self.n_blocks):
-                for s in range(self.steps):
-                    self._block_step(b, s)
-        torch.cuda.synchronize()
-
-    def replay(self):
-        self.reset()
-        self.graph.replay()
+def wam_decode(B: int, layers: int, device, logits=None, seed: int = WAM.seed, num_splits: int = 0):
+    """The library's BlockDecode on the WAM-Diff2 sweep at block size B: 16/8
+    heads, head dim 128, prompt prefix 2,048, 256 output tokens, top
+    synth.wam_k(B) per step, synth.wam_steps(B) steps per block.  Queries and
+    the cache are drawn on the device from a seeded generator; logits: float32
+    host array [n_blocks, steps, B, V] of bf16 values, or None for seeded
+    N(0, 3) rows drawn on the device."""
+    import torch
+    from block_causal_masked_gb300.decode import BlockDecode
+    n_blocks, steps = WAM_TOKENS // B, synth.wam_steps(B)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000 + B)
+    bf = torch.bfloat16
+    kv_len = WAM.prefix + WAM_TOKENS
+    q = [torch.randn((B, WAM.Hq, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+    kk = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+    vv = [torch.randn((WAM.Hkv, kv_len, WAM.D), generator=g, device=device).to(bf) for _ in range(layers)]
+    if logits is None:
+        lg = (torch.randn((n_blocks, steps, B, synth.VOCAB), generator=g, device=device) * 3.0).to(bf)
+    else:
+        lg = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(device).to(bf)
+    return BlockDecode(q, kk, vv, lg, WAM.prefix, synth.wam_k(B), num_splits=num_splits)
 
 
 def run_wam_sweep(args, device):
-    """One JSON line per block size: committed tokens/s of the whole decode."""
+    """One line per block size: committed tokens/s of the whole decode (one
+    CUDA graph), with the per-launch roofline of its attention (at the
+    decode's midpoint, prefix 2,048 + 128) and unmask kernels."""
     import torch
+    import block_causal_masked_gb300 as bd
     torch.cuda.set_device(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    peaks = measured_peaks()
+    lines = []
     for B in (1, 4, 8, 16, 32):
-        dec = WamDecode(B, WAM.layers, device)
+        dec = wam_decode(B, WAM.layers, device)
         t0 = time.time()
         dec.capture()
         cap_s = time.time() - t0
         for _ in range(args.warmup):
             dec.replay()
         torch.cuda.synchronize()
-        ms = []
-        for _ in range(args.steps):
-            flush.zero_()
-            dec.reset()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            e0.record()
-            dec.graph.replay()
-            e1.record()
-            e1.synchronize()
-            ms.append(e0.elapsed_time(e1))
+        t = _replay_ms(dec.graph, args.steps, flush, before=dec.reset)
+        dec.replay()
+        torch.cuda.synchronize()
         committed = int((dec.state == synth.COMMITTED).sum())
         status = int(dec.dev_status[0])
-        t = statistics.median(ms)
-        print(json.dumps({"metric": "committed tokens/s (whole decode, one CUDA graph)", "value": committed / t * 1e3,
-                          "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-                          "ms_per_decode": t, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-                          "config": {"workload": f"wam_diff2_sweep B={B}: {WAM_TOKENS} tokens, blocks of {B}, top "
-                                                 f"{dec.k} per step, {dec.steps} steps per block, 16/8 heads, "
-                                                 f"head dim 128, {WAM.layers} layers, prefix {WAM.prefix}",
-                                     "gpu_launches_per_decode": dec.launches, "graph_capture_s": round(cap_s, 2),
-                                     "l2": "flushed before every timed decode"},
-                          "committed": committed, "dev_status": status}), flush=True)
-        del dec
+        # per-launch kernel times: one step's 36 attention layers at the
+        # decode's midpoint, and 16 independent unmask calls on fresh blocks
+        C = WAM.prefix + (dec.n_blocks // 2) * B
+
+        def attn_layers():
+            for l in range(WAM.layers):
+                bd.bd_block_causal_attn(dec.q[l], dec.kk[l], dec.vv[l], C, block_start=dec.block, o=dec.o,
+                                        lse=dec.lse, prefix_ready=True)
+        attn_us = _replay_ms(_graph(attn_layers), args.steps, flush) * 1e3 / WAM.layers
+        copies = 16
+        win = _Window(np.zeros(B), np.full(B, -1), copies, device)
+        lgs = [dec.logits[0, 0].clone() for _ in range(copies)]
+        outs = [_unmask_outs(B, 1, device) for _ in range(copies)]
+
+        def unmask(i):
+            bd.bd_unmask_step(lgs[i], dec.logit_row, dec.block, win.state[i], win.tokens[i], tau_full=2.0,
+                              tau_half=2.0, min_frac=(0, 1), k_fixed=dec.k, add_thr=(1, 2), act_thr=(17, 20),
+                              **outs[i])
+        um_us = _per_launch_us([lambda i=i: unmask(i) for i in range(copies)], win.reset, flush, args.steps)
+        nbytes = 2 * WAM.Hkv * (C + B) * WAM.D * 2 + 2 * B * WAM.Hq * WAM.D * 2 + B * WAM.Hq * 4
+        kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * WAM.D * WAM.Hq * B * (C + B), peaks, True),
+                   "unmask_kernel": _vocab_roof(um_us, B * synth.VOCAB * 2, peaks)}
+        lines.append({"metric": "committed tokens/s (whole decode, one CUDA graph)", "value": committed / t * 1e3,
+                      "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_decode": t, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"wam_diff2_sweep B={B}: {WAM_TOKENS} tokens, blocks of {B}, top "
+                                             f"{dec.k} per step, {dec.steps} steps per block, 16/8 heads, "
+                                             f"head dim 128, {WAM.layers} layers, prefix {WAM.prefix}",
+                                 "gpu_launches_per_decode": dec.launches, "graph_capture_s": round(cap_s, 2),
+                                 "l2": "flushed before every timed decode"},
+                      "committed": committed, "dev_status": status, "roofline": kernels})
+        del dec, lgs, outs, win
         torch.cuda.empty_cache()
+    return lines
 
 
 # ------------------------------------------------------------------------------ the other workloads
@@ -427,7 +294,7 @@ def _extra_line(workload: str, tokens_per_step: float, step_ms: float, args, ker
                        "timing": "median of CUDA-event timed graph replays"},
             "committed_per_step": tokens_per_step, "roofline": kernels}
     line.update(extra)
-    print(json.dumps(line), flush=True)
+    return line
 
 
 class _Window:
@@ -537,7 +404,7 @@ def run_tiny(args, dev):
     kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * T.D * T.Hq * vis, peaks, False),
                "unmask_kernel": _vocab_roof(um_us, n_masked * T.V * 4, peaks),
                "verify_kernel": _vocab_roof(vf_us, (E + 1) * T.V * 4, peaks)}
-    _extra_line("tiny: 1 layer, 4/2 heads, head dim 64, prefix 256, 2 blocks of 8 (3 scaffold each), "
+    return _extra_line("tiny: 1 layer, 4/2 heads, head dim 64, prefix 256, 2 blocks of 8 (3 scaffold each), "
                 "fp32 logits [16, 1024]; one round (attention, unmask tau 0.9 + 1/4 + draft, causal AR "
                 "attention, verify)", committed, step_ms, args, kernels, {"gpu_launches_per_step": 4})
 
@@ -598,7 +465,7 @@ def run_fast_dvla(args, dev):
     nbytes = 2 * F.Hkv * (C + n_q) * F.D * 2 + 2 * n_q * F.Hq * F.D * 2 + n_q * F.Hq * 4
     kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * F.D * F.Hq * _attn_visible(C, bs), peaks, True),
                "unmask_kernel": _vocab_roof(um_us, len(masked) * F.V * 2, peaks)}
-    _extra_line(f"fast_dvla: 16/2 heads, head dim 128, 36 layers, prefix {C} keys, window of 3 blocks x 7 "
+    return _extra_line(f"fast_dvla: 16/2 heads, head dim 128, 36 layers, prefix {C} keys, window of 3 blocks x 7 "
                 f"({len(masked)} masked), vocab 151936; one denoise step (36 attention layers + unmask)",
                 committed, step_ms, args, kernels,
                 {"gpu_launches_per_step": F.layers + 1, "block_status": outs[0]["status"].tolist()})
@@ -622,6 +489,7 @@ def run_fork(args, dev):
     k_pos = torch.from_numpy(synth.streaming_prefix_positions()).to(dev)
     rope = dict(k_pos=k_pos, delta=256, theta=1e4)
     bf = torch.bfloat16
+    lines = []
     for N in (1, 8, 32):
         gen = torch.Generator(device=dev)
         gen.manual_seed(S.seed * 1000 + N)
@@ -680,13 +548,14 @@ def run_fork(args, dev):
                   + 2 * N * n_q * S.Hq * S.D * 2 + N * n_q * S.Hq * 4)
         kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * S.D * S.Hq * vis, peaks, True),
                    "verify_kernel": _vocab_roof(vf_us, N * (E + 1) * S.V * (2 + 4), peaks)}
-        _extra_line(f"fork_streaming N={N}: 16/2 heads, head dim 128, 36 layers, 4306 pre-RoPE prefix keys "
+        lines.append(_extra_line(f"fork_streaming N={N}: 16/2 heads, head dim 128, 36 layers, 4306 pre-RoPE prefix keys "
                     f"(RoPE at k_pos - 256), trajectory block of 39 positions after 41 private rows per rollout; "
                     f"one round (MDM fork, causal AR fork, sampled verify of {N} rollouts)",
                     committed, step_ms, args, kernels,
-                    {"gpu_launches_per_step": "2 x 36 x (RoPE pass + attention) + 1", "rollouts": N})
+                    {"gpu_launches_per_step": "2 x 36 x (RoPE pass + attention) + 1", "rollouts": N}))
         del layers, ar, u, ars, us
         torch.cuda.empty_cache()
+    return lines
 
 
 def run_stream(args, dev):
@@ -766,7 +635,7 @@ def run_stream(args, dev):
                                    f"{delta}", "l2": "flushed (256 MiB write) before every timed step",
                        "visible_keys_per_query": vis / n},
             "roofline": kernels}
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def algorithmic(inp):
@@ -803,6 +672,13 @@ class Clocks:
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            # timing starts only once the sampler has written its first row
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and self.proc.poll() is None:
+                with open(self.path) as f:
+                    if f.readline().strip():
+                        break
+                time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
 
@@ -847,8 +723,8 @@ def measured_peaks():
         return None
 
 
-def cpu_baseline(inp, budget_s: float = 12.0):
-    """The float64 oracle on the host cores, full rounds until the budget is spent."""
+def _oracle_sample(inp, budget_s: float):
+    """Full oracle rounds until `budget_s` is spent: (rounds, tokens, seconds)."""
     import oracle
     t0 = time.perf_counter()
     steps, tokens = 0, 0
@@ -857,24 +733,43 @@ def cpu_baseline(inp, budget_s: float = 12.0):
         steps += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{steps} full round(s) of the workload (72 attention layers, unmask, verify) in float64 "
-                      f"numpy, {dt:.1f} s"}
+    return steps, tokens, time.perf_counter() - t0
+
+
+ONE_THREAD_ENV = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                                   "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS")}
+
+
+def cpu_baseline(inp, budget_s: float = 12.0, one_core_budget_s: float = 10.0):
+    """The float64 oracle on the host: on every core (numpy's BLAS threads, this
+    process), and on one core (a child process pinned to one CPU with one BLAS
+    thread), full rounds of the workload until each budget is spent."""
+    steps, tokens, dt = _oracle_sample(inp, budget_s)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    out = {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{steps} full round(s) of the workload (72 attention layers, unmask, verify) in float64 "
+                     f"numpy, {dt:.1f} s"}
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample-s", str(one_core_budget_s)]
+    if hasattr(os, "sched_getaffinity"):
+        cpu = sorted(os.sched_getaffinity(0))[0]
+        cmd = [sys.executable, "-c", f"import os, runpy, sys; os.sched_setaffinity(0, {{{cpu}}}); "
+               f"sys.argv = {cmd[1:]!r}; runpy.run_path(sys.argv[0], run_name='__main__')"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=10 * one_core_budget_s + 120)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out["one_core"] = {"value": one["tokens"] / one["seconds"], "unit": UNIT, "cores": 1,
+                           "sample": f"{one['rounds']} full round(s), {one['seconds']:.1f} s, one CPU, one BLAS "
+                                     "thread"}
+    except (subprocess.SubprocessError, OSError, ValueError, IndexError, KeyError) as e:
+        out["one_core"] = {"value": None, "error": str(e)[:200]}
+    return out
 
 
 def oracle_round(oracle, inp) -> int:
-    from fractions import Fraction
-    C, n_q = inp["C"], inp["n_q"]
-    for q, _, k, v in inp["layers"]:
-        oracle.block_causal_attention(q, k, v, C, [0, n_q])
-    r = oracle.unmask_step(inp["logits"], inp["logit_row"], [0, n_q], inp["state"], inp["tokens"], tau_full=TAU,
-                           tau_half=TAU, min_frac=Fraction(0, 1), k_fixed=0, add_thr=Fraction(1, 2),
-                           act_thr=Fraction(17, 20), write_draft=True)
-    for _, q, k, v in inp["layers"]:
-        oracle.block_causal_attention(q, k, v, C, list(range(n_q + 1)))
-    vr = oracle.spec_verify(r["tokens"][None], r["state"][None], inp["ar_logits"][None])
-    return int(r["n_committed"][0]) + int(vr["accepted_len"][0])
+    """Committed tokens of one round by the float64 oracle."""
+    return oracle.speculative_round(inp["layers"], inp["C"], inp["n_q"], inp["logits"], inp["logit_row"],
+                                    inp["state"], inp["tokens"], inp["ar_logits"], TAU)[0]
 
 
 def e2e_measure(rd, inp, steps: int):
@@ -884,7 +779,7 @@ def e2e_measure(rd, inp, steps: int):
     from pinned host memory and reads its result (committed counts and tokens)
     back to the host, all inside the timed region.  Two device input sets let
     step i+1's copies (on their own stream) overlap step i's kernels."""
-    torch = rd.torch
+    import torch
     hq = [torch.from_numpy(np.array(q, copy=True)).to(torch.bfloat16).pin_memory() for q, _, _, _ in inp["layers"]]
     hqa = [torch.from_numpy(np.array(q, copy=True)).to(torch.bfloat16).pin_memory() for _, q, _, _ in inp["layers"]]
     hl = torch.from_numpy(np.array(inp["logits"], copy=True)).to(torch.bfloat16).pin_memory()
@@ -892,13 +787,13 @@ def e2e_measure(rd, inp, steps: int):
     hs = torch.from_numpy(inp["state"].copy()).pin_memory()
     ht = torch.from_numpy(inp["tokens"].copy()).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in hq + hqa + [hl, ha, hs, ht])
-    sets = [rd, GpuRound(inp, rd.dev)]
+    sets = [rd, gpu_round(inp, rd.q[0].device)]
     sets[1].capture()
     outs = [torch.empty(2, dtype=torch.int32).pin_memory() for _ in sets]
     out_tok = [torch.empty_like(ht).pin_memory() for _ in sets]
     d2h = outs[0].numel() * 4 + out_tok[0].numel() * 4
     compute = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(rd.dev)
+    copy = torch.cuda.Stream(rd.q[0].device)
     copied = [torch.cuda.Event() for _ in sets]
     done = [torch.cuda.Event() for _ in sets]
 
@@ -979,6 +874,38 @@ def vocab_times(rd, inp, device, reps: int):
     return um, vf
 
 
+def latency_floor(device, flush, reps: int) -> dict:
+    """Per-launch time of launches that do almost nothing, 72 back to back in
+    one graph (as the round's attention launches are): an empty elementwise
+    kernel; the attention kernel on one key tile (one CTA, no cluster); and on
+    one 128-key tile per CTA of a 16-CTA cluster (1,920 cached keys + 1, 16
+    splits), which adds the cluster launch and the split merge.  The gap between
+    a kernel's time and these is in-kernel work; the rest is fixed cost."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    n = 72
+    x = torch.zeros(1, device=device)
+    empty_us = _replay_ms(_graph(lambda: [x.add_(1.0) for _ in range(n)]), reps, flush) * 1e3 / n
+    g = torch.Generator(device=device)
+    g.manual_seed(99)
+    q = torch.randn((1, 1, 128), generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn((1, 1921, 128), generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn((1, 1921, 128), generator=g, device=device).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1), dtype=torch.float32, device=device)
+
+    def one_tile():
+        for _ in range(n):
+            bd.bd_block_causal_attn(q, k, v, 0, block_size=1, o=o, lse=lse, num_splits=1, prefix_ready=True)
+
+    def cluster16():
+        for _ in range(n):
+            bd.bd_block_causal_attn(q, k, v, 1920, block_size=1, o=o, lse=lse, num_splits=16, prefix_ready=True)
+    one_us = _replay_ms(_graph(one_tile), reps, flush) * 1e3 / n
+    clu_us = _replay_ms(_graph(cluster16), reps, flush) * 1e3 / n
+    return {"empty_kernel_us": empty_us, "attn_one_tile_us": one_us, "attn_cluster16_one_tile_each_us": clu_us}
+
+
 def replica_seed(rank: int) -> int:
     """Seed of the request rank `rank` decodes (independent inputs per replica)."""
     return W.seed + 100 * rank
@@ -989,19 +916,19 @@ def run_gpu(args, rank, world, local_rank):
     device = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
     inp = make_inputs(replica_seed(rank))
-    rd = GpuRound(inp, device)
+    rd = gpu_round(inp, device)
     rd.capture()
     clocks = Clocks(local_rank)
     for _ in range(args.warmup):
-        rd.timed_step()
-        rd.timed_parts()
+        timed_step(rd)
+        timed_parts(rd)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     steps_ms = []
     committed = 0
     for _ in range(args.steps):
-        steps_ms.append(rd.timed_step())
+        steps_ms.append(timed_step(rd))
         committed += rd.committed()
     torch.cuda.synchronize()
     # per-kernel times for the roofline: the attention from the round replayed
@@ -1010,9 +937,10 @@ def run_gpu(args, rank, world, local_rank):
     attn_ms = []
     reps = max(3, min(50, args.steps // 4))
     for _ in range(reps):
-        _, a, _ = rd.timed_parts()
+        _, a, _ = timed_parts(rd)
         attn_ms.append(a)
     unmask_us, verify_us = vocab_times(rd, inp, device, reps)
+    floor = latency_floor(device, rd.flush, reps)
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_s = sum(steps_ms) / 1e3
@@ -1027,7 +955,7 @@ def run_gpu(args, rank, world, local_rank):
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
     achieved = attn_bytes / attn_launch_s / 1e9
     unmask_s = unmask_us / 1e6
-    splits = rd.attn_splits()
+    splits = planned_splits(inp["C"], inp["n_q"], W.Hq, W.Hkv, W.D)
     launches_per_step = 2 * W.layers + 2
     line = {
         "metric": METRIC, "value": committed_all / total_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -1047,6 +975,7 @@ def run_gpu(args, rank, world, local_rank):
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": "measured" if peaks else "fallback", "traffic": attn_traffic(),
                      "alg_bytes_per_launch": attn_bytes, "avg_launch_us": attn_launch_s * 1e6,
+                     "latency_floor": floor,
                      "unmask": {"alg_bytes": alg["unmask_bytes"], "us": unmask_s * 1e6,
                                 "achieved_gbs": alg["unmask_bytes"] / unmask_s / 1e9,
                                 "frac": alg["unmask_bytes"] / unmask_s / 1e9 / hbm},
@@ -1086,6 +1015,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--contract-only", action="store_true",
+                    help="print the Fast-dDrive-shaped line without the other workloads' results")
+    ap.add_argument("--oracle-sample-s", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork", "stream"],
                     default="fast_ddrive",
                     help="fast_ddrive: the contract's line; the others print extra lines: wam_sweep (the whole "
@@ -1095,6 +1027,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.oracle_sample_s is not None:       # the one-core oracle timing (a child of cpu_baseline)
+        rounds, tokens, secs = _oracle_sample(make_inputs(W.seed), args.oracle_sample_s)
+        print(json.dumps({"rounds": rounds, "tokens": tokens, "seconds": secs}), flush=True)
+        return 0
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -1103,7 +1039,9 @@ def main(argv=None):
     if args.workload in extra:
         import torch
         torch.cuda.set_device(local_rank)
-        extra[args.workload](args, f"cuda:{local_rank}")
+        out = extra[args.workload](args, f"cuda:{local_rank}")
+        for ln in (out if isinstance(out, list) else [out]):
+            print(json.dumps(ln), flush=True)
         return 0
     if args.impl == "reference":
         if rank == 0:
@@ -1113,6 +1051,14 @@ def main(argv=None):
         import torch
         torch.distributed.init_process_group("nccl")
     line = run_gpu(args, rank, world, local_rank)
+    if line is not None and world == 1 and not args.contract_only:
+        # the other four workloads (and the WAM-Diff2 sweep's five block sizes),
+        # each with its per-kernel rooflines, measured after the contract's line
+        sub = argparse.Namespace(steps=max(5, min(args.steps, 20)), warmup=3)
+        dev = f"cuda:{local_rank}"
+        line["configs"] = {"tiny": run_tiny(sub, dev), "fast_dvla": run_fast_dvla(sub, dev),
+                           "wam_diff2_sweep": run_wam_sweep(sub, dev), "fork_streaming": run_fork(sub, dev),
+                           "stream": run_stream(sub, dev)}
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:
