@@ -321,3 +321,117 @@ WAM_SWEEP = Workload("wam_diff2_sweep", 2, 16, 8, 128, 36, 2048, VOCAB, True)
 FAST_DVLA = Workload("fast_dvla", 3, 16, 2, 128, 36, 600, VOCAB, True)
 FORK_STREAM = Workload("fork_streaming", 4, 16, 2, 128, 36, 4096 + 210, VOCAB, True)
 WORKLOADS = {w.name: w for w in (TINY, FAST_DDRIVE, WAM_SWEEP, FAST_DVLA, FORK_STREAM)}
+
+
+# --------------------------------------------------------------------------------------
+# whole-step inputs of the workloads the benchmark times
+# --------------------------------------------------------------------------------------
+
+DDRIVE_TAU = 0.9      # confidence threshold of the Fast-dDrive-shaped round's MDM commits
+WAM_TOKENS = 256      # output length of the WAM-Diff2 block sweep
+
+
+def wam_k(B: int) -> int:
+    """Commits per denoise step of the WAM-Diff2 sweep at block size B: B / 8, at least 1."""
+    return max(1, B // 8)
+
+
+def wam_steps(B: int) -> int:
+    """Denoise steps per block of the WAM-Diff2 sweep: at most 8, and a block
+    ends once complete (top k = wam_k(B) commits per step)."""
+    return min(8, -(-B // wam_k(B)))
+
+
+def fast_ddrive_round(seed: int) -> dict:
+    """Host inputs of one scaffold-speculative round of the Fast-dDrive-shaped
+    workload (float32 arrays holding bf16 values).
+
+    The active block is the second explanation block of the 404-position
+    scaffolded output; its cache is the 3,000-token prompt plus the blocks
+    decoded before it.  Per layer: the MDM pass's queries, the AR pass's
+    queries, K and V (the prompt's 300 text rows carry a shared bias).  MDM
+    logits of the editable rows have one planted token each, its softmax
+    probability ~ U(0.3, 0.99); the AR rows agree with the planted tokens on
+    every row at or above the threshold and on the first ``planted_accept``
+    rows below it, and disagree on the next one.
+    """
+    W = FAST_DDRIVE
+    lay = section_layout(W.seed)
+    active = 2
+    C = W.prefix + int(lay.block_start[active])
+    lo, hi = int(lay.block_start[active]), int(lay.block_start[active + 1])
+    n_q = hi - lo
+    scaf = lay.scaffold[lo:hi].astype(np.int64)
+    E = int((scaf == 0).sum())
+    layers = []
+    for l in range(W.layers):
+        a = attn_case(seed, l, C=C, block_start=[0, n_q], Hq=W.Hq, Hkv=W.Hkv, D=W.D, text_from=2700)
+        q_ar = attn_case(seed, 1000 + l, C=0, block_start=[0, n_q], Hq=W.Hq, Hkv=1, D=W.D).q
+        layers.append((a.q, q_ar, a.k, a.v))
+    logits, tok, conf = planted_logits(seed, 1, E, W.V)
+    g = rng(seed, 77)
+    masked_rows = [e for e in range(E) if conf[e] < DDRIVE_TAU]
+    k = int(g.integers(0, len(masked_rows) + 1))
+    want = g.integers(0, W.V, size=E + 1)
+    for e in range(E):
+        if conf[e] >= DDRIVE_TAU or e in masked_rows[:k]:
+            want[e] = tok[e]
+    if k < len(masked_rows):
+        e = masked_rows[k]
+        want[e] = (tok[e] + 1) % W.V
+    ar_logits, _, _ = planted_logits(seed, 2, E + 1, W.V, tokens=want)
+    state = np.where(scaf == 1, SCAFFOLD, MASKED).astype(np.uint8)
+    tokens = np.where(scaf == 1, 11, -1).astype(np.int32)
+    logit_row = np.full(n_q, -1, np.int32)
+    logit_row[scaf == 0] = np.arange(E)
+    return dict(C=C, n_q=n_q, E=E, layers=layers, logits=logits, ar_logits=ar_logits, state=state,
+                tokens=tokens, logit_row=logit_row, planted_accept=k, planted_conf=conf)
+
+
+# --------------------------------------------------------------------------------------
+# FP8 (E4M3) KV cache: what a cache writer stores
+# --------------------------------------------------------------------------------------
+
+KV_BLOCK = 128        # cache rows per power-of-two scale
+E4M3_MAX = 448.0
+
+
+def _e4m3_grid() -> Tuple[np.ndarray, np.ndarray]:
+    """The non-negative finite E4M3 values in increasing order and their bytes
+    (exponent field e, mantissa m: e = 0 gives m 2^-9, else (8 + m) 2^(e - 10);
+    S.1111.111 is not a value)."""
+    vals, codes = [], []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            vals.append(m * 2.0 ** -9 if e == 0 else (8 + m) * 2.0 ** (e - 10))
+            codes.append((e << 3) | m)
+    return np.array(vals), np.array(codes, dtype=np.uint8)
+
+
+def quantize_kv_e4m3(x: np.ndarray, block: int = KV_BLOCK) -> Tuple[np.ndarray, np.ndarray]:
+    """Store x [H, S, D] as E4M3 bytes with one power-of-two scale per (head,
+    block of `block` rows): exp = the smallest e with max|x| 2^-e <= 448 in the
+    block, then each x 2^-exp rounded to the nearest E4M3 value (ties to the
+    even mantissa).  Returns (bytes uint8 [H, S, D], exponents int8 [H, ceil(S / block)])."""
+    x = np.asarray(x, dtype=np.float64)
+    H, S, D = x.shape
+    nb = -(-S // block)
+    exps = np.zeros((H, nb), np.int8)
+    grid, codes = _e4m3_grid()
+    q = np.empty((H, S, D), np.uint8)
+    for h in range(H):
+        for b in range(nb):
+            blk = x[h, b * block:(b + 1) * block]
+            amax = float(np.abs(blk).max()) if blk.size else 0.0
+            e = int(np.ceil(np.log2(amax / E4M3_MAX))) if amax > 0 else 0
+            exps[h, b] = e
+            y = np.abs(blk) * 2.0 ** -e
+            hi = np.clip(np.searchsorted(grid, y, side="left"), 0, len(grid) - 1)
+            lo = np.clip(hi - 1, 0, len(grid) - 1)
+            dlo, dhi = y - grid[lo], grid[hi] - y
+            pick_hi = (dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0))
+            idx = np.where(y >= grid[-1], len(grid) - 1, np.where(pick_hi, hi, lo))
+            q[h, b * block:(b + 1) * block] = codes[idx] | np.where(blk < 0, 0x80, 0).astype(np.uint8)
+    return q, exps

@@ -2,7 +2,11 @@
 the tolerances the workload fixes.
 
 Attention: |o - o_ref| <= 1e-2 + 1e-2 |o_ref| element-wise, LSE within 1e-5
-relative.  Integer and index outputs: bit-exact.  Confidences: 2e-6 relative
+relative (plus 1e-6 absolute: an LSE near zero -- a row that sees one or two
+keys -- is one or two scores, and a score's fp32 error is absolute, about
+2^-24 times the sum of |q_d k_d| / sqrt(D) over its D terms, ~5e-7 for N(0, 1)
+inputs at D = 128; no relative bound can hold there).  Integer and index
+outputs: bit-exact.  Confidences: 2e-6 relative
 (fp32 accumulation over the vocabulary against float64); the commit decisions
 taken from them are exact because every input is drawn with decision margins
 that the tests assert (see the ``margins`` returned by the oracle).
@@ -65,29 +69,3 @@ def bf16_midpoint_distance(x) -> np.ndarray:
     scaled = m * 256.0                       # bf16 values are the integers here
     d = np.abs(scaled - np.floor(scaled) - 0.5) * np.ldexp(1.0, e - 8)
     return np.where(x == 0.0, np.inf, d)
-
-
-ROPE_MARGIN = 2e-6
-
-
-def condition_rope_keys(k, pos, delta: int, theta: float, seed: int, C: int | None = None,
-                        margin: float = ROPE_MARGIN):
-    """Redraws (in place, seeded) the pre-RoPE prefix key rows [0, C) of k [Hkv, S, D]
-    whose rotated elements lie within `margin` of a bf16 rounding midpoint.
-
-    The bf16 rounding of a rotated key is a decision taken in floating point: the
-    kernel rotates in fp32 (angle within 1e-7 rad, sin / cos within an ulp, so a
-    rotated element of keys below 8 in magnitude is within ~1.2e-6), the oracle
-    in float64; inputs are kept where no such error can change that rounding, as
-    for every other decision."""
-    C = k.shape[1] if C is None else C
-    p = np.asarray(pos, dtype=np.int64)[:C] - int(delta)
-    for attempt in range(100):
-        r = oracle.rope_rotate(k[:, :C], p, theta)
-        bad = np.argwhere((bf16_midpoint_distance(r) < margin).any(axis=-1))
-        if bad.size == 0:
-            return k
-        g = synth.rng(seed, 990, attempt)
-        for h, j in bad:
-            k[h, j] = synth.to_bf16(g.standard_normal(k.shape[-1]).astype(np.float32))
-    raise AssertionError("rope keys could not be conditioned")

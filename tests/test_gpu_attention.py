@@ -12,7 +12,7 @@ import torch
 import block_causal_masked_gb300 as bd
 import oracle
 import synth
-from helpers import DEV, assert_attn_close, bf16, condition_rope_keys, host, i32, status_word
+from helpers import DEV, assert_attn_close, bf16, bf16_midpoint_distance, host, i32, status_word
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,6 @@ def test_in_kernel_rope_matches_oracle(D):
     C = 600
     case = synth.attn_case(14, D, C=C, block_start=[0, 12, 20], Hq=16, Hkv=2, D=D)
     k_pos = (np.arange(C) * 3 + 256).astype(np.int32)
-    condition_rope_keys(case.k, k_pos, 256, 10000.0, 14, C=C)
     rope = dict(k_pos=i32(k_pos), delta=256, theta=10000.0)
     o, lse = _run(case, 0, rope=rope)
     o_ref, lse_ref = oracle.block_causal_attention(case.q, case.k, case.v, C, case.block_start, k_pos=k_pos,
@@ -97,20 +96,50 @@ def test_in_kernel_rope_matches_oracle(D):
     assert_attn_close(o, lse, o_ref, lse_ref, f"rope D={D}")
 
 
+@pytest.mark.parametrize("D,C,delta,spread", [(128, 4306, 256, 0), (64, 3000, 7, 3), (128, 1024, 12345, 997)])
+def test_rotated_prefix_keys_bit_exact(D, C, delta, spread):
+    """The operator's rotated copy of the pre-RoPE prefix keys -- the first
+    Hkv * C * D bf16 values of the workspace when the call runs unsplit -- is,
+    element by element, the bf16 rounding (to nearest even) of the float64
+    rotation, on unconditioned N(0, 1) keys: the streaming prefix's view-major
+    positions, a strided layout, and positions up to ~1e6.  The inputs reach
+    rotated elements within 1e-6 of a bf16 rounding midpoint, where the fp32
+    rotation cannot decide the rounding and the float64 one does."""
+    if spread == 0:
+        k_pos = synth.streaming_prefix_positions()
+    else:
+        k_pos = (np.arange(C) * spread + delta + 1).astype(np.int32)
+    Hkv = 2
+    case = synth.attn_case(21 + spread, D, C=C, block_start=[0, 8], Hq=4, Hkv=Hkv, D=D)
+    nbytes = Hkv * C * D * 2
+    ws = torch.zeros(nbytes + 4096, dtype=torch.uint8, device=DEV)
+    ds = status_word()
+    bd.bd_block_causal_attn(bf16(case.q), bf16(case.k), bf16(case.v), C, block_start=i32(case.block_start),
+                            num_splits=1, workspace=ws, dev_status=ds,
+                            rope=dict(k_pos=i32(k_pos), delta=delta, theta=1e4))
+    assert bd.bd_check(ds) == 0
+    got = host(ws[:nbytes].view(torch.bfloat16)).reshape(Hkv, C, D).astype(np.float64)
+    rot = oracle.rope_rotate(case.k[:, :C], k_pos.astype(np.int64) - delta, 1e4)
+    ref = oracle.round_bf16(rot)
+    bad = got != ref
+    assert not bad.any(), f"{bad.sum()} of {bad.size} rotated elements differ"
+    assert (bf16_midpoint_distance(rot) < 1e-6).sum() > 0
+
+
 def test_in_kernel_rope_equals_prerotated_keys():
-    """RoPE inside the operator gives the no-RoPE result on keys rotated
-    beforehand (rotated in float64 and rounded to bf16 on the host)."""
+    """RoPE inside the operator gives bitwise the no-RoPE result on keys rotated
+    beforehand (rotated in float64 and rounded to bf16 on the host): the
+    operator's rotated keys are those same bf16 values, and the two calls run
+    the same plan."""
     C = 4096 + 210
     case = synth.attn_case(15, 0, C=C, block_start=[0, 39], Hq=16, Hkv=2, D=128)
     k_pos = synth.streaming_prefix_positions()
-    condition_rope_keys(case.k, k_pos, 256, 1e4, 15, C=C)
     o, lse = _run(case, 0, rope=dict(k_pos=i32(k_pos), delta=256, theta=1e4))
     k2 = case.k.copy()
     k2[:, :C] = oracle.round_bf16(oracle.rope_rotate(case.k[:, :C], k_pos.astype(np.int64) - 256, 1e4))
     case2 = synth.AttnCase(case.q, k2, case.v, C, case.block_start)
     o2, lse2 = _run(case2, 0)
-    assert np.allclose(host(lse), host(lse2), rtol=2e-6, atol=1e-6)
-    assert np.allclose(host(o), host(o2), rtol=1e-2, atol=1e-2)
+    assert torch.equal(lse, lse2) and torch.equal(o, o2)
 
 
 # ---------------------------------------------------------------------------------------- fork
@@ -121,8 +150,6 @@ def _fork(seed, N, C, n_q, priv_len, bs, D=128, rope=False):
         k_pos = (np.arange(C) + 256).astype(np.int32)
     f = synth.fork_case(seed, 0, N=N, C=C, n_q=n_q, priv_len=priv_len, block_start=bs, Hq=16, Hkv=2, D=D,
                         k_pos=k_pos, delta=256 if rope else 0, theta=1e4)
-    if rope:
-        condition_rope_keys(f.prefix_k, k_pos, 256, 1e4, seed)
     return f
 
 
@@ -187,8 +214,6 @@ def test_prefix_ready_matches_default_in_a_graph(rope):
     RoPE the flag is ignored.  The last launch also matches the oracle."""
     C, bs, n = 1500, [0, 33], 4
     case = synth.attn_case(12, 0, C=C, block_start=bs, Hq=16, Hkv=2, D=128)
-    if rope:
-        condition_rope_keys(case.k, np.arange(C) + 7, 7, 1e4, 12, C=C)
     k, v = bf16(case.k), bf16(case.v)
     q0 = bf16(case.q)
     blk = i32(bs)

@@ -9,9 +9,11 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
-import bench
+import torch
+
 import oracle
 import synth
+from block_causal_masked_gb300.decode import BlockDecode
 from helpers import DEV, assert_attn_close, host
 
 pytestmark = pytest.mark.gpu
@@ -21,12 +23,12 @@ V = synth.VOCAB
 def _oracle_decode(B: int):
     """Logits of every step (redrawn until the top-k cut has a margin fp32 cannot
     cross) and the oracle's final state and tokens."""
-    n_blocks, steps, k = bench.WAM_TOKENS // B, bench.wam_steps(B), max(1, B // 8)
+    n_blocks, steps, k = synth.WAM_TOKENS // B, synth.wam_steps(B), synth.wam_k(B)
     kw = dict(tau_full=2.0, tau_half=2.0, min_frac=Fraction(0, 1), k_fixed=k, add_thr=Fraction(1, 2),
               act_thr=Fraction(17, 20))
     logits = np.empty((n_blocks, steps, B, V), np.float32)
-    state = np.zeros(bench.WAM_TOKENS, np.int64)
-    tokens = np.full(bench.WAM_TOKENS, -1, np.int64)
+    state = np.zeros(synth.WAM_TOKENS, np.int64)
+    tokens = np.full(synth.WAM_TOKENS, -1, np.int64)
     for b in range(n_blocks):
         sl = slice(b * B, (b + 1) * B)
         for s in range(steps):
@@ -45,14 +47,22 @@ def _oracle_decode(B: int):
 @pytest.mark.parametrize("B", [1, 8, 32])
 def test_wam_decode_graph_matches_oracle(B):
     logits, state_ref, tokens_ref = _oracle_decode(B)
-    dec = bench.WamDecode(B, 2, DEV, logits=logits)
+    W = synth.WAM_SWEEP
+    g = torch.Generator(device=DEV)
+    g.manual_seed(1000 * W.seed + B)
+    kv_len = W.prefix + synth.WAM_TOKENS
+    q = [torch.randn((B, W.Hq, W.D), generator=g, device=DEV).to(torch.bfloat16) for _ in range(2)]
+    kk = [torch.randn((W.Hkv, kv_len, W.D), generator=g, device=DEV).to(torch.bfloat16) for _ in range(2)]
+    vv = [torch.randn((W.Hkv, kv_len, W.D), generator=g, device=DEV).to(torch.bfloat16) for _ in range(2)]
+    lg = torch.from_numpy(logits).to(DEV).to(torch.bfloat16)
+    dec = BlockDecode(q, kk, vv, lg, W.prefix, synth.wam_k(B))
     dec.capture()
     dec.replay()
     assert int(host(dec.dev_status)[0]) == 0
     assert np.array_equal(host(dec.state).astype(np.int64), state_ref)
     assert np.array_equal(host(dec.tokens).astype(np.int64), tokens_ref)
     # the last launch of the graph: layer 1 of the last block's last step
-    C = bench.WAM.prefix + (dec.n_blocks - 1) * B
+    C = W.prefix + (dec.n_blocks - 1) * B
     q, k, v = (host(t).astype(np.float32) for t in (dec.q[1], dec.kk[1], dec.vv[1]))
     o_ref, lse_ref = oracle.block_causal_attention(q, k, v, C, [0, B])
     assert_attn_close(dec.o, dec.lse, o_ref, lse_ref, f"B={B}")

@@ -9,19 +9,27 @@ import numpy as np
 import pytest
 import torch
 
-import bench
 import block_causal_masked_gb300 as bd
+from block_causal_masked_gb300.decode import SpeculativeRound
 import oracle
 import synth
-from helpers import CONF_RTOL, DEV, assert_attn_close, bf16, condition_rope_keys, f32, host, i32, status_word, u8
+from helpers import CONF_RTOL, DEV, assert_attn_close, bf16, f32, host, i32, status_word, u8
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module")
 def ddrive():
-    inp = bench.make_inputs(bench.W.seed)
-    rd = bench.GpuRound(inp, DEV)
+    """The Fast-dDrive-shaped round the benchmark times, on the library's
+    SpeculativeRound driver."""
+    inp = synth.fast_ddrive_round(synth.FAST_DDRIVE.seed)
+    t = lambda x, dt: torch.from_numpy(np.array(x, order="C", copy=True)).to(DEV).to(dt)  # noqa: E731
+    bf = torch.bfloat16
+    rd = SpeculativeRound([t(q, bf) for q, _, _, _ in inp["layers"]], [t(q, bf) for _, q, _, _ in inp["layers"]],
+                          [t(k, bf) for _, _, k, _ in inp["layers"]], [t(v, bf) for _, _, _, v in inp["layers"]],
+                          inp["C"], t(inp["logits"], bf), t(inp["ar_logits"][None], bf),
+                          t(inp["logit_row"], torch.int32), t(inp["state"], torch.uint8),
+                          t(inp["tokens"], torch.int32), synth.DDRIVE_TAU)
     return inp, rd
 
 
@@ -44,7 +52,8 @@ def test_bench_round_unmask_and_verify(ddrive):
     does the committed count the bench reports."""
     inp, rd = ddrive
     n_q = inp["n_q"]
-    kw = dict(tau_full=bench.TAU, tau_half=bench.TAU, min_frac=Fraction(0, 1), k_fixed=0, add_thr=Fraction(1, 2),
+    kw = dict(tau_full=synth.DDRIVE_TAU, tau_half=synth.DDRIVE_TAU, min_frac=Fraction(0, 1), k_fixed=0,
+              add_thr=Fraction(1, 2),
               act_thr=Fraction(17, 20), write_draft=True)
     ref = oracle.unmask_step(inp["logits"], inp["logit_row"], [0, n_q], inp["state"], inp["tokens"], **kw)
     assert ref["margins"]["tau"] >= 1e-4
@@ -63,7 +72,15 @@ def test_bench_round_unmask_and_verify(ddrive):
     assert int(rd.bonus_pos[0]) == int(vref["bonus_pos"][0])
     assert np.array_equal(host(rd.tokens).astype(np.int64), vref["tokens"][0])
     assert np.array_equal(host(rd.state).astype(np.int64), vref["state"][0])
-    assert rd.committed() == bench.oracle_round(oracle, inp)
+    total, _, _ = oracle.speculative_round(inp["layers"], inp["C"], inp["n_q"], inp["logits"], inp["logit_row"],
+                                           inp["state"], inp["tokens"], inp["ar_logits"], synth.DDRIVE_TAU)
+    assert rd.committed() == total
+    # the round captured as one CUDA graph and replayed commits the same
+    rd.capture()
+    rd.replay()
+    torch.cuda.synchronize()
+    assert rd.committed() == total
+    assert np.array_equal(host(rd.tokens).astype(np.int64), vref["tokens"][0])
 
 
 @pytest.mark.parametrize("N", [1, 8, 32])
@@ -75,7 +92,6 @@ def test_fork_streaming_full_size(N):
     k_pos = synth.streaming_prefix_positions()
     f = synth.fork_case(4, N, N=N, C=C, n_q=39, priv_len=41, block_start=[0, 39], Hq=16, Hkv=2, D=128,
                         k_pos=k_pos, delta=256, theta=1e4)
-    condition_rope_keys(f.prefix_k, k_pos, 256, 1e4, 4)
     ds = status_word()
     o, lse = bd.bd_fork_rollouts(bf16(f.q), bf16(f.prefix_k), bf16(f.prefix_v), bf16(f.priv_k), bf16(f.priv_v),
                                  f.priv_len, C, block_start=i32(f.block_start),

@@ -12,7 +12,7 @@ import torch
 import block_causal_masked_gb300 as bd
 import oracle
 import synth
-from helpers import DEV, assert_attn_close, bf16, condition_rope_keys, host, i32, status_word
+from helpers import DEV, assert_attn_close, bf16, host, i32, status_word
 
 pytestmark = pytest.mark.gpu
 
@@ -82,8 +82,6 @@ def test_streaming_mask_matches_oracle(views, frames, per, D, rope):
     Hq, Hkv = 16, 2
     k, v, kp, delta, q, qpos = _stream_case(3, views, frames, per, Hq, Hkv, D, slides=2)
     C = views * frames * per
-    if rope:
-        condition_rope_keys(k, kp, delta, 1e4, 3, C=C)
     ds = status_word()
     o, lse = bd.bd_block_causal_attn(bf16(q), bf16(k), bf16(v), C, q_pos=i32(qpos),
                                      rope=dict(k_pos=i32(kp), delta=delta, theta=1e4) if rope else

@@ -266,17 +266,15 @@ def test_fork_rollouts_are_independent():
     assert np.array_equal(o[[0, 2]], o2[[0, 2]]) and not np.array_equal(o[1], o2[1])
 
 
-def test_rope_key_conditioning_margin():
-    """The helper that keeps RoPE test inputs away from bf16 rounding midpoints:
-    hand values (bf16 spacing is 2^-7 on [1, 2): 1 + 2^-8 is a midpoint, 1 and
-    1 + 2^-7 are bf16 values half a spacing from one; spacing 2^-6 at 3), and
-    conditioned keys keep the margin."""
+def test_bf16_midpoint_distance_helper():
+    """The helper the GPU RoPE test uses to show that its inputs reach elements
+    near a bf16 rounding midpoint: hand values (bf16 spacing is 2^-7 on [1, 2):
+    1 + 2^-8 is a midpoint, 1 and 1 + 2^-7 are bf16 values half a spacing from
+    one; spacing 2^-6 at 3), and rounding by the oracle flips exactly across a
+    midpoint."""
     import helpers
     d = helpers.bf16_midpoint_distance(np.array([1.0, 1.0 + 2 ** -8, 1.0 + 2 ** -7, 0.0, -3.0]))
     assert d[0] == 2 ** -8 and d[1] == 0.0 and d[2] == 2 ** -8
     assert np.isinf(d[3]) and d[4] == 2 ** -7
-    k = synth.attn_case(30, 0, C=200, block_start=[0, 4], Hq=4, Hkv=2, D=16).k
-    pos = np.arange(200) * 5
-    helpers.condition_rope_keys(k, pos, 3, 1e4, 30, C=200)
-    r = oracle.rope_rotate(k[:, :200], pos - 3, 1e4)
-    assert (helpers.bf16_midpoint_distance(r) >= helpers.ROPE_MARGIN).all()
+    mid = 1.0 + 2 ** -8 + 2 ** -7          # midpoint between 1 + 2^-7 and 1 + 2^-6
+    assert oracle.round_bf16(mid - 1e-12) == 1.0 + 2 ** -7 and oracle.round_bf16(mid + 1e-12) == 1.0 + 2 ** -6
