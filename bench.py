@@ -490,7 +490,7 @@ def run_fork(args, dev):
     rope = dict(k_pos=k_pos, delta=256, theta=1e4)
     bf = torch.bfloat16
     lines = []
-    for N in (1, 8, 32):
+    for N in ((args.rollouts,) if getattr(args, "rollouts", None) else (1, 8, 32)):
         gen = torch.Generator(device=dev)
         gen.manual_seed(S.seed * 1000 + N)
         rn = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(bf)  # noqa: E731
@@ -556,6 +556,58 @@ def run_fork(args, dev):
         del layers, ar, u, ars, us
         torch.cuda.empty_cache()
     return lines
+
+
+def run_kv_fp8(args, dev):
+    """The FP8 (E4M3) KV-cache variant beside the bf16 attention, per launch, on
+    the WAM-Diff2 decode shape (16/8 heads, head dim 128, prefix 2,048 + 128
+    decoded, blocks of 32 and of 1) and the Fast-dDrive decode shape (16/2
+    heads, 3,124 cached keys, 33 positions): 36 distinct layers back to back in
+    a graph, L2 flushed before each replay.  The E4M3 cache holds half the
+    bytes; the roofline counts the bytes each variant must read."""
+    import torch
+    import block_causal_masked_gb300 as bd
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks = measured_peaks()
+    shapes = [("wam_diff2 B=32", 16, 8, 2048 + 128, 32), ("wam_diff2 B=1", 16, 8, 2048 + 128, 1),
+              ("fast_ddrive", 16, 2, 3124, 33)]
+    out = {}
+    for name, Hq, Hkv, C, n_q in shapes:
+        D, L = 128, 36
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        S = C + n_q
+        q = [torch.randn((n_q, Hq, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+        kb = [torch.randn((Hkv, S, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+        vb = [torch.randn((Hkv, S, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+        # E4M3 copies: bytes drawn uniformly over the finite codes, exponent -4 per block
+        # (timing only: any bytes run the same instructions)
+        k8 = [torch.randint(0, 0x7e, (Hkv, S, D), generator=g, device=dev, dtype=torch.uint8) for _ in range(L)]
+        v8 = [torch.randint(0, 0x7e, (Hkv, S, D), generator=g, device=dev, dtype=torch.uint8) for _ in range(L)]
+        ex = torch.full((Hkv, -(-S // 128)), -4, dtype=torch.int8, device=dev)
+        o = torch.empty((n_q, Hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((Hq, n_q), dtype=torch.float32, device=dev)
+        blk = torch.tensor([0, n_q], dtype=torch.int32, device=dev)
+
+        def bf():
+            for l in range(L):
+                bd.bd_block_causal_attn(q[l], kb[l], vb[l], C, block_start=blk, o=o, lse=lse, prefix_ready=True)
+
+        def f8():
+            for l in range(L):
+                bd.bd_block_causal_attn(q[l], k8[l], v8[l], C, block_start=blk, o=o, lse=lse, k_exp=ex, v_exp=ex)
+        us_bf = _replay_ms(_graph(bf), args.steps, flush) * 1e3 / L
+        us_f8 = _replay_ms(_graph(f8), args.steps, flush) * 1e3 / L
+        qo = 2 * n_q * Hq * D * 2 + n_q * Hq * 4
+        flops = 4 * D * Hq * n_q * S
+        out[name] = {"bf16": _attn_roof(us_bf, qo + 2 * Hkv * S * D * 2, flops, peaks, True),
+                     "e4m3": _attn_roof(us_f8, qo + 2 * Hkv * S * D + 2 * Hkv * (-(-S // 128)), flops, peaks, True)}
+        del q, kb, vb, k8, v8
+        torch.cuda.empty_cache()
+    return {"metric": "attention us per launch, bf16 vs FP8 (E4M3) KV cache", "unit": "us", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "dtype": "bf16 / e4m3", "data": "synthetic",
+            "config": {"workload": "kv_fp8: 36 layers back to back per shape, L2 flushed before each replay"},
+            "roofline": out}
 
 
 def run_stream(args, dev):
@@ -1018,12 +1070,16 @@ def main(argv=None):
     ap.add_argument("--contract-only", action="store_true",
                     help="print the Fast-dDrive-shaped line without the other workloads' results")
     ap.add_argument("--oracle-sample-s", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork", "stream"],
+    ap.add_argument("--workload", choices=["fast_ddrive", "wam_sweep", "tiny", "fast_dvla", "fork", "stream",
+                                           "kv_fp8"],
                     default="fast_ddrive",
                     help="fast_ddrive: the contract's line; the others print extra lines: wam_sweep (the whole "
                          "WAM-Diff2 decode per block size as one CUDA graph), tiny, fast_dvla (one denoise step of "
                          "the 3-block window), fork (one round for N = 1, 8, 32 rollouts), stream (one new camera frame "
-                         "into the streaming window: insert + streaming-mask attention)")
+                         "into the streaming window: insert + streaming-mask attention), kv_fp8 (bf16 and E4M3 KV "
+                         "cache attention per launch)")
+    ap.add_argument("--rollouts", type=int, default=None, choices=[1, 8, 32],
+                    help="fork workload: only this rollout count (default: 1, 8 and 32)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1035,7 +1091,7 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     extra = {"wam_sweep": run_wam_sweep, "tiny": run_tiny, "fast_dvla": run_fast_dvla, "fork": run_fork,
-             "stream": run_stream}
+             "stream": run_stream, "kv_fp8": run_kv_fp8}
     if args.workload in extra:
         import torch
         torch.cuda.set_device(local_rank)
@@ -1058,7 +1114,7 @@ def main(argv=None):
         dev = f"cuda:{local_rank}"
         line["configs"] = {"tiny": run_tiny(sub, dev), "fast_dvla": run_fast_dvla(sub, dev),
                            "wam_diff2_sweep": run_wam_sweep(sub, dev), "fork_streaming": run_fork(sub, dev),
-                           "stream": run_stream(sub, dev)}
+                           "stream": run_stream(sub, dev), "kv_fp8": run_kv_fp8(sub, dev)}
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -24,7 +24,7 @@ __all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_unm
 
 MASKED, COMMITTED, SCAFFOLD = 0, 1, 2
 INACTIVE, HALF, FULL, DONE = 0, 1, 2, 3
-BD_F32, BD_BF16 = 0, 1
+BD_F32, BD_BF16, BD_E4M3 = 0, 1, 2
 
 
 class BdError(RuntimeError):
@@ -44,7 +44,8 @@ class bd_attn_args(ct.Structure):
                 ("kv_stride", ct.c_int32), ("sm_scale", ct.c_float), ("rope", bd_rope),
                 ("num_splits", ct.c_int32), ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t),
                 ("dev_status", ct.c_void_p), ("prefix_ready", ct.c_int32), ("q_pos", ct.c_void_p),
-                ("wait_limit_ns", ct.c_uint64)]
+                ("wait_limit_ns", ct.c_uint64), ("kv_dtype", ct.c_int32), ("k_exp", ct.c_void_p),
+                ("v_exp", ct.c_void_p)]
 
 
 class bd_fork_args(ct.Structure):
@@ -55,7 +56,9 @@ class bd_fork_args(ct.Structure):
                 ("C", ct.c_int32), ("n_q", ct.c_int32), ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("D", ct.c_int32),
                 ("sm_scale", ct.c_float), ("rope", bd_rope), ("num_splits", ct.c_int32),
                 ("workspace", ct.c_void_p), ("workspace_bytes", ct.c_size_t), ("dev_status", ct.c_void_p),
-                ("prefix_ready", ct.c_int32), ("wait_limit_ns", ct.c_uint64)]
+                ("prefix_ready", ct.c_int32), ("wait_limit_ns", ct.c_uint64), ("kv_dtype", ct.c_int32),
+                ("prefix_k_exp", ct.c_void_p), ("prefix_v_exp", ct.c_void_p), ("priv_k_exp", ct.c_void_p),
+                ("priv_v_exp", ct.c_void_p)]
 
 
 class bd_stream_insert_args(ct.Structure):
@@ -173,6 +176,18 @@ def _rope(rope) -> bd_rope:
     return r
 
 
+def _kv_dtype(k, exps) -> int:
+    """BD_E4M3 for a cache of E4M3 bytes (uint8 or float8_e4m3fn tensors, with
+    their block exponents), else bf16."""
+    fp8 = k.dtype == torch.uint8 or k.dtype == getattr(torch, "float8_e4m3fn", None)
+    if fp8 and any(e is None for e in exps):
+        raise ValueError("an E4M3 cache needs its block exponents (int8 tensors)")
+    for e in exps:
+        if e is not None:
+            assert e.dtype == torch.int8 and e.is_cuda and e.is_contiguous()
+    return BD_E4M3 if fp8 else BD_BF16
+
+
 def _bs(block_start):
     if block_start is None:
         return None, 0
@@ -183,12 +198,13 @@ def _bs(block_start):
 def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0, o=None, lse=None,
                          sm_scale: float = 0.0, rope=None, num_splits: int = 0, workspace=None,
                          dev_status=None, stream=None, prefix_ready: bool = False, q_pos=None,
-                         wait_limit_ns: int = 0):
+                         wait_limit_ns: int = 0, k_exp=None, v_exp=None):
     """Block-causal attention of the active positions.  q [n_q, Hq, D] bf16;
-    k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after).
-    With q_pos (int32 [n_q]) the streaming mask instead: queries over rows
-    [0, C) only, key j visible iff rope k_pos[j] - delta <= q_pos[i].
-    Returns (o [n_q, Hq, D] bf16, lse [Hq, n_q] fp32)."""
+    k, v [Hkv, kv_stride, D] bf16 (prefix rows [0, C), active rows after), or
+    E4M3 bytes (uint8 / float8_e4m3fn) with int8 block exponents k_exp, v_exp
+    [Hkv, ceil(kv_stride / 128)].  With q_pos (int32 [n_q]) the streaming mask
+    instead: queries over rows [0, C) only, key j visible iff rope k_pos[j] -
+    delta <= q_pos[i].  Returns (o [n_q, Hq, D] bf16, lse [Hq, n_q] fp32)."""
     n_q, Hq, D = q.shape
     Hkv, kv_stride, _ = k.shape
     if o is None:
@@ -204,6 +220,8 @@ def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0,
     a.rope = _rope(rope)
     a.num_splits = int(num_splits)
     a.prefix_ready = 1 if prefix_ready else 0
+    a.kv_dtype = _kv_dtype(k, (k_exp, v_exp))
+    a.k_exp, a.v_exp = _ptr(k_exp), _ptr(v_exp)
     if q_pos is not None:  # part of the plan: set before the workspace is sized
         assert q_pos.dtype == torch.int32 and q_pos.is_cuda and q_pos.numel() == n_q
         a.q_pos = q_pos.data_ptr()
@@ -220,9 +238,12 @@ def bd_block_causal_attn(q, k, v, C: int, block_start=None, block_size: int = 0,
 def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: int, block_start=None,
                      block_size: int = 0, o=None, lse=None, sm_scale: float = 0.0, rope=None, num_splits: int = 0,
                      workspace=None, dev_status=None, stream=None, prefix_ready: bool = False,
-                     wait_limit_ns: int = 0):
+                     wait_limit_ns: int = 0, prefix_k_exp=None, prefix_v_exp=None, priv_k_exp=None,
+                     priv_v_exp=None):
     """N rollouts over one shared prefix.  q [N, n_q, Hq, D]; prefix_k/v [Hkv, prefix_stride, D];
-    priv_k/v [N, Hkv, priv_stride, D].  Returns (o [N, n_q, Hq, D], lse [N, Hq, n_q])."""
+    priv_k/v [N, Hkv, priv_stride, D], bf16 or E4M3 bytes with int8 block exponents
+    ([Hkv, ceil(prefix_stride / 128)] and [N, Hkv, ceil(priv_stride / 128)]).
+    Returns (o [N, n_q, Hq, D], lse [N, Hq, n_q])."""
     N, n_q, Hq, D = q.shape
     Hkv, prefix_stride, _ = prefix_k.shape
     priv_stride = priv_k.shape[2]
@@ -241,6 +262,9 @@ def bd_fork_rollouts(q, prefix_k, prefix_v, priv_k, priv_v, priv_len: int, C: in
     a.sm_scale = float(sm_scale)
     a.rope = _rope(rope)
     a.num_splits = int(num_splits)
+    a.kv_dtype = _kv_dtype(prefix_k, (prefix_k_exp, prefix_v_exp, priv_k_exp, priv_v_exp))
+    a.prefix_k_exp, a.prefix_v_exp = _ptr(prefix_k_exp), _ptr(prefix_v_exp)
+    a.priv_k_exp, a.priv_v_exp = _ptr(priv_k_exp), _ptr(priv_v_exp)
     need = lib().bd_fork_workspace_size(a)
     ws = workspace if workspace is not None else _WS["attn"].get(need, q.device)
     a.workspace = None if ws is None else ws.data_ptr()

@@ -18,9 +18,28 @@ namespace {
 
 using namespace bd;
 
-// Work is planned for the 152 SMs of a GB300 so that workspace sizes are plain
-// host arithmetic that does not depend on which device is current.
-constexpr int kPlanSms = 152;
+// SMs of the current device, asked once per device; 152 (a full GB300) when
+// no device answers, so that workspace sizes can be computed on a host without
+// a GPU.  Plans -- and so workspace sizes -- are made for the current device.
+int plan_sms() {
+  static std::mutex mu;
+  static int sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = 152;
+    }
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -61,21 +80,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; the box is {64, 128, 1, ...} unless given.
+// bf16 tensor map with 128-byte swizzle; the box is {64, 128, 1, ...} unless
+// given.  With bytes = true: 8-bit elements, no swizzle, box {dims[0], 128, 1, ...}.
 bd_status make_kv_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                      const uint32_t* box_in = nullptr) {
+                      const uint32_t* box_in = nullptr, bool bytes = false) {
   auto fn = encode_fn();
   if (!fn) return BD_ERR_CUDA;
   cuuint64_t gdim[4];
   cuuint64_t gstr[3];
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kAttnBN), 1, 1};
+  cuuint32_t box[4] = {bytes ? static_cast<cuuint32_t>(dims[0]) : 64u, static_cast<cuuint32_t>(kAttnBN), 1, 1};
   if (box_in)
     for (int i = 0; i < rank; ++i) box[i] = box_in[i];
   cuuint32_t estr[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
   for (int i = 0; i < rank - 1; ++i) gstr[i] = strides[i];
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstr, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                        const_cast<void*>(base), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
 }
@@ -105,6 +126,9 @@ struct AttnDesc {
   int prefix_ready;
   const int32_t* q_pos;  // streaming mask (plain attention only)
   uint64_t wait_ns;
+  int kv_dtype;          // 0 / BD_BF16 or BD_E4M3
+  const int8_t *pk_exp, *pv_exp, *rk_exp, *rv_exp;
+  int p_exp_stride, r_exp_stride, r_exp_row0;
 };
 
 // One call runs as one launch, or as two when its (row tile, KV head) groups
@@ -136,10 +160,11 @@ struct AttnPlan {
 //   * 0.3 x the fraction of the next launch's clusters that cannot be resident
 //     beside this launch's (those cannot start their set-up early).
 int choose_splits(long long groups, long long T, int D) {
+  const int n_sms = plan_sms();
   int best = 1;
   double best_cost = 1e300;
   for (int S = 1; S <= kAttnMaxSplits; ++S) {
-    if (S > 1 && (groups * S > kPlanSms || groups > attn_resident_clusters(S))) continue;
+    if (S > 1 && (groups * S > n_sms || groups > attn_max_clusters(S, D))) continue;
     const long long c = (T + S - 1) / S;
     double cost = static_cast<double>(c);
     if (S > 1) {
@@ -155,7 +180,7 @@ int choose_splits(long long groups, long long T, int D) {
         }
       }
       if (c >= 2 && T - lo_last == c) cost += 0.3;
-      const long long blocked = 2 * groups - attn_resident_clusters(S);
+      const long long blocked = 2 * groups - attn_max_clusters(S, D);
       if (blocked > 0) cost += 0.3 * static_cast<double>(blocked < groups ? blocked : groups) / groups;
     }
     if (cost <= best_cost) {
@@ -179,6 +204,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   }
   if (d.num_splits < 0 || d.num_splits > kAttnMaxSplits) return BD_ERR_INVALID_ARG;
   if (d.rope.enabled && !(d.rope.theta > 0.f)) return BD_ERR_INVALID_ARG;
+  if (d.kv_dtype != 0 && d.kv_dtype != BD_BF16 && d.kv_dtype != BD_E4M3) return BD_ERR_INVALID_ARG;
+  if (d.kv_dtype == BD_E4M3 && (d.rope.enabled || d.q_pos != nullptr)) return BD_ERR_UNSUPPORTED;
   const long long G = d.Hq / d.Hkv;
   const long long per_roll = static_cast<long long>(d.n_q) * G;
   const long long rows = per_roll * d.N;
@@ -200,8 +227,8 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
     // wave), the split count chosen by choose_splits
     const long long groups = static_cast<long long>(pl->m_tiles) * d.Hkv;
     pl->part[0].splits = choose_splits(groups, max_tiles, d.D);
-    const long long waves = groups / kPlanSms;
-    const int bulk = static_cast<int>(waves * kPlanSms / d.Hkv);  // whole waves of row tiles
+    const long long waves = groups / plan_sms();
+    const int bulk = static_cast<int>(waves * plan_sms() / d.Hkv);  // whole waves of row tiles
     if (waves > 0 && bulk > 0 && bulk < pl->m_tiles) {
       const int tail_splits = choose_splits(static_cast<long long>(pl->m_tiles - bulk) * d.Hkv, max_tiles, d.D);
       if (tail_splits > 1) {
@@ -228,6 +255,8 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   bd_status st = plan_attention(d, &pl);
   if (st != BD_OK) return st;
   if (!d.q || !d.pv || !d.pk || !d.rk || !d.rv || !d.o) return BD_ERR_INVALID_ARG;
+  const bool kv8 = d.kv_dtype == BD_E4M3;
+  if (kv8 && (!d.pk_exp || !d.pv_exp || !d.rk_exp || !d.rv_exp)) return BD_ERR_INVALID_ARG;
   if (!aligned(d.q, 16) || !aligned(d.o, 16) || !aligned(d.pk, 16) || !aligned(d.pv, 16) || !aligned(d.rk, 16) ||
       !aligned(d.rv, 16) || (d.lse && !aligned(d.lse, 4)))
     return BD_ERR_UNSUPPORTED;
@@ -264,6 +293,17 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   p.kpos = d.rope.k_pos;
   p.kdelta = d.rope.delta;
   p.wait_ns = wait_limit(d.wait_ns);
+  if (kv8) {
+    p.kv8 = 1;
+    p.prefix_early = 0;
+    p.pk_exp = d.pk_exp;
+    p.pv_exp = d.pv_exp;
+    p.rk_exp = d.rk_exp;
+    p.rv_exp = d.rv_exp;
+    p.p_exp_stride = d.p_exp_stride;
+    p.r_exp_stride = d.r_exp_stride;
+    p.r_exp_row0 = d.r_exp_row0;
+  }
   const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt(static_cast<float>(d.D));
   p.scale_log2 = scale * 1.4426950408889634f;
   // RoPE: the pre-RoPE prefix keys are rotated once for the whole call into
@@ -309,20 +349,21 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
     const uint32_t box[4] = {64, static_cast<uint32_t>(pl.G), 1, static_cast<uint32_t>(kAttnBM / pl.G)};
     if ((st = make_kv_map(&maps.q, d.q, 4, dims, strides, box)) != BD_OK) return st;
   }
+  const uint64_t kv_row_b = kv8 ? static_cast<uint64_t>(d.D) : row_b;  // bytes of one K/V row
   if (d.C > 0) {
     const uint64_t dims[3] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.C), static_cast<uint64_t>(d.Hkv)};
-    const uint64_t kstrides[2] = {row_b, static_cast<uint64_t>(prefix_k_stride) * row_b};
-    const uint64_t strides[2] = {row_b, static_cast<uint64_t>(d.prefix_stride) * row_b};
-    if ((st = make_kv_map(&maps.pk, prefix_k, 3, dims, kstrides)) != BD_OK) return st;
-    if ((st = make_kv_map(&maps.pv, d.pv, 3, dims, strides)) != BD_OK) return st;
+    const uint64_t kstrides[2] = {kv_row_b, static_cast<uint64_t>(prefix_k_stride) * kv_row_b};
+    const uint64_t strides[2] = {kv_row_b, static_cast<uint64_t>(d.prefix_stride) * kv_row_b};
+    if ((st = make_kv_map(&maps.pk, prefix_k, 3, dims, kstrides, nullptr, kv8)) != BD_OK) return st;
+    if ((st = make_kv_map(&maps.pv, d.pv, 3, dims, strides, nullptr, kv8)) != BD_OK) return st;
   }
   {
     const uint64_t dims[4] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(d.priv_len + d.n_q),
                               static_cast<uint64_t>(d.Hkv), static_cast<uint64_t>(d.N)};
-    const uint64_t strides[3] = {row_b, static_cast<uint64_t>(d.priv_stride) * row_b,
-                                 static_cast<uint64_t>(d.priv_stride) * row_b * d.Hkv};
-    if ((st = make_kv_map(&maps.rk, d.rk, 4, dims, strides)) != BD_OK) return st;
-    if ((st = make_kv_map(&maps.rv, d.rv, 4, dims, strides)) != BD_OK) return st;
+    const uint64_t strides[3] = {kv_row_b, static_cast<uint64_t>(d.priv_stride) * kv_row_b,
+                                 static_cast<uint64_t>(d.priv_stride) * kv_row_b * d.Hkv};
+    if ((st = make_kv_map(&maps.rk, d.rk, 4, dims, strides, nullptr, kv8)) != BD_OK) return st;
+    if ((st = make_kv_map(&maps.rv, d.rv, 4, dims, strides, nullptr, kv8)) != BD_OK) return st;
   }
   if (rope && launch_rope_prefix(rp, stream) != cudaSuccess) return BD_ERR_CUDA;
   for (int i = 0; i < pl.n_parts; ++i) {
@@ -341,7 +382,8 @@ AttnDesc desc_of(const bd_attn_args* a) {
   d.pk = a->k;
   d.pv = a->v;
   d.prefix_stride = a->kv_stride;
-  const size_t off = static_cast<size_t>(a->C > 0 ? a->C : 0) * (a->D > 0 ? a->D : 0) * 2;
+  const size_t esz = a->kv_dtype == BD_E4M3 ? 1 : 2;  // bytes of a K/V element
+  const size_t off = static_cast<size_t>(a->C > 0 ? a->C : 0) * (a->D > 0 ? a->D : 0) * esz;
   d.rk = a->k ? static_cast<const char*>(a->k) + off : nullptr;
   d.rv = a->v ? static_cast<const char*>(a->v) + off : nullptr;
   d.priv_stride = a->kv_stride;
@@ -365,6 +407,11 @@ AttnDesc desc_of(const bd_attn_args* a) {
   d.prefix_ready = a->prefix_ready;
   d.q_pos = a->q_pos;
   d.wait_ns = a->wait_limit_ns;
+  d.kv_dtype = a->kv_dtype;
+  d.pk_exp = d.rk_exp = a->k_exp;    // the active rows' exponents are those of rows C.. of the buffer
+  d.pv_exp = d.rv_exp = a->v_exp;
+  d.p_exp_stride = d.r_exp_stride = (a->kv_stride + kAttnBN - 1) / kAttnBN;
+  d.r_exp_row0 = a->C;
   if (d.q_pos) {  // no active rows are read: point the private map at the cache itself
     d.rk = a->k;
     d.rv = a->v;
@@ -402,6 +449,14 @@ AttnDesc desc_of(const bd_fork_args* a) {
   d.ds = a->dev_status;
   d.prefix_ready = a->prefix_ready;
   d.wait_ns = a->wait_limit_ns;
+  d.kv_dtype = a->kv_dtype;
+  d.pk_exp = a->prefix_k_exp;
+  d.pv_exp = a->prefix_v_exp;
+  d.rk_exp = a->priv_k_exp;
+  d.rv_exp = a->priv_v_exp;
+  d.p_exp_stride = (a->prefix_stride + kAttnBN - 1) / kAttnBN;
+  d.r_exp_stride = (a->priv_stride + kAttnBN - 1) / kAttnBN;
+  d.r_exp_row0 = 0;
   return d;
 }
 
@@ -418,7 +473,7 @@ bd_status plan_unmask(const bd_unmask_args* a, int* chunks, int* elems, size_t* 
     return BD_ERR_INVALID_ARG;
   if (a->R > kMaxVerifyRows) return BD_ERR_UNSUPPORTED;  // one CTA row per logits row (grid y)
   const int rows = a->R;
-  vocab_split(rows, a->V, kPlanSms, chunks, elems);
+  vocab_split(rows, a->V, plan_sms(), chunks, elems);
   *ws = unmask_workspace_bytes(a->R);
   return BD_OK;
 }
@@ -432,7 +487,7 @@ bd_status plan_verify(const bd_verify_args* a, int* chunks, int* elems, size_t* 
   if (a->logits_dtype != BD_F32 && a->logits_dtype != BD_BF16) return BD_ERR_INVALID_ARG;
   if (a->logits_ld < a->V || a->logits_ld % 8 != 0) return BD_ERR_INVALID_ARG;
   if (a->noise && !(a->temperature > 0.f)) return BD_ERR_INVALID_ARG;
-  vocab_split(a->n_seq * a->n_rows, a->V, kPlanSms, chunks, elems);
+  vocab_split(a->n_seq * a->n_rows, a->V, plan_sms(), chunks, elems);
   *ws = verify_workspace_bytes(a->n_seq, a->n_rows);
   return BD_OK;
 }

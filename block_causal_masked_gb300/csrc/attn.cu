@@ -36,9 +36,11 @@
 // hardware cluster barriers, which every CTA of the cluster reaches on every
 // path.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -49,13 +51,19 @@ namespace {
 
 constexpr int BM = kAttnBM;
 constexpr int BN = kAttnBN;
-constexpr int kKStages = 3;  // K ring: a stage is free once S = Q.K^T of its tile is done
+constexpr int kKStages = 3;  // K ring: a stage is free once S = Q.K^T of its tile is done (2 with FP8 K/V)
 constexpr int kVStages = 2;  // V ring: a stage is free once P.V of its tile is done
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
 // warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax
 constexpr int kSmWarps = 8;
-constexpr int kThreads = 32 * (2 + kSmWarps);
+// FP8 (E4M3) K/V: two more warps dequantise the tiles, staged by TMA in a ring
+// of kStgStages byte tiles, into the fp16 K / V rings
+constexpr int kConvWarps = 2;
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kStgStages = 3;
+template <bool KV8>
+constexpr int threads_of() { return 32 * (2 + kSmWarps + (KV8 ? kConvWarps : 0)); }
 
 struct TileEntry {
   int rollout;  // -1: shared prefix tile
@@ -67,18 +75,23 @@ enum Bar : int {
   // PFULL / ODONE: two each, by tile parity (tile t uses PFULL + t % 2 and
   // ODONE + t % 2), so that the softmax may run one tile ahead of P.V
   KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 14, QFULL = 16,
-  DRAIN = 17, MERGE_O = 18, NUM_BARS = 19
+  DRAIN = 17, MERGE_O = 18,
+  // FP8 K/V: queries converted to fp16; staging ring of E4M3 tiles
+  QCONV = 19, STG_FULL = 20, STG_EMPTY = 23, NUM_BARS = 26
 };
 
-template <int D>
+template <int D, bool KV8 = false>
 struct Layout {
+  static constexpr int kKSt = KV8 ? 2 : kKStages;  // K ring stages
   static constexpr int kQBytes = BM * D * 2;
-  static constexpr int kKVBytes = BN * D * 2;  // one K or one V tile
+  static constexpr int kKVBytes = BN * D * 2;  // one K or one V tile (16-bit elements)
+  static constexpr int kStgBytes = BN * D;     // one E4M3 tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + kKStages * kKVBytes;
+  static constexpr int kV = kK + kKSt * kKVBytes;
   static constexpr int kRingEnd = kV + kVStages * kKVBytes;
-  static constexpr int kBar = kRingEnd;
+  static constexpr int kStg = kRingEnd;
+  static constexpr int kBar = kStg + (KV8 ? kStgStages * kStgBytes : 0);
   static constexpr int kMisc = kBar + NUM_BARS * 8;
   // the two halves of a row trade tile maxima ([2 parities][2 halves][BM])
   // and final sums ([2 halves][BM])
@@ -92,6 +105,7 @@ struct Layout {
   static constexpr int kRecv = kK;
   static_assert(kRecv + (BM + 2 * kAttnMaxSplits) * D * 2 <= kRingEnd, "merge slices must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
+  static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
   // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -127,6 +141,11 @@ __device__ __forceinline__ int block_end_of(const AttnParams& p, int i) {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
@@ -311,12 +330,16 @@ __device__ uint32_t rope_pair_ff(int pos, double freq, float a, float b, float c
   const FF ys[2] = {y1, y2};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    // [lo_end, hi_end] holds [y - e, y + e]
-    const float lo_end = __fadd_rd(ys[i].hi, __fsub_rd(ys[i].lo, e));
-    const float hi_end = __fadd_ru(ys[i].hi, __fadd_ru(ys[i].lo, e));
-    const uint32_t r0 = bf16_bits_rn(lo_end);
-    ok = ok && r0 == bf16_bits_rn(hi_end);
-    out |= r0 << (16 * i);
+    // y = hi + lo: its distance to m, the midpoint of hi's bf16 interval (hi - m
+    // is exact: both share their top 16 bits), decides the rounding unless it is
+    // within e; the neighbouring intervals' midpoints are 2^15 fp32 ulps away
+    const uint32_t u = __float_as_uint(ys[i].hi);
+    const float m = __uint_as_float((u & 0xffff0000u) | 0x8000u);
+    const float d = __fadd_rn(__fsub_rn(ys[i].hi, m), ys[i].lo);
+    ok = ok && fabsf(d) > e;
+    // |y| above |m| rounds the magnitude up to the next bf16 value
+    const bool up = (d > 0.f) == (ys[i].hi > 0.f);
+    out |= ((u >> 16) + (up ? 1u : 0u)) << (16 * i);
   }
   *decided = ok;
   return out;
@@ -381,10 +404,10 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
 //      weights l_s 2^(m_s - M) / L (M = max m_s, L = sum l_s 2^(m_s - M)),
 //      then stores O = sum w_s O_s in bf16 and, for the first 8 columns,
 //      LSE = (M + log2 L) ln 2.
-template <int D>
+template <int D, bool KV8>
 __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
                               float l_tot, uint64_t* bars, volatile int* abort_flag) {
-  using L = Layout<D>;
+  using L = Layout<D, KV8>;
   constexpr int kCh = D / 8;  // bf16x8 chunks of a row
   constexpr int kThreads = 32 * kSmWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -499,12 +522,150 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   }
 }
 
+// The n-th of the 2 nt E4M3 tiles of a CTA in the converters' order: K 0,
+// then K(j + 1) (while j + 1 < nt) and V(j) for j = 0 .. nt - 1 -- the order in
+// which the products need them (S(t + 1) is issued before P.V(t)).
+__device__ __forceinline__ void kv8_item(int n, int nt, int& t, bool& is_v) {
+  if (n == 0) {
+    t = 0;
+    is_v = false;
+  } else if (n - 1 < 2 * (nt - 1)) {
+    t = ((n - 1) >> 1) + (((n - 1) & 1) ? 0 : 1);
+    is_v = ((n - 1) & 1) != 0;
+  } else {
+    t = nt - 1;
+    is_v = true;
+  }
+}
+
+// 2^e in fp16 (e in [-15, 7]: 2^-15 is subnormal), both halves.
+__device__ __forceinline__ __half2 pow2_f16x2(int e) {
+  const unsigned short b = e >= -14 ? static_cast<unsigned short>((15 + e) << 10) : static_cast<unsigned short>(0x0200);
+  const __half h = __ushort_as_half(b);
+  return __halves2half2(h, h);
+}
+
+// Sixteen E4M3 bytes to sixteen fp16 values times 2^e (exact: the products
+// stay within fp16's range and grid for e in [-15, 7]).
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 x, __half2 sc, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xffffu));
+    const uint32_t b = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+    const __half2 ha = __hmul2(*reinterpret_cast<const __half2*>(&a), sc);
+    const __half2 hb = __hmul2(*reinterpret_cast<const __half2*>(&b), sc);
+    r[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
+    r[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+  }
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+  hi = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// Two bf16 values to two fp16 values (exact for 2^-17 <= |x| < 65504).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  float lo, hi;
+  bf16x2_unpack(w, lo, hi);
+  return pack_f16x2(lo, hi);
+}
+
+// FP8 K/V converters (kConvThreads threads): the queries' tile from bf16 to
+// fp16 in place once it has landed, then every E4M3 K / V tile from its
+// staging stage into its fp16 stage -- the 128-byte-swizzled layout that TMA
+// gives a bf16 tile, which the products read -- scaled by the exponent of
+// each row's 128-row block.  Rows past the segment arrive as zero bytes (TMA
+// fill) and stay zero.  An exponent outside [-15, 7] is clamped and
+// BD_DEV_BAD_INPUT recorded.
+template <int D, bool KV8>
+__device__ void convert_kv8(const AttnParams& p, const TileRange& tr, int nt, uint8_t* smem, uint64_t* bars,
+                            volatile int* abort_flag, int kvh) {
+  using L = Layout<D, KV8>;
+  constexpr int kKSt = L::kKSt;
+  constexpr int kCPR = D / 16;        // 16-byte E4M3 chunks of a key row
+  constexpr int kChunks = BN * kCPR;  // of a tile
+  const int ct = static_cast<int>(threadIdx.x) - 32 * (2 + kSmWarps);
+  int32_t* ds = p.dev_status;
+  bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds, p.wait_ns);
+  if (ok) {
+    uint4* q = reinterpret_cast<uint4*>(smem + L::kQ);
+    for (int i = ct; i < L::kQBytes / 16; i += kConvThreads) {
+      uint4 w = q[i];
+      w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      q[i] = w;
+    }
+    fence_proxy_async_smem();  // generic writes before the products read them
+  }
+  mbar_arrive(&bars[QCONV]);
+  bool bad = false;
+  for (int n = 0; ok && n < 2 * nt; ++n) {
+    int t;
+    bool is_v;
+    kv8_item(n, nt, t, is_v);
+    // the tile's exponents -- its 128 rows span at most two 128-row blocks --
+    // are fetched before the waits, so that they have landed by then
+    const TileEntry te = tile_at(p, tr, t);
+    const int8_t* ex;
+    int row0, valid, n_blk;
+    if (te.rollout < 0) {
+      ex = (is_v ? p.pv_exp : p.pk_exp) + static_cast<size_t>(kvh) * p.p_exp_stride;
+      row0 = te.key0;
+      valid = p.C - te.key0;
+      n_blk = p.p_exp_stride;
+    } else {
+      ex = (is_v ? p.rv_exp : p.rk_exp) + (static_cast<size_t>(te.rollout) * p.Hkv + kvh) * p.r_exp_stride;
+      row0 = p.r_exp_row0 + te.key0;
+      valid = p.priv_len + p.n_q - te.key0;
+      n_blk = p.r_exp_stride;
+    }
+    const int blk0 = row0 >> 7;
+    const int split_row = (blk0 + 1) * 128 - row0;  // first row of the tile in the second block
+    const bool two = (valid < BN ? valid : BN) > split_row && blk0 + 1 < n_blk;
+    int e0 = __ldg(ex + blk0);
+    int e1 = two ? __ldg(ex + blk0 + 1) : 0;
+    if (e0 < -15 || e0 > 7 || e1 < -15 || e1 > 7) {
+      bad = true;
+      e0 = e0 < -15 ? -15 : (e0 > 7 ? 7 : e0);
+      e1 = e1 < -15 ? -15 : (e1 > 7 ? 7 : e1);
+    }
+    const __half2 sc0 = pow2_f16x2(e0), sc1 = pow2_f16x2(e1);
+    const int st = n % kStgStages;
+    if (!mbar_wait(&bars[STG_FULL + st], (n / kStgStages) & 1, abort_flag, ds, p.wait_ns)) break;
+    const int stages = is_v ? kVStages : kKSt;
+    const int slot = t % stages;
+    // the fp16 stage holds tile t - stages until its product is done
+    if (t >= stages &&
+        !mbar_wait(&bars[(is_v ? VEMPTY : KEMPTY) + slot], (t / stages - 1) & 1, abort_flag, ds, p.wait_ns))
+      break;
+    const uint8_t* stg = smem + L::kStg + st * L::kStgBytes;
+    uint8_t* dst = smem + (is_v ? L::kV : L::kK) + slot * L::kKVBytes;
+#pragma unroll 4
+    for (int c = ct; c < kChunks; c += kConvThreads) {
+      const int row = c / kCPR;
+      const int col = (c - row * kCPR) * 16;
+      const uint4 x = *reinterpret_cast<const uint4*>(stg + c * 16);
+      // rows past the segment hold zero bytes: any scale keeps them zero
+      uint4 lo, hi;
+      e4m3x16_to_f16(x, row >= split_row ? sc1 : sc0, lo, hi);
+      *reinterpret_cast<uint4*>(dst + sw128_offset(row, col, BN)) = lo;
+      *reinterpret_cast<uint4*>(dst + sw128_offset(row, col + 8, BN)) = hi;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&bars[(is_v ? VFULL : KFULL) + slot]);
+    mbar_arrive(&bars[STG_EMPTY + st]);
+  }
+  if (bad && ds) atomicOr(ds, BD_DEV_BAD_INPUT);
+}
+
 // STREAM: the streaming mask (q_pos), compiled apart so that the block-causal
-// path carries none of its code.
-template <int D, bool STREAM>
-__global__ void __launch_bounds__(kThreads, 1)
+// path carries none of its code.  KV8: E4M3 K/V with power-of-two block
+// scales, dequantised to fp16 in shared memory by two more warps; the products
+// then take fp16 operands (queries converted in place).
+template <int D, bool STREAM, bool KV8>
+__global__ void __launch_bounds__(threads_of<KV8>(), 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
-  using L = Layout<D>;
+  using L = Layout<D, KV8>;
+  constexpr int kKSt = L::kKSt;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -523,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMA of K tile t into K stage t % 3 and of V tile t into V stage t % 2 (the
   // caller has made sure the stage is free)
   auto issue_tile = [&](int t, bool is_v) {
-    const int s = is_v ? t % kVStages : t % kKStages;
+    const int s = is_v ? t % kVStages : t % kKSt;
     const TileEntry te = tile_at(p, tr, t);
     uint8_t* dst = smem + (is_v ? L::kV : L::kK) + s * L::kKVBytes;
     uint64_t* bar = &bars[(is_v ? VFULL : KFULL) + s];
@@ -542,13 +703,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The first K/V loads (K 0, V 0, K 1, V 1, K 2 -- K runs one tile ahead of
   // V): with early = true only the leading prefix tiles among them, issued
   // before the dependency wait; with early = false the rest.
+  // FP8 K/V: the n-th E4M3 tile in the converters' order (kv8_item) by TMA
+  // into staging stage n % kStgStages (the caller has made sure the stage is
+  // free)
+  auto issue_item = [&](int n) {
+    int t;
+    bool is_v;
+    kv8_item(n, nt, t, is_v);
+    const TileEntry te = tile_at(p, tr, t);
+    uint8_t* dst = smem + L::kStg + (n % kStgStages) * L::kStgBytes;
+    uint64_t* bar = &bars[STG_FULL + n % kStgStages];
+    mbar_arrive_expect_tx(bar, L::kStgBytes);
+    if (te.rollout < 0)
+      tma_load_3d(dst, is_v ? &maps.pv : &maps.pk, 0, te.key0, kvh, bar);
+    else
+      tma_load_4d(dst, is_v ? &maps.rv : &maps.rk, 0, te.key0, kvh, te.rollout, bar);
+  };
+
   auto issue_initial = [&](bool early) {
-    for (int u = 0; u < 5; ++u) {
-      const int t = u >> 1;
-      const bool is_v = (u & 1) != 0;
-      if (t >= nt) break;
-      const bool prefix = tr.lo + t < p.n_prefix_tiles;
-      if (early ? (prefix && p.prefix_early) : !(prefix && p.prefix_early)) issue_tile(t, is_v);
+    if constexpr (KV8) {
+      if (!early)
+        for (int n = 0; n < kStgStages && n < 2 * nt; ++n) issue_item(n);
+    } else {
+      for (int u = 0; u < 5; ++u) {
+        const int t = u >> 1;
+        const bool is_v = (u & 1) != 0;
+        if (t >= nt) break;
+        const bool prefix = tr.lo + t < p.n_prefix_tiles;
+        if (early ? (prefix && p.prefix_early) : !(prefix && p.prefix_early)) issue_tile(t, is_v);
+      }
     }
   };
 
@@ -560,13 +743,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tma_prefetch_desc(&maps.rk);
     tma_prefetch_desc(&maps.rv);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&bars[KFULL + i], 1);
+    // FP8 K/V: the fp16 stages are filled by the converter threads' arrivals
+    for (int i = 0; i < kKSt; ++i) {
+      mbar_init(&bars[KFULL + i], KV8 ? kConvThreads : 1);
       mbar_init(&bars[KEMPTY + i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&bars[VFULL + i], 1);
+      mbar_init(&bars[VFULL + i], KV8 ? kConvThreads : 1);
       mbar_init(&bars[VEMPTY + i], 1);
+    }
+    if (KV8) {
+      mbar_init(&bars[QCONV], kConvThreads);
+      for (int i = 0; i < kStgStages; ++i) {
+        mbar_init(&bars[STG_FULL + i], 1);
+        mbar_init(&bars[STG_EMPTY + i], kConvThreads);
+      }
     }
     mbar_init(&bars[SFULL + 0], 1);
     mbar_init(&bars[SFULL + 1], 1);
@@ -614,7 +805,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   float l_run = 0.f;
   bool have_o = false;
 
-  if (warp == 0) {
+  if (warp == 0 && KV8) {
+    // ---------------------------------------------------------------- TMA producer (FP8 K/V)
+    if (lane == 0 && nt > 0) {
+      // item n goes into staging stage n % 3 once the converters are done with item n - 3
+      int n = kStgStages < 2 * nt ? kStgStages : 2 * nt;  // items issued so far
+      for (; n < 2 * nt; ++n) {
+        if (!mbar_wait(&bars[STG_EMPTY + n % kStgStages], (n / kStgStages - 1) & 1, abort_flag, ds, p.wait_ns))
+          break;
+        issue_item(n);
+      }
+      if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
+      for (int u = n > kStgStages ? n - kStgStages : 0; u < n; ++u)
+        mbar_drain(&bars[STG_FULL + u % kStgStages], (u / kStgStages) & 1, ds);
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
       // K tile t + 1 needs S of tile t - 2 done (its stage), V tile t needs P.V
@@ -623,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk = nt < 3 ? nt : 3, nv = nt < 2 ? nt : 2;  // tiles issued so far
       for (int t = 2; t < nt; ++t) {
         if (t + 1 < nt) {
-          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKStages], ((t + 1) / kKStages - 1) & 1, abort_flag, ds, p.wait_ns)) break;
+          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKSt], ((t + 1) / kKSt - 1) & 1, abort_flag, ds, p.wait_ns)) break;
           issue_tile(t + 1, false);
           nk = t + 2;
         }
@@ -633,23 +838,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every copy issued lands before the CTA gives up its shared memory
       if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
-      for (int u = nk > kKStages ? nk - kKStages : 0; u < nk; ++u)
-        mbar_drain(&bars[KFULL + u % kKStages], (u / kKStages) & 1, ds);
+      for (int u = nk > kKSt ? nk - kKSt : 0; u < nk; ++u)
+        mbar_drain(&bars[KFULL + u % kKSt], (u / kKSt) & 1, ds);
       for (int u = nv > kVStages ? nv - kVStages : 0; u < nv; ++u)
         mbar_drain(&bars[VFULL + u % kVStages], (u / kVStages) & 1, ds);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
-      constexpr uint32_t kIdS = mma_idesc_bf16(BM, BN, false);
-      constexpr uint32_t kIdPV = mma_idesc_bf16(BM, D, true);
+      constexpr uint32_t kIdS = mma_idesc_16(BM, BN, false, !KV8);
+      constexpr uint32_t kIdPV = mma_idesc_16(BM, D, true, !KV8);
       const uint32_t qa = smem_addr(smem + L::kQ);
       auto issue_s = [&](int u) -> bool {
         const int s = u & 1;
-        const int ks = u % kKStages;
+        const int ks = u % kKSt;
         // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
         // point by this thread, and executed in issue order -- has consumed
-        if (!mbar_wait(&bars[KFULL + ks], (u / kKStages) & 1, abort_flag, ds, p.wait_ns)) return false;
+        if (!mbar_wait(&bars[KFULL + ks], (u / kKSt) & 1, abort_flag, ds, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
 #pragma unroll
@@ -663,7 +868,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[KEMPTY + ks]);  // K tile consumed: the producer may refill the stage
         return true;
       };
-      bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds, p.wait_ns);
+      // FP8 K/V: the queries once the converters have made them fp16
+      bool ok = mbar_wait(&bars[KV8 ? QCONV : QFULL], 0, abort_flag, ds, p.wait_ns);
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
@@ -689,6 +895,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[DRAIN]);
       mbar_drain(&bars[DRAIN], 0, ds);
     }
+  } else if (KV8 && warp >= 2 + kSmWarps) {
+    // ---------------------------------------------------------------- FP8 converters
+    if (nt > 0) convert_kv8<D, KV8>(p, tr, nt, smem, bars, abort_flag, kvh);
   } else if (warp < 2 + kSmWarps) {
     // ---------------------------------------------------------------- softmax rows
     // Two warps per TMEM lane quadrant: warp 2 + 4h + q holds the rows of lanes
@@ -879,7 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a = fast_exp2(xa);
             const float b = fast_exp2(xb);
             add2(ls[2 * (j & 3)], ls[2 * (j & 3) + 1], a, b);
-            pk[j] = pack_bf16x2(a, b);
+            pk[j] = KV8 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
           }
           tmem_st16(lane_base + s * BN + c0 + 16 * c, pk);
         }
@@ -933,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (p.num_splits > 1) cluster_merge<D>(p, smem, tmem, m0, have_o, m_run, l_run, bars, abort_flag);
+  if (p.num_splits > 1) cluster_merge<D, KV8>(p, smem, tmem, m0, have_o, m_run, l_run, bars, abort_flag);
 
   tc_fence_before();
   __syncthreads();
@@ -943,11 +1152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool STREAM>
+template <int D, bool STREAM, bool KV8>
 cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
   static PerDeviceOnce configured;  // one per instantiation
-  const int smem = attn_smem_bytes(D);
-  auto kernel = attn_kernel<D, STREAM>;
+  const int smem = attn_smem_bytes(D, KV8);
+  auto kernel = attn_kernel<D, STREAM, KV8>;
   cudaError_t ce = configured.run([&] {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -956,7 +1165,7 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of<KV8>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   for (;;) {
@@ -1100,17 +1309,60 @@ cudaError_t launch_rope_t(const RopeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int attn_smem_bytes(int D) {
+int attn_smem_bytes(int D, bool kv8) {
   // D = 64 is padded so that one CTA (and its 512 TMEM columns) fills an SM.
-  return D == 128 ? Layout<128>::kAlloc : (Layout<64>::kAlloc > 120 * 1024 ? Layout<64>::kAlloc : 120 * 1024);
+  const int a = D == 128 ? (kv8 ? Layout<128, true>::kAlloc : Layout<128>::kAlloc)
+                         : (kv8 ? Layout<64, true>::kAlloc : Layout<64>::kAlloc);
+  return D == 128 || a > 120 * 1024 ? a : 120 * 1024;
+}
+
+int attn_max_clusters(int S, int D) {
+  if (S < 1 || S > kAttnMaxSplits) return 0;
+  static std::mutex mu;
+  static int cache[64][2][kAttnMaxSplits + 1];  // 0: not asked yet, -1: no answer
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return attn_resident_clusters(S);
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  int& c = cache[dev][D == 128 ? 1 : 0][S];
+  if (c == 0) {
+    auto kernel = D == 128 ? attn_kernel<128, false, false> : attn_kernel<64, false, false>;
+    const int smem = attn_smem_bytes(D, false);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3(threads_of<false>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess) {
+      c = n;
+    } else {
+      (void)cudaGetLastError();
+      c = -1;
+    }
+  }
+  return c >= 0 ? c : attn_resident_clusters(S);
 }
 
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream) {
   if (p.q_pos)
-    return p.D == 128 ? launch_attn_t<128, true>(p, maps, m_tiles, stream)
-                      : launch_attn_t<64, true>(p, maps, m_tiles, stream);
-  return p.D == 128 ? launch_attn_t<128, false>(p, maps, m_tiles, stream)
-                    : launch_attn_t<64, false>(p, maps, m_tiles, stream);
+    return p.D == 128 ? launch_attn_t<128, true, false>(p, maps, m_tiles, stream)
+                      : launch_attn_t<64, true, false>(p, maps, m_tiles, stream);
+  if (p.kv8)
+    return p.D == 128 ? launch_attn_t<128, false, true>(p, maps, m_tiles, stream)
+                      : launch_attn_t<64, false, true>(p, maps, m_tiles, stream);
+  return p.D == 128 ? launch_attn_t<128, false, false>(p, maps, m_tiles, stream)
+                    : launch_attn_t<64, false, false>(p, maps, m_tiles, stream);
 }
 
 cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream) {

@@ -41,9 +41,9 @@ constexpr int kAttnMaxTiles = 4096; // K/V tiles of one (row tile, KV head) befo
 constexpr int kAttnMaxSplits = 16;  // KV splits = CTAs of one cluster
 
 // Clusters of S attention CTAs (one CTA per SM: ~200 KB of shared memory and
-// all 512 TMEM columns) that a GB300 holds at once, as
+// all 512 TMEM columns) that a full GB300 holds at once, as
 // cudaOccupancyMaxActiveClusters reports it for 1 <= S <= 16: the GPCs fit
-// fewer wide clusters than 152 / S.
+// fewer wide clusters than 152 / S.  Used when no device can be asked.
 __host__ __device__ constexpr int attn_resident_clusters(int S) {
   constexpr int kTable[17] = {0, 152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7};
   return S >= 1 && S <= 16 ? kTable[S] : 0;
@@ -84,6 +84,14 @@ struct AttnParams {
   const int32_t* kpos;
   int kdelta;
   unsigned long long wait_ns;  // limit of a pipeline wait (drains keep the full limit)
+  // FP8 (E4M3) K/V (kv8 != 0): the tiles arrive as bytes and are dequantised to
+  // fp16 in shared memory; row r of a segment is scaled by 2^exp[., (row0 + r) / 128]
+  int kv8;
+  const int8_t* pk_exp;   // prefix [Hkv, p_exp_stride]
+  const int8_t* pv_exp;
+  const int8_t* rk_exp;   // private [N, Hkv, r_exp_stride]
+  const int8_t* rv_exp;
+  int p_exp_stride, r_exp_stride, r_exp_row0;
 };
 
 // New frame of the streaming cache written into every view's frame slot.
@@ -112,11 +120,15 @@ struct RopeParams {
 
 struct AttnMaps {
   CUtensorMap q;          // Q: 4D (D, G, Hkv, N * n_q), box {64, G, 1, 128 / G}
-  CUtensorMap pk, pv;     // prefix K/V: 3D (D, C, Hkv)
+  CUtensorMap pk, pv;     // prefix K/V: 3D (D, C, Hkv); bf16 box {64, 128, 1}, or E4M3 box {D, 128, 1}
   CUtensorMap rk, rv;     // private K/V: 4D (D, priv_len + n_q, Hkv, N)
 };
 
-int attn_smem_bytes(int D);
+int attn_smem_bytes(int D, bool kv8);
+// Clusters of S attention CTAs (head dim D) the current device holds at once
+// (cudaOccupancyMaxActiveClusters, cached per device), or the full-GB300
+// table when no device answers.
+int attn_max_clusters(int S, int D);
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int m_tiles, cudaStream_t stream);
 cudaError_t launch_rope_prefix(const RopeParams& p, cudaStream_t stream);
 cudaError_t launch_stream_insert(const StreamInsertParams& p, cudaStream_t stream);

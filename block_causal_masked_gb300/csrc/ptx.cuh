@@ -419,6 +419,20 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N, bool b_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with A and B both bf16 (bf16 = true) or both fp16 (type code 0):
+// one tcgen05.mma never mixes the two.
+__host__ __device__ constexpr uint32_t mma_idesc_16(int M, int N, bool b_mn_major, bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two E4M3 values (low byte -> low half) to two fp16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
 // Byte offset of element (row, col) of a 128-byte-swizzled tile of 16-bit values
 // stored as [col / 64] sub-tiles of `rows` x 128 B (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B and a 64-element inner box).

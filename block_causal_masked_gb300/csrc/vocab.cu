@@ -4,12 +4,15 @@
 //   verify_kernel  argmax (greedy or Gumbel-max) of every AR row, then the
 //                  left-to-right speculative match of each sequence.
 //
-// Both are HBM streams: a grid of (chunk, row) CTAs reads each row once with
-// 16-byte loads, keeps a running (max, first argmax, Σexp) per thread and
-// merges it with warp shuffles.  The last CTA to finish a row (atomic ticket,
-// no spinning) merges the row's chunk partials; the last row to finish runs the
-// small per-block / per-sequence decision in the same launch.  Counters are
-// returned to zero, so the workspace needs clearing only once.
+// Both are HBM streams: a grid of (chunk, row) CTAs streams each row once
+// (bulk copies into shared memory), keeps a running (max, first argmax, Σexp)
+// per thread and merges it with warp shuffles.  The chunks of one row are one
+// thread-block cluster: each hands its partial to rank 0 through distributed
+// shared memory, and after one cluster barrier rank 0 merges the row and
+// writes its result.  The last row to finish (atomic ticket, no spinning) runs
+// the small per-block / per-sequence decision in the same launch, reading one
+// result per row.  Counters are returned to zero, so the workspace needs
+// clearing only once.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -583,7 +586,10 @@ static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) break;
     (void)cudaGetLastError();
-    vocab_split(rows, V, 152, &p.chunks, &p.chunk_elems, 8);
+    int sms = 152;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    vocab_split(rows, V, sms, &p.chunks, &p.chunk_elems, 8);
   }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
   return e == cudaSuccess ? cudaGetLastError() : e;

@@ -76,9 +76,28 @@ typedef enum bd_status {
 #define BD_FULL 2
 #define BD_DONE 3
 
-/* logits element types */
+/* logits element types; K/V element types (kv_dtype) */
 #define BD_F32 0
 #define BD_BF16 1
+#define BD_E4M3 2
+
+/* -----------------------------------------------------------------------------
+ * FP8 KV cache (kv_dtype = BD_E4M3).
+ *
+ * No counterpart on the pages (their low-precision work concerns weights): a
+ * storage variant of the attention operator that halves the K/V bytes read.
+ * K and V hold 8-bit floats in the OCP E4M3 format (1 sign, 4 exponent bits
+ * of bias 7, 3 mantissa bits; largest value 448), with one power-of-two scale
+ * per (KV head, block of 128 rows of the buffer, counted from its first row):
+ * the dequantised row r of head h is the E4M3 value times 2^exp[h, r / 128].
+ * Exponents must lie in [-15, 7] -- every dequantised value is then exact in
+ * fp16 -- and a kernel that meets another one records BD_DEV_BAD_INPUT and
+ * uses the nearest bound.  The attention is the computation of the bf16
+ * operator over the dequantised cache: the kernel dequantises each tile to
+ * fp16 in shared memory and multiplies in fp16 (queries are converted to
+ * fp16, exact for 2^-17 <= |q| < 65504).  RoPE and the streaming mask are not
+ * supported with E4M3 (BD_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------------*/
 
 /* -----------------------------------------------------------------------------
  * RoPE applied inside the attention operator to pre-RoPE cached keys.
@@ -179,6 +198,11 @@ typedef struct bd_attn_args {
   int32_t prefix_ready;
   const int32_t* q_pos;
   uint64_t wait_limit_ns;
+  /* 0 or BD_BF16: k, v bf16.  BD_E4M3: k, v E4M3 bytes [Hkv, kv_stride, D]
+   * with exponents k_exp, v_exp int8 [Hkv, ceil(kv_stride / 128)] (device) */
+  int32_t kv_dtype;
+  const int8_t* k_exp;
+  const int8_t* v_exp;
 } bd_attn_args;
 
 bd_status bd_block_causal_attn(const bd_attn_args* a, void* stream);
@@ -231,6 +255,14 @@ typedef struct bd_fork_args {
   int32_t* dev_status;
   int32_t prefix_ready;
   uint64_t wait_limit_ns;
+  /* 0 or BD_BF16: bf16.  BD_E4M3: prefix_k/v and priv_k/v hold E4M3 bytes with
+   * exponents prefix_k_exp, prefix_v_exp int8 [Hkv, ceil(prefix_stride / 128)]
+   * and priv_k_exp, priv_v_exp int8 [N, Hkv, ceil(priv_stride / 128)] */
+  int32_t kv_dtype;
+  const int8_t* prefix_k_exp;
+  const int8_t* prefix_v_exp;
+  const int8_t* priv_k_exp;
+  const int8_t* priv_v_exp;
 } bd_fork_args;
 
 bd_status bd_fork_rollouts(const bd_fork_args* a, void* stream);
