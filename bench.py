@@ -473,11 +473,12 @@ def run_fast_dvla(args, dev):
 
 def run_fork(args, dev):
     """Shared-prefix fork + streaming cache, one scaffold-speculative round of
-    the second trajectory block for N = 1, 8, 32 rollouts: 36 x
-    bd_fork_rollouts (MDM pass, the 39-position block bidirectional; 41 private
-    rows of the first trajectory block before it; 4,306 pre-RoPE prefix keys in
-    view-major order rotated at k_pos - 256), 36 x bd_fork_rollouts (AR pass,
-    causal), then the sampled verifier over the N rollouts (AR rows [N, 33,
+    the second trajectory block for N = 1, 8, 32 rollouts: 36 x bd_rope_keys
+    (each layer's 4,306 pre-RoPE prefix keys in view-major order rotated at
+    k_pos - 256, once for both passes), 36 x bd_fork_rollouts (MDM pass, the
+    39-position block bidirectional; 41 private rows of the first trajectory
+    block before it), 36 x bd_fork_rollouts (AR pass, causal), then the sampled
+    verifier over the N rollouts (AR rows [N, 33,
     151936] bf16 with Gumbel noise fp32).  Inputs are drawn on the device from
     a seeded generator; every rollout's AR rows agree with its draft on a
     seeded number of slots."""
@@ -522,18 +523,26 @@ def run_fork(args, dev):
         accs = [torch.empty(N, dtype=torch.int32, device=dev) for _ in range(copies)]
         acc = accs[0]
 
+        # RoPE: each layer's pre-RoPE prefix is rotated once per round (bd_rope_keys)
+        # and both passes read the rotated copy
+        rot = [torch.empty((S.Hkv, C, S.D), dtype=bf, device=dev) for _ in range(S.layers)]
+
+        def rope_keys():
+            for (_, _, pk, _, _, _), r in zip(layers, rot):
+                bd.bd_rope_keys(pk, C, rope, out=r)
+
         def mdm():
-            for q, _, pk, pv, rk, rv in layers:
-                bd.bd_fork_rollouts(q, pk, pv, rk, rv, priv_len, C, block_start=blk, o=o, lse=lse, rope=rope)
+            for (q, _, _, pv, rk, rv), r in zip(layers, rot):
+                bd.bd_fork_rollouts(q, r, pv, rk, rv, priv_len, C, block_start=blk, o=o, lse=lse)
 
         def ar_pass():
-            for _, q, pk, pv, rk, rv in layers:
-                bd.bd_fork_rollouts(q, pk, pv, rk, rv, priv_len, C, block_size=1, o=o, lse=lse, rope=rope)
+            for (_, q, _, pv, rk, rv), r in zip(layers, rot):
+                bd.bd_fork_rollouts(q, r, pv, rk, rv, priv_len, C, block_size=1, o=o, lse=lse)
 
         def verify(i=0):
             bd.bd_spec_verify(win.tokens[i], win.state[i], ars[i], us[i], 1.0, accepted_len=accs[i])
 
-        round_g = _graph(lambda: (mdm(), ar_pass(), verify()))
+        round_g = _graph(lambda: (rope_keys(), mdm(), ar_pass(), verify()))
         reps = max(3, args.steps // (1 + N // 4))
         for _ in range(args.warmup):
             win.reset()
@@ -541,19 +550,23 @@ def run_fork(args, dev):
         step_ms = _replay_ms(round_g, reps, flush, before=win.reset)
         committed = int(acc.sum())
         attn_us = _replay_ms(_graph(lambda: (mdm(), ar_pass())), reps, flush) * 1e3 / (2 * S.layers)
+        rope_us = _replay_ms(_graph(rope_keys), reps, flush) * 1e3 / S.layers
         vf_us = _per_launch_us([lambda i=i: verify(i) for i in range(copies)], win.reset, flush, reps)
         peaks = measured_peaks()
         vis = N * (_attn_visible(C + priv_len, [0, n_q]) + _attn_visible(C + priv_len, [0, n_q], causal=True)) / 2
         nbytes = (2 * S.Hkv * C * S.D * 2 + N * 2 * S.Hkv * (priv_len + n_q) * S.D * 2
                   + 2 * N * n_q * S.Hq * S.D * 2 + N * n_q * S.Hq * 4)
         kernels = {"attn_kernel": _attn_roof(attn_us, nbytes, 4 * S.D * S.Hq * vis, peaks, True),
+                   "rope_prefix_kernel": _vocab_roof(rope_us, 2 * S.Hkv * C * S.D * 2 + C * 4, peaks),
                    "verify_kernel": _vocab_roof(vf_us, N * (E + 1) * S.V * (2 + 4), peaks)}
         lines.append(_extra_line(f"fork_streaming N={N}: 16/2 heads, head dim 128, 36 layers, 4306 pre-RoPE prefix keys "
-                    f"(RoPE at k_pos - 256), trajectory block of 39 positions after 41 private rows per rollout; "
-                    f"one round (MDM fork, causal AR fork, sampled verify of {N} rollouts)",
+                    f"(RoPE at k_pos - 256: one bd_rope_keys per layer, read by both passes), trajectory block of "
+                    f"39 positions after 41 private rows per rollout; one round (RoPE, MDM fork, causal AR fork, "
+                    f"sampled verify of {N} rollouts)",
                     committed, step_ms, args, kernels,
-                    {"gpu_launches_per_step": "2 x 36 x (RoPE pass + attention) + 1", "rollouts": N}))
-        del layers, ar, u, ars, us
+                    {"gpu_launches_per_step": "36 x RoPE + 2 x 36 x attention (+1 when a call splits the rows "
+                                              "into two launches) + 1", "rollouts": N}))
+        del layers, ar, u, ars, us, rot
         torch.cuda.empty_cache()
     return lines
 
@@ -994,11 +1007,11 @@ def run_gpu(args, rank, world, local_rank):
     unmask_us, verify_us = vocab_times(rd, inp, device, reps)
     floor = latency_floor(device, rd.flush, reps)
     torch.cuda.synchronize()
-    clk = clocks.stop()
     total_s = sum(steps_ms) / 1e3
     total_s, committed_all = aggregate(total_s, committed, world, device)
     e2e = e2e_measure(rd, inp, max(3, min(100, args.steps // 2)))
     if rank != 0:
+        clocks.stop()
         return None
     alg = algorithmic(inp)
     peaks = measured_peaks()
@@ -1036,7 +1049,7 @@ def run_gpu(args, rank, world, local_rank):
                                 "frac": alg["verify_bytes"] / verify_us / 1e3 / hbm}},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "_clocks": clocks,   # stopped by main() once every measured workload has run
     }
     if world == 1:
         line["cpu_baseline"] = cpu_baseline(inp)
@@ -1107,15 +1120,18 @@ def main(argv=None):
         import torch
         torch.distributed.init_process_group("nccl")
     line = run_gpu(args, rank, world, local_rank)
-    if line is not None and world == 1 and not args.contract_only:
-        # the other four workloads (and the WAM-Diff2 sweep's five block sizes),
-        # each with its per-kernel rooflines, measured after the contract's line
-        sub = argparse.Namespace(steps=max(5, min(args.steps, 20)), warmup=3)
-        dev = f"cuda:{local_rank}"
-        line["configs"] = {"tiny": run_tiny(sub, dev), "fast_dvla": run_fast_dvla(sub, dev),
-                           "wam_diff2_sweep": run_wam_sweep(sub, dev), "fork_streaming": run_fork(sub, dev),
-                           "stream": run_stream(sub, dev), "kv_fp8": run_kv_fp8(sub, dev)}
     if line is not None:
+        if world == 1 and not args.contract_only:
+            # the other four workloads (and the WAM-Diff2 sweep's five block sizes),
+            # each with its per-kernel rooflines, measured after the contract's line
+            sub = argparse.Namespace(steps=max(5, min(args.steps, 20)), warmup=3)
+            dev = f"cuda:{local_rank}"
+            line["configs"] = {"tiny": run_tiny(sub, dev), "fast_dvla": run_fast_dvla(sub, dev),
+                               "wam_diff2_sweep": run_wam_sweep(sub, dev), "fork_streaming": run_fork(sub, dev),
+                               "stream": run_stream(sub, dev), "kv_fp8": run_kv_fp8(sub, dev)}
+        # SM clocks and throttle reasons sampled from the contract's warm-up
+        # through the last workload's timed region
+        line["clocks"] = line.pop("_clocks").stop()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 __all__ = ["bd_block_causal_attn", "bd_fork_rollouts", "bd_unmask_step", "bd_unmask_step_noalloc",
-           "bd_spec_verify", "bd_stream_insert", "bd_check",
+           "bd_spec_verify", "bd_stream_insert", "bd_rope_keys", "bd_check",
            "bd_status_string", "lib", "BdError", "Workspace", "MASKED", "COMMITTED", "SCAFFOLD",
            "INACTIVE", "HALF", "FULL", "DONE"]
 
@@ -68,6 +68,11 @@ class bd_stream_insert_args(ct.Structure):
                 ("cache_stride", ct.c_int32)]
 
 
+class bd_rope_keys_args(ct.Structure):
+    _fields_ = [("k", ct.c_void_p), ("k_stride", ct.c_int32), ("out", ct.c_void_p), ("Hkv", ct.c_int32),
+                ("C", ct.c_int32), ("D", ct.c_int32), ("rope", bd_rope)]
+
+
 class bd_unmask_args(ct.Structure):
     _fields_ = [("logits", ct.c_void_p), ("logits_dtype", ct.c_int32), ("logits_ld", ct.c_int64),
                 ("R", ct.c_int32), ("V", ct.c_int32), ("logit_row", ct.c_void_p), ("n_pos", ct.c_int32),
@@ -103,7 +108,7 @@ def lib() -> ct.CDLL:
             L = ct.CDLL(path)
             for name, argt in (("bd_block_causal_attn", bd_attn_args), ("bd_fork_rollouts", bd_fork_args),
                                ("bd_unmask_step", bd_unmask_args), ("bd_spec_verify", bd_verify_args),
-                               ("bd_stream_insert", bd_stream_insert_args)):
+                               ("bd_stream_insert", bd_stream_insert_args), ("bd_rope_keys", bd_rope_keys_args)):
                 fn = getattr(L, name)
                 fn.argtypes = [ct.POINTER(argt), ct.c_void_p]
                 fn.restype = ct.c_int
@@ -369,6 +374,22 @@ def bd_stream_insert(k_cache, v_cache, k_pos, new_k, new_v, new_pos, views: int,
     a.views, a.frames, a.per_frame, a.slot = int(views), int(frames), int(per_frame), int(slot)
     a.Hkv, a.D, a.cache_stride = Hkv, D, stride
     _check("bd_stream_insert", lib().bd_stream_insert(a, _stream(stream)))
+
+
+def bd_rope_keys(k, C: int, rope, out=None, stream=None):
+    """The in-operator RoPE rotation written out: keys [0, C) of k (bf16 [Hkv,
+    k_stride, D], pre-RoPE) rotated at rope k_pos - delta into out (bf16 [Hkv,
+    C, D], created when not given), each element the bf16 rounding of the
+    float64 rotation.  Attention calls can then read out with RoPE off."""
+    Hkv, k_stride, D = k.shape
+    if out is None:
+        out = torch.empty((Hkv, C, D), dtype=torch.bfloat16, device=k.device)
+    a = bd_rope_keys_args()
+    a.k, a.k_stride, a.out = k.data_ptr(), k_stride, out.data_ptr()
+    a.Hkv, a.C, a.D = Hkv, int(C), D
+    a.rope = _rope(rope)
+    _check("bd_rope_keys", lib().bd_rope_keys(a, _stream(stream)))
+    return out
 
 
 def bd_check(dev_status, stream=None) -> int:

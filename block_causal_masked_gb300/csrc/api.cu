@@ -250,6 +250,32 @@ bd_status plan_attention(const AttnDesc& d, AttnPlan* pl) {
   return BD_OK;
 }
 
+// Parameters of the rotation of keys [0, C) of k (bf16 [Hkv, stride, D]) at
+// k_pos - delta into out (bf16 [Hkv, C, D]): the frequencies theta^(-2d/D) in
+// float64 and as 0.64 fixed-point turns, and 2 pi / 2^64 as float-float.
+void rope_params(RopeParams* rp, const void* k, long long stride, void* out, int Hkv, int C, int D, const bd_rope& r) {
+  std::memset(rp, 0, sizeof(*rp));
+  rp->k = k;
+  rp->out = out;
+  rp->k_pos = r.k_pos;
+  rp->Hkv = Hkv;
+  rp->C = C;
+  rp->D = D;
+  rp->delta = r.delta;
+  rp->stride = stride;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < D / 2; ++i) {
+    const double f = std::pow(static_cast<double>(r.theta), -2.0 * i / D);
+    double x = f / two_pi;
+    x -= std::floor(x);
+    rp->turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
+    rp->freq[i] = f;
+  }
+  const double c = std::ldexp(two_pi, -64);
+  rp->two_pi_64[0] = static_cast<float>(c);
+  rp->two_pi_64[1] = static_cast<float>(c - static_cast<double>(rp->two_pi_64[0]));
+}
+
 bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   AttnPlan pl;
   bd_status st = plan_attention(d, &pl);
@@ -311,28 +337,9 @@ bd_status run_attention(const AttnDesc& d, cudaStream_t stream) {
   const void* prefix_k = d.pk;
   long long prefix_k_stride = d.prefix_stride;
   RopeParams rp;
-  std::memset(&rp, 0, sizeof(rp));
   const bool rope = d.rope.enabled && d.C > 0;
   if (rope) {
-    rp.k = d.pk;
-    rp.out = static_cast<char*>(d.ws) + pl.rope_off;
-    rp.k_pos = d.rope.k_pos;
-    rp.Hkv = d.Hkv;
-    rp.C = d.C;
-    rp.D = d.D;
-    rp.delta = d.rope.delta;
-    rp.stride = d.prefix_stride;
-    const double two_pi = 6.283185307179586476925286766559;
-    for (int i = 0; i < d.D / 2; ++i) {
-      const double f = std::pow(static_cast<double>(d.rope.theta), -2.0 * i / d.D);
-      double x = f / two_pi;
-      x -= std::floor(x);
-      rp.turns[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
-      rp.freq[i] = f;
-    }
-    const double c = std::ldexp(two_pi, -64);
-    rp.two_pi_64[0] = static_cast<float>(c);
-    rp.two_pi_64[1] = static_cast<float>(c - static_cast<double>(rp.two_pi_64[0]));
+    rope_params(&rp, d.pk, d.prefix_stride, static_cast<char*>(d.ws) + pl.rope_off, d.Hkv, d.C, d.D, d.rope);
     prefix_k = rp.out;
     prefix_k_stride = d.C;
   }
@@ -550,6 +557,25 @@ bd_status bd_stream_insert(const bd_stream_insert_args* a, void* stream) {
   p.D = a->D;
   p.stride = a->cache_stride;
   return launch_stream_insert(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+bd_status bd_rope_keys(const bd_rope_keys_args* a, void* stream) {
+  if (!a || !a->k || !a->out) return BD_ERR_INVALID_ARG;
+  if (a->Hkv < 1 || a->C < 0 || a->k_stride < a->C || !(a->rope.theta > 0.f)) return BD_ERR_INVALID_ARG;
+  if (a->D != 64 && a->D != 128) return BD_ERR_UNSUPPORTED;
+  if (!aligned(a->k, 16) || !aligned(a->out, 16) || (a->rope.k_pos && !aligned(a->rope.k_pos, 4)))
+    return BD_ERR_UNSUPPORTED;
+  const char* k0 = static_cast<const char*>(a->k);
+  const char* k1 = k0 + static_cast<size_t>(a->Hkv) * a->k_stride * a->D * 2;
+  const char* o0 = static_cast<const char*>(a->out);
+  const char* o1 = o0 + static_cast<size_t>(a->Hkv) * a->C * a->D * 2;
+  if (o0 < k1 && k0 < o1) return BD_ERR_INVALID_ARG;  // out overlaps k
+  bd_status st = check_device();
+  if (st != BD_OK) return st;
+  if (a->C == 0) return BD_OK;
+  RopeParams rp;
+  rope_params(&rp, a->k, a->k_stride, a->out, a->Hkv, a->C, a->D, a->rope);
+  return launch_rope_prefix(rp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 size_t bd_unmask_workspace_size(const bd_unmask_args* a) {

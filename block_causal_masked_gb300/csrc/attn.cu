@@ -41,6 +41,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -1192,16 +1193,17 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
 // Rotates the cached prefix keys [0, C) of every KV head at k_pos - delta into
 // a contiguous bf16 copy [Hkv, C, D] (FlashDrive tutorial, "流式推理": the cache
 // stays pre-RoPE; the operator applies the rotation at the re-based
-// positions).  One thread per (KV head, key, 8 rotation pairs): the pairs
-// (d, d + D/2) for d in [8 c, 8 c + 8).  Each rotated element is the bf16
+// positions).  One thread per (KV head, key, 4 rotation pairs): the pairs
+// (d, d + D/2) for d in [4 c, 4 c + 4).  Each rotated element is the bf16
 // rounding (to nearest even) of the rotation computed in float64; see the
 // error bound above.  The pairs whose rounding the fp32 rotation leaves open
 // are queued in shared memory and redone, one pair per lane of whole warps,
 // after the CTA's fast results are stored: from the float64 angle with
 // float-float sin / cos, and in float64 where that still leaves the rounding
 // open (float64 runs at a small fraction of the fp32 rate on this part).
-constexpr int kRopeThreads = 512;
-constexpr int kRopeQueue = 1024;  // queued pairs per CTA (a thread past it redoes its own)
+constexpr int kRopeThreads = 256;
+constexpr int kRopePairs = 4;     // rotation pairs (d, d + D/2) of one thread
+constexpr int kRopeQueue = 512;   // queued pairs per CTA (a thread past it redoes its own)
 
 struct RopeRedo {
   int pos;      // k_pos - delta
@@ -1212,10 +1214,14 @@ struct RopeRedo {
 
 template <int D>
 __global__ void __launch_bounds__(kRopeThreads) rope_prefix_kernel(const __grid_constant__ RopeParams p) {
-  constexpr int kChunks = D / 16;  // 8-pair chunks of a key row
+  constexpr int kChunks = D / 2 / kRopePairs;  // chunks of kRopePairs pairs in a key row
+  constexpr int kW = kRopePairs / 2;           // 32-bit words of a chunk's kRopePairs bf16 values
+  using Vec = typename std::conditional<kW == 4, uint4, uint2>::type;
   __shared__ RopeRedo queue[kRopeQueue];
-  __shared__ int n_queued;
+  __shared__ unsigned long long turns[D / 2];  // per-thread frequency indices vary within a warp: not from
+  __shared__ int n_queued;                     // the constant bank, which serialises distinct addresses
   if (threadIdx.x == 0) n_queued = 0;
+  for (int d = threadIdx.x; d < D / 2; d += blockDim.x) turns[d] = p.turns[d];
   pdl_wait();
   pdl_trigger();
   __syncthreads();
@@ -1232,21 +1238,22 @@ __global__ void __launch_bounds__(kRopeThreads) rope_prefix_kernel(const __grid_
     __nv_bfloat16* dst = out + static_cast<size_t>(row) * D;
     const int pos = (p.k_pos ? __ldg(p.k_pos + key) : key) - p.delta;
     const float delta = kRopeSinCosErr + 0x1p-24f + static_cast<float>(abs(pos)) * 0x1p-50f;
-    uint4 xa = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
-    uint4 xb = __ldg(reinterpret_cast<const uint4*>(src + c * 8 + D / 2));
+    const int d0 = c * kRopePairs;
+    Vec xa = __ldg(reinterpret_cast<const Vec*>(src + d0));
+    Vec xb = __ldg(reinterpret_cast<const Vec*>(src + d0 + D / 2));
     const uint32_t* wa = reinterpret_cast<const uint32_t*>(&xa);
     const uint32_t* wb = reinterpret_cast<const uint32_t*>(&xb);
-    float a[8], b[8], ya[8], yb[8];
+    float a[kRopePairs], b[kRopePairs], ya[kRopePairs], yb[kRopePairs];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kW; ++w) {
       bf16x2_unpack(wa[w], a[2 * w], a[2 * w + 1]);
       bf16x2_unpack(wb[w], b[2 * w], b[2 * w + 1]);
     }
     unsigned redo = 0;  // pairs whose rounding the fp32 rotation does not settle
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kRopePairs; ++j) {
       float cs, sn;
-      rope_cos_sin(pos, p.turns[c * 8 + j], cs, sn);
+      rope_cos_sin(pos, turns[d0 + j], cs, sn);
       ya[j] = fmaf(a[j], cs, -(b[j] * sn));
       yb[j] = fmaf(b[j], cs, a[j] * sn);
       const float e0 = (fabsf(a[j]) + fabsf(b[j])) * delta * (1.f + 0x1p-20f);
@@ -1254,24 +1261,26 @@ __global__ void __launch_bounds__(kRopeThreads) rope_prefix_kernel(const __grid_
       const float eb = fmaf(fabsf(yb[j]), 0x1p-22f, e0);
       if (!bf16_rounding_decided(ya[j], ea) || !bf16_rounding_decided(yb[j], eb)) redo |= 1u << j;
     }
-    uint32_t oa[4], ob[4];
+    Vec oa, ob;
+    uint32_t* pa = reinterpret_cast<uint32_t*>(&oa);
+    uint32_t* pb = reinterpret_cast<uint32_t*>(&ob);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      oa[w] = pack_bf16x2(ya[2 * w], ya[2 * w + 1]);
-      ob[w] = pack_bf16x2(yb[2 * w], yb[2 * w + 1]);
+    for (int w = 0; w < kW; ++w) {
+      pa[w] = pack_bf16x2(ya[2 * w], ya[2 * w + 1]);
+      pb[w] = pack_bf16x2(yb[2 * w], yb[2 * w + 1]);
     }
-    *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4*>(dst + c * 8 + D / 2) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    *reinterpret_cast<Vec*>(dst + d0) = oa;
+    *reinterpret_cast<Vec*>(dst + d0 + D / 2) = ob;
     if (redo) {
-      const uint32_t at = static_cast<uint32_t>(row * D + c * 8);
+      const uint32_t at = static_cast<uint32_t>(row * D + d0);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kRopePairs; ++j) {
         if (!((redo >> j) & 1u)) continue;
         const int q = atomicAdd(&n_queued, 1);
         if (q < kRopeQueue) {
-          queue[q] = RopeRedo{pos, c * 8 + j, a[j], b[j], at + j};
+          queue[q] = RopeRedo{pos, d0 + j, a[j], b[j], at + j};
         } else {  // the queue is full (never with N(0, 1) keys): this thread redoes the pair itself
-          const uint32_t r = rope_pair_f64(pos, p.freq[c * 8 + j], a[j], b[j]);
+          const uint32_t r = rope_pair_f64(pos, p.freq[d0 + j], a[j], b[j]);
           reinterpret_cast<unsigned short*>(out)[at + j] = static_cast<unsigned short>(r & 0xffffu);
           reinterpret_cast<unsigned short*>(out)[at + j + D / 2] = static_cast<unsigned short>(r >> 16);
         }
@@ -1293,7 +1302,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_prefix_kernel(const __grid_
 
 template <int D>
 cudaError_t launch_rope_t(const RopeParams& p, cudaStream_t stream) {
-  const long long total = static_cast<long long>(p.Hkv) * p.C * (D / 16);
+  const long long total = static_cast<long long>(p.Hkv) * p.C * (D / 2 / kRopePairs);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(static_cast<unsigned>((total + kRopeThreads - 1) / kRopeThreads));

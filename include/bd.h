@@ -311,6 +311,34 @@ typedef struct bd_stream_insert_args {
 bd_status bd_stream_insert(const bd_stream_insert_args* a, void* stream);
 
 /* -----------------------------------------------------------------------------
+ * bd_rope_keys
+ *
+ * FlashDrive tutorial (agifrontier.github.io), "流式推理": RoPE applied to the
+ * pre-RoPE cached keys at the re-based position p - Δ.  The rotation that
+ * bd_block_causal_attn / bd_fork_rollouts apply inside the call (bd_rope),
+ * written out: key s of head h is rotated at k_pos[s] - delta into out[h, s, :],
+ * each element the bf16 rounding of the rotation formed in float64.  One
+ * rotation then serves every attention pass over the same prefix -- the MDM
+ * and AR passes of a speculative round -- which read `out` with RoPE off.
+ *
+ *   k       bf16 [Hkv, k_stride, D] pre-RoPE keys, rows [0, C) rotated
+ *   out     bf16 [Hkv, C, D] (caller-owned; must not overlap k)
+ *   rope    k_pos (device int32 [C] or NULL), delta, theta; `enabled` is ignored
+ * Supported: D in {64, 128}; |k_pos[s] - delta| < 2^24.
+ * ---------------------------------------------------------------------------*/
+typedef struct bd_rope_keys_args {
+  const void* k;
+  int32_t k_stride;
+  void* out;
+  int32_t Hkv;
+  int32_t C;
+  int32_t D;
+  bd_rope rope;
+} bd_rope_keys_args;
+
+bd_status bd_rope_keys(const bd_rope_keys_args* a, void* stream);
+
+/* -----------------------------------------------------------------------------
  * bd_unmask_step
  *
  * Fast-dDrive method summary (e.mffb.com.cn) §3.1 (masked positions predicted

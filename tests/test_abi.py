@@ -35,7 +35,8 @@ def test_library_exports_every_declared_symbol():
     assert set(_declared()) <= exported
 
 
-STRUCTS = ["bd_rope", "bd_attn_args", "bd_fork_args", "bd_unmask_args", "bd_verify_args", "bd_stream_insert_args"]
+STRUCTS = ["bd_rope", "bd_attn_args", "bd_fork_args", "bd_unmask_args", "bd_verify_args", "bd_stream_insert_args",
+           "bd_rope_keys_args"]
 
 
 def test_ctypes_structs_match_c_layout(tmp_path):
@@ -134,6 +135,22 @@ def test_stream_insert_argument_errors_on_host():
         for k, v in kw.items():
             setattr(b, k, v)
         assert bd.lib().bd_stream_insert(b, None) == want, kw
+
+
+def test_rope_keys_argument_errors_on_host():
+    """Bad head dim, misaligned or overlapping buffers, no theta: refused before CUDA."""
+    a = bd.bd_rope_keys_args()
+    a.k, a.out, a.k_stride, a.Hkv, a.C, a.D = FAKE, FAKE + (1 << 20), 100, 2, 64, 128
+    a.rope.theta = 1e4
+    for kw, want in ((dict(D=96), 2), (dict(out=FAKE + 8 + (1 << 20)), 2), (dict(out=FAKE + 64), 1),
+                     (dict(k_stride=10), 1), (dict(k=None), 1)):
+        b = bd.bd_rope_keys_args.from_buffer_copy(a)
+        for k, v in kw.items():
+            setattr(b, k, v)
+        assert bd.lib().bd_rope_keys(b, None) == want, kw
+    b = bd.bd_rope_keys_args.from_buffer_copy(a)
+    b.rope.theta = 0.0
+    assert bd.lib().bd_rope_keys(b, None) == 1
 
 
 def test_streaming_mask_argument_errors_on_host():

@@ -126,6 +126,26 @@ def test_rotated_prefix_keys_bit_exact(D, C, delta, spread):
     assert (bf16_midpoint_distance(rot) < 1e-6).sum() > 0
 
 
+def test_rope_keys_equal_the_operator_rotation():
+    """bd_rope_keys writes the rotation the operator applies: bit-exact to the
+    oracle's bf16 rounding of the float64 rotation, and attention over it with
+    RoPE off equals attention with RoPE in the operator, bitwise."""
+    C = 4096 + 210
+    case = synth.attn_case(16, 0, C=C, block_start=[0, 39], Hq=16, Hkv=2, D=128)
+    k_pos = synth.streaming_prefix_positions()
+    rope = dict(k_pos=i32(k_pos), delta=256, theta=1e4)
+    k = bf16(case.k)
+    rot = bd.bd_rope_keys(k, C, rope)
+    ref = oracle.round_bf16(oracle.rope_rotate(case.k[:, :C], k_pos.astype(np.int64) - 256, 1e4))
+    assert np.array_equal(host(rot).astype(np.float64), ref)
+    blk = i32(case.block_start)
+    o1, l1 = bd.bd_block_causal_attn(bf16(case.q), k, bf16(case.v), C, block_start=blk, rope=rope)
+    k2 = k.clone()
+    k2[:, :C] = rot
+    o2, l2 = bd.bd_block_causal_attn(bf16(case.q), k2, bf16(case.v), C, block_start=blk)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_in_kernel_rope_equals_prerotated_keys():
     """RoPE inside the operator gives bitwise the no-RoPE result on keys rotated
     beforehand (rotated in float64 and rounded to bf16 on the host): the
