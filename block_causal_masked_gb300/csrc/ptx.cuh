@@ -189,6 +189,27 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Adds 1 to *t at GPU scope and returns the old value, as a release of this
+// thread's earlier writes and an acquire for its later reads (the last of a
+// set of CTAs to take a ticket sees every other's writes).
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* t) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+
+// Per-thread register count of the executing warpgroup (all four warps execute
+// it): dec hands registers back to the CTA's pool, inc waits until the pool
+// holds enough.  N is a multiple of 8 in [24, 256].
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier over `count` threads (ids 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -9,9 +9,9 @@
 // per thread and merges it with warp shuffles.  The chunks of one row are one
 // thread-block cluster: each hands its partial to rank 0 through distributed
 // shared memory, and after one cluster barrier rank 0 merges the row and
-// writes its result.  The last row to finish (atomic ticket, no spinning) runs
-// the small per-block / per-sequence decision in the same launch, reading one
-// result per row.  Counters are returned to zero, so the workspace needs
+// writes its result.  The last row to finish (an acquire-release atomic
+// ticket, no spinning) runs the small per-block / per-sequence decision in the
+// same launch, reading one result per row.  Counters are returned to zero, so the workspace needs
 // clearing only once.
 #include <cuda_bf16.h>
 
@@ -407,12 +407,10 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant_
   if (chunk != 0) return;
   if (threadIdx.x == 0) {
     p.row_res[row] = make_float4(r.m, r.s, __int_as_float(r.idx), 0.f);
-    __threadfence();
-    last = atomicAdd(p.grid_ticket, 1u) == static_cast<unsigned>(p.R - 1);
+    last = ticket_acq_rel(p.grid_ticket) == static_cast<unsigned>(p.R - 1);
   }
-  __syncthreads();
+  __syncthreads();  // carries thread 0's acquire to the CTA
   if (!last) return;
-  __threadfence();
   unmask_select(p, dyn);
   if (threadIdx.x == 0) *p.grid_ticket = 0u;
 }
@@ -509,12 +507,10 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant_
   if (chunk != 0) return;
   if (threadIdx.x == 0) {
     p.row_res[row] = make_float4(r.m, 0.f, __int_as_float(r.idx), 0.f);
-    __threadfence();
-    last = atomicAdd(p.seq_ticket + s, 1u) == static_cast<unsigned>(p.n_rows - 1);
+    last = ticket_acq_rel(p.seq_ticket + s) == static_cast<unsigned>(p.n_rows - 1);
   }
-  __syncthreads();
+  __syncthreads();  // carries thread 0's acquire to the CTA
   if (!last) return;
-  __threadfence();
   verify_match(p, s);
   if (threadIdx.x == 0) p.seq_ticket[s] = 0u;
 }
