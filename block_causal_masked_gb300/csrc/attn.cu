@@ -14,16 +14,13 @@
 //     three-stage K ring (a stage is refilled as soon as S of its tile is done)
 //     and a two-stage V ring; the prefix tiles come from one shared tensor map
 //     and are reused by every packed row, private tiles from a per-rollout map;
-//   * warp 1 allocates TMEM and issues S = Q·Kᵀ and O += P·V (P read from
-//     TMEM, O resident in TMEM for the whole KV range), one thread;
-//   * warps 2-9 are two softmax groups of four warps (one per TMEM lane
-//     quadrant); group g takes the key tiles t with t % 2 == g, with its own
-//     TMEM S buffer and O accumulator, so that one group's softmax runs while
-//     the tensor pipe serves the other.  A thread holds a whole 128-key row of
-//     a tile: masked online softmax in fp32 from TMEM, P rounded to bf16 and
-//     written back into its S buffer; the running max is only moved (and O
-//     rescaled in TMEM) when it grows by more than 2^8.  At the end the two
-//     groups' partial rows (max, sum, O) are merged;
+//   * warp 1 allocates TMEM and issues S = Q·Kᵀ (into one of two TMEM S buffers)
+//     and O += P·V (P read from TMEM, O resident in TMEM for the whole KV
+//     range), one thread;
+//   * warps 2-9, two per TMEM lane quadrant, each hold half of the key columns
+//     of their 32 packed rows: masked online softmax in fp32 from TMEM, P
+//     rounded to bf16 and written back into its own S buffer; the running max
+//     is only moved (and O rescaled in TMEM) when it grows by more than 2^8;
 //   * the KV splits of one (row tile, KV head) form a thread-block cluster; at
 //     the end every softmax thread writes its row's normalised O and (max,
 //     sum) for the CTA that owns the row, one cluster barrier makes them
@@ -56,28 +53,18 @@ namespace {
 constexpr int BM = kAttnBM;
 constexpr int BN = kAttnBN;
 constexpr int kKStages = 3;  // K ring: a stage is free once S = Q.K^T of its tile is done (2 with FP8 K/V)
-constexpr int kVStages = 3;  // V ring: a stage is free once P.V of its tile is done (2 with FP8 K/V)
+constexpr int kVStages = 2;  // V ring: a stage is free once P.V of its tile is done
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale running max while the tile max is within 2^8
-// Three warpgroups.  Warpgroup 0: warp 0 TMA producer, warp 1 MMA issuer,
-// warps 2-3 the FP8 (E4M3) K/V converters (idle with bf16 K/V), which
-// dequantise the tiles, staged by TMA in a ring of kStgStages byte tiles, into
-// the fp16 K / V rings.  Warpgroups 1 and 2: the two softmax groups.
-constexpr int kConvWarp0 = 2;
+// warps: 0 TMA producer, 1 MMA issuer, 2..2+kSmWarps softmax
+constexpr int kSmWarps = 8;
+// FP8 (E4M3) K/V: two more warps dequantise the tiles, staged by TMA in a ring
+// of kStgStages byte tiles, into the fp16 K / V rings
 constexpr int kConvWarps = 2;
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kSmWarp0 = 4;
-constexpr int kSmWarps = 8;
 constexpr int kStgStages = 3;
-constexpr int kAttnThreads = 32 * (kSmWarp0 + kSmWarps);
-// Registers per thread: every warp starts with kRegsLaunch (the most that three
-// warps of one SM sub-partition can hold); warpgroup 0 gives registers up
-// (setmaxnreg) so that a softmax thread can hold a whole S row.  Warpgroup 0
-// and the two softmax warpgroups' shares add up to the launch's.
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsCtl = 40;
-constexpr int kRegsSm = 232;
-static_assert(kRegsCtl + 2 * kRegsSm <= 3 * kRegsLaunch, "register split exceeds the launch's registers");
+template <bool KV8>
+constexpr int threads_of() { return 32 * (2 + kSmWarps + (KV8 ? kConvWarps : 0)); }
 
 struct TileEntry {
   int rollout;  // -1: shared prefix tile
@@ -86,44 +73,42 @@ struct TileEntry {
 
 
 enum Bar : int {
-  // SFULL / PFULL / ODONE: one each per softmax group (tile t uses index t % 2)
-  KFULL = 0, VFULL = 3, KEMPTY = 6, VEMPTY = 9, SFULL = 12, PFULL = 14, ODONE = 16, QFULL = 18,
-  DRAIN = 19, MERGE_O = 20,
+  // PFULL / ODONE: two each, by tile parity (tile t uses PFULL + t % 2 and
+  // ODONE + t % 2), so that the softmax may run one tile ahead of P.V
+  KFULL = 0, VFULL = 3, KEMPTY = 5, VEMPTY = 8, SFULL = 10, PFULL = 12, ODONE = 14, QFULL = 16,
+  DRAIN = 17, MERGE_O = 18,
   // FP8 K/V: queries converted to fp16; staging ring of E4M3 tiles
-  QCONV = 21, STG_FULL = 22, STG_EMPTY = 25, NUM_BARS = 28
+  QCONV = 19, STG_FULL = 20, STG_EMPTY = 23, NUM_BARS = 26
 };
 
 template <int D, bool KV8 = false>
 struct Layout {
   static constexpr int kKSt = KV8 ? 2 : kKStages;  // K ring stages
-  static constexpr int kVSt = KV8 ? 2 : kVStages;  // V ring stages
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;  // one K or one V tile (16-bit elements)
   static constexpr int kStgBytes = BN * D;     // one E4M3 tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kV = kK + kKSt * kKVBytes;
-  static constexpr int kRingEnd = kV + kVSt * kKVBytes;
+  static constexpr int kRingEnd = kV + kVStages * kKVBytes;
   static constexpr int kStg = kRingEnd;
   static constexpr int kBar = kStg + (KV8 ? kStgStages * kStgBytes : 0);
   static constexpr int kMisc = kBar + NUM_BARS * 8;
+  // the two halves of a row trade tile maxima ([2 parities][2 halves][BM])
+  // and final sums ([2 halves][BM])
+  static constexpr int kXch = kMisc + 64;
   // (max, sum) of this CTA's rows from every split of the cluster, written by
   // the other CTAs through distributed shared memory: [S][r] float2
-  static constexpr int kMLRecv = kMisc + 64;
+  static constexpr int kMLRecv = kXch + 6 * BM * 4;
   static constexpr int kEnd = kMLRecv + (BM + 2 * kAttnMaxSplits) * 8;
-  // At the end, over the K ring (idle once every S = Q.K^T is done, which the
-  // last P.V's completion implies): the split-KV merge's S bf16 O slices of
-  // this CTA's rows (S * r <= BM + 2 * S rows), then the two softmax groups'
-  // final (max, sum, has-O) of every row, [3][2 groups][BM] floats
+  // split-KV merge, over the K / V rings (idle by then): the S bf16 O
+  // slices of this CTA's rows (S * r <= BM + 2 * S rows)
   static constexpr int kRecv = kK;
-  static constexpr int kXch = kRecv + (BM + 2 * kAttnMaxSplits) * D * 2;
-  static_assert(kXch + 6 * BM * 4 <= kV, "merge slices and the groups' exchange must fit in the K ring");
+  static_assert(kRecv + (BM + 2 * kAttnMaxSplits) * D * 2 <= kRingEnd, "merge slices must fit");
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
   static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
-  // TMEM columns: S buffer of softmax group g at [g BN, (g + 1) BN), its O at
-  // [2 BN + g D, 2 BN + (g + 1) D)
+  // TMEM columns: S buffers [0, 2*BN), O [2*BN, 2*BN + D)
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(2 * BN + 2 * D <= 512, "TMEM columns");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -134,18 +119,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ bool all_lanes(bool v) { return __all_sync(0xffffffffu, v); }
 
 // Same as mbar_wait but ignores the abort flag: used to let copies and MMAs in
-// flight finish before the CTA releases its shared memory and TMEM.  Inline
-// (no call): the warps run under different setmaxnreg register counts, and a
-// called function would be compiled for one of them.
+// flight finish before the CTA releases its shared memory and TMEM.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return;
-  const long long c0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - c0 > wait_cycles(kWaitLimitNs)) {
-      if (dev_status) atomicOr(dev_status, BD_DEV_TIMEOUT);
-      return;
-    }
-  }
+  (void)mbar_wait_bounded(bar, parity, dev_status);
 }
 
 // End (exclusive) of the block that holds active position i, clamped to [1, n_q].
@@ -417,34 +393,11 @@ __device__ __forceinline__ TileEntry tile_at(const AttnParams& p, const TileRang
   return {tr.r_first + k / tr.n_priv, (k % tr.n_priv) * BN};
 }
 
-// 32 consecutive columns of a row's O merged over the two softmax groups,
-// w0 O_0 + w1 O_1 (O_g at TMEM column 2 BN + g D + the column), where a group
-// without an accumulator contributes nothing (its columns are not read).
-template <int D>
-__device__ __forceinline__ void merged_o_chunk(uint32_t o0_col, bool have0, bool have1, float w0, float w1,
-                                               float* v) {
-  if (have0) {
-    tmem_ld32(o0_col, v);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= w0;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = 0.f;
-  }
-  if (have1) {
-    float u[32];
-    tmem_ld32(o0_col + D, u);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = fmaf(u[j], w1, v[j]);
-  }
-}
-
 // Merges the KV splits of a cluster (one CTA per split, same rows).  Called by
 // every thread of every CTA of the cluster once its own K/V range is done:
-//   1. each softmax thread writes half of its row -- O / L in bf16, merged over
-//      the two softmax groups, from TMEM -- into the owner's slice in global
-//      memory (L2), and one thread of the row writes its (max M, sum L)
-//      straight into that CTA's shared memory;
+//   1. each softmax thread writes its half of its row -- O / l in bf16 from
+//      TMEM -- into the workspace slice of the CTA that owns the row, and its
+//      (running max m, sum l) straight into that CTA's shared memory;
 //   2. cluster barrier (release / acquire): every split's rows are written;
 //   3. CTA q owns rows [q * r, (q + 1) * r): one thread pulls its S O slices
 //      (contiguous) into shared memory with one bulk copy; meanwhile each
@@ -453,13 +406,13 @@ __device__ __forceinline__ void merged_o_chunk(uint32_t o0_col, bool have0, bool
 //      then stores O = sum w_s O_s in bf16 and, for the first 8 columns,
 //      LSE = (M + log2 L) ln 2.
 template <int D, bool KV8>
-__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, float M_row, float L_row,
-                              float w0, float w1, bool have0, bool have1, uint64_t* bars, volatile int* abort_flag) {
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, int m0, bool have_o, float m_run,
+                              float l_tot, uint64_t* bars, volatile int* abort_flag) {
   using L = Layout<D, KV8>;
   constexpr int kCh = D / 8;  // bf16x8 chunks of a row
   constexpr int kThreads = 32 * kSmWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool is_sm = warp >= kSmWarp0 && warp < kSmWarp0 + kSmWarps;
+  const bool is_sm = warp >= 2 && warp < 2 + kSmWarps;
   const int S = p.num_splits;
   const int split = blockIdx.x;
   const int rpc = attn_merge_rows(S);
@@ -470,25 +423,33 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   float2* recv_ml = reinterpret_cast<float2*>(smem + L::kMLRecv);         // [S][rpc]
   if (is_sm) {
     const int quad = warp & 3;
-    const int grp = (warp - kSmWarp0) >> 2;
+    const int half = (warp - 2) >> 2;
     const int rl = quad * 32 + lane;
     if (__any_sync(0xffffffffu, m0 + rl < p.rows_per_head)) {
       const int q = rl / rpc;
       const int r = rl - q * rpc;
       uint4* dst = part_o + static_cast<size_t>(q * S + split) * kCh * rpc + r;
-      const uint32_t o0 = tmem + (static_cast<uint32_t>(quad * 32) << 16) + 2 * BN + grp * (D / 2);
-      const float inv_l = L_row > 0.f ? 1.f / L_row : 0.f;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + 2 * BN + half * (D / 2);
+      const float inv_l = have_o && l_tot > 0.f ? 1.f / l_tot : 0.f;
       float v[32];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        merged_o_chunk<D>(o0 + c * 32, have0, have1, w0 * inv_l, w1 * inv_l, v);
+        if (have_o) {
+          tmem_ld32(lane_base + c * 32, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8)
-          __stcg(dst + (grp * (kCh / 2) + c * 4 + q8) * rpc,
-                 make_uint4(pack_bf16x2(v[8 * q8 + 0], v[8 * q8 + 1]), pack_bf16x2(v[8 * q8 + 2], v[8 * q8 + 3]),
-                            pack_bf16x2(v[8 * q8 + 4], v[8 * q8 + 5]), pack_bf16x2(v[8 * q8 + 6], v[8 * q8 + 7])));
+          __stcg(dst + (half * (kCh / 2) + c * 4 + q8) * rpc,
+                 make_uint4(pack_bf16x2(v[8 * q8 + 0] * inv_l, v[8 * q8 + 1] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 2] * inv_l, v[8 * q8 + 3] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 4] * inv_l, v[8 * q8 + 5] * inv_l),
+                            pack_bf16x2(v[8 * q8 + 6] * inv_l, v[8 * q8 + 7] * inv_l)));
       }
-      if (grp == 0) st_cluster_v2(cluster_addr(smem_addr(recv_ml + split * rpc + r), q), M_row, L_row);
+      if (half == 0)
+        st_cluster_v2(cluster_addr(smem_addr(recv_ml + split * rpc + r), q), m_run, have_o ? l_tot : 0.f);
       fence_proxy_async_global();
     }
   }
@@ -508,7 +469,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     mbar_drain(&bars[MERGE_O], 0, ds);
   }
   if (!is_sm) return;
-  const int t = threadIdx.x - 32 * kSmWarp0;
+  const int t = threadIdx.x - 64;
   const int per_roll = p.n_q * p.G;
   const int kvh = blockIdx.z;
   for (int it = t; it < mine * kCh; it += kThreads) {
@@ -624,7 +585,7 @@ __device__ void convert_kv8(const AttnParams& p, const TileRange& tr, int nt, ui
   constexpr int kKSt = L::kKSt;
   constexpr int kCPR = D / 16;        // 16-byte E4M3 chunks of a key row
   constexpr int kChunks = BN * kCPR;  // of a tile
-  const int ct = static_cast<int>(threadIdx.x) - 32 * kConvWarp0;
+  const int ct = static_cast<int>(threadIdx.x) - 32 * (2 + kSmWarps);
   int32_t* ds = p.dev_status;
   bool ok = mbar_wait(&bars[QFULL], 0, abort_flag, ds, p.wait_ns);
   if (ok) {
@@ -671,7 +632,7 @@ __device__ void convert_kv8(const AttnParams& p, const TileRange& tr, int nt, ui
     const __half2 sc0 = pow2_f16x2(e0), sc1 = pow2_f16x2(e1);
     const int st = n % kStgStages;
     if (!mbar_wait(&bars[STG_FULL + st], (n / kStgStages) & 1, abort_flag, ds, p.wait_ns)) break;
-    const int stages = is_v ? L::kVSt : kKSt;
+    const int stages = is_v ? kVStages : kKSt;
     const int slot = t % stages;
     // the fp16 stage holds tile t - stages until its product is done
     if (t >= stages &&
@@ -702,7 +663,7 @@ __device__ void convert_kv8(const AttnParams& p, const TileRange& tr, int nt, ui
 // scales, dequantised to fp16 in shared memory by two more warps; the products
 // then take fp16 operands (queries converted in place).
 template <int D, bool STREAM, bool KV8>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(threads_of<KV8>(), 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps maps) {
   using L = Layout<D, KV8>;
   constexpr int kKSt = L::kKSt;
@@ -724,7 +685,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // TMA of K tile t into K stage t % 3 and of V tile t into V stage t % 2 (the
   // caller has made sure the stage is free)
   auto issue_tile = [&](int t, bool is_v) {
-    const int s = is_v ? t % L::kVSt : t % kKSt;
+    const int s = is_v ? t % kVStages : t % kKSt;
     const TileEntry te = tile_at(p, tr, t);
     uint8_t* dst = smem + (is_v ? L::kV : L::kK) + s * L::kKVBytes;
     uint64_t* bar = &bars[(is_v ? VFULL : KFULL) + s];
@@ -740,9 +701,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   };
 
-  // The first K/V loads (K 0, V 0, K 1, V 1, K 2, V 2: one per ring stage):
-  // with early = true only the leading prefix tiles among them, issued before
-  // the dependency wait; with early = false the rest.
+  // The first K/V loads (K 0, V 0, K 1, V 1, K 2 -- K runs one tile ahead of
+  // V): with early = true only the leading prefix tiles among them, issued
+  // before the dependency wait; with early = false the rest.
   // FP8 K/V: the n-th E4M3 tile in the converters' order (kv8_item) by TMA
   // into staging stage n % kStgStages (the caller has made sure the stage is
   // free)
@@ -765,11 +726,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!early)
         for (int n = 0; n < kStgStages && n < 2 * nt; ++n) issue_item(n);
     } else {
-      for (int u = 0; u < 2 * (kKSt > L::kVSt ? kKSt : L::kVSt); ++u) {
+      for (int u = 0; u < 5; ++u) {
         const int t = u >> 1;
         const bool is_v = (u & 1) != 0;
         if (t >= nt) break;
-        if (t >= (is_v ? L::kVSt : kKSt)) continue;
         const bool prefix = tr.lo + t < p.n_prefix_tiles;
         if (early ? (prefix && p.prefix_early) : !(prefix && p.prefix_early)) issue_tile(t, is_v);
       }
@@ -789,7 +749,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&bars[KFULL + i], KV8 ? kConvThreads : 1);
       mbar_init(&bars[KEMPTY + i], 1);
     }
-    for (int i = 0; i < L::kVSt; ++i) {
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bars[VFULL + i], KV8 ? kConvThreads : 1);
       mbar_init(&bars[VEMPTY + i], 1);
     }
@@ -802,8 +762,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(&bars[SFULL + 0], 1);
     mbar_init(&bars[SFULL + 1], 1);
-    mbar_init(&bars[PFULL + 0], 32 * kSmWarps / 2);  // one softmax group each
-    mbar_init(&bars[PFULL + 1], 32 * kSmWarps / 2);
+    mbar_init(&bars[PFULL + 0], 32 * kSmWarps);
+    mbar_init(&bars[PFULL + 1], 32 * kSmWarps);
     mbar_init(&bars[ODONE + 0], 1);
     mbar_init(&bars[ODONE + 1], 1);
     mbar_init(&bars[QFULL], p.q_tma ? 1 : 128);
@@ -842,144 +802,113 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   pdl_trigger();  // the next kernel may start its own set-up on free SMs
   const uint32_t tmem = misc[0];
   // softmax state of this thread's packed row (softmax warps), kept for the merge
-  float m_run = -INFINITY;  // running max of the group's tiles, log2-scaled
+  float m_run = -INFINITY;  // running max, log2-scaled
   float l_run = 0.f;
-  // the row merged over both softmax groups (softmax warps), kept for the split merge:
-  // max M, sum L, the groups' weights 2^(m_g - M) and whether each group has an O
-  float mrg_M = -INFINITY, mrg_L = 0.f, w0 = 0.f, w1 = 0.f;
-  bool have0 = false, have1 = false;
+  bool have_o = false;
 
-  // Warpgroup 0 hands registers to the softmax warpgroups for the K/V loop and
-  // takes them back before the split merge and the teardown, which every warp runs.
-  // setmaxnreg and bar.sync are warp-aligned: each warp is reconverged
-  // (__syncwarp) first, since its lanes may come from lane-0-only code (load
-  // issue, the MMA loop).
-  if (warp < kSmWarp0) {
-    __syncwarp();
-    regs_dec<kRegsCtl>();
-    if (warp == 0 && KV8) {
-      // ---------------------------------------------------------------- TMA producer (FP8 K/V)
-      if (lane == 0 && nt > 0) {
-        // item n goes into staging stage n % 3 once the converters are done with item n - 3
-        int n = kStgStages < 2 * nt ? kStgStages : 2 * nt;  // items issued so far
-        for (; n < 2 * nt; ++n) {
-          if (!mbar_wait(&bars[STG_EMPTY + n % kStgStages], (n / kStgStages - 1) & 1, abort_flag, ds, p.wait_ns))
-            break;
-          issue_item(n);
-        }
-        if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
-        for (int u = n > kStgStages ? n - kStgStages : 0; u < n; ++u)
-          mbar_drain(&bars[STG_FULL + u % kStgStages], (u / kStgStages) & 1, ds);
+  if (warp == 0 && KV8) {
+    // ---------------------------------------------------------------- TMA producer (FP8 K/V)
+    if (lane == 0 && nt > 0) {
+      // item n goes into staging stage n % 3 once the converters are done with item n - 3
+      int n = kStgStages < 2 * nt ? kStgStages : 2 * nt;  // items issued so far
+      for (; n < 2 * nt; ++n) {
+        if (!mbar_wait(&bars[STG_EMPTY + n % kStgStages], (n / kStgStages - 1) & 1, abort_flag, ds, p.wait_ns))
+          break;
+        issue_item(n);
       }
-    } else if (warp == 0) {
-      // ---------------------------------------------------------------- TMA producer
-      if (lane == 0 && nt > 0) {
-        // K tile t + 1 needs S of tile t - 2 done (its stage of three), V tile
-        // t needs P.V of tile t - 3 done; the products run S(t - 2) before
-        // P.V(t - 3), so issuing in the order K(t + 1), V(t) never waits
-        // behind a later event.  The V ring is three deep because a V tile
-        // takes longer to land from L2 than two tiles' softmax take.
-        constexpr int kVSt = L::kVSt;
-        int nk = nt < kKSt ? nt : kKSt, nv = nt < kVSt ? nt : kVSt;  // tiles issued so far
-        for (int t = 2; t < nt; ++t) {
-          if (t + 1 < nt && t + 1 >= nk) {
-            if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKSt], ((t + 1) / kKSt - 1) & 1, abort_flag, ds, p.wait_ns)) break;
-            issue_tile(t + 1, false);
-            nk = t + 2;
-          }
-          if (t >= nv) {
-            if (!mbar_wait(&bars[VEMPTY + t % kVSt], (t / kVSt - 1) & 1, abort_flag, ds, p.wait_ns)) break;
-            issue_tile(t, true);
-            nv = t + 1;
-          }
-        }
-        // every copy issued lands before the CTA gives up its shared memory
-        if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
-        for (int u = nk > kKSt ? nk - kKSt : 0; u < nk; ++u)
-          mbar_drain(&bars[KFULL + u % kKSt], (u / kKSt) & 1, ds);
-        for (int u = nv > kVSt ? nv - kVSt : 0; u < nv; ++u)
-          mbar_drain(&bars[VFULL + u % kVSt], (u / kVSt) & 1, ds);
-      }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------------- MMA issuer
-      if (lane == 0 && nt > 0) {
-        constexpr uint32_t kIdS = mma_idesc_16(BM, BN, false, !KV8);
-        constexpr uint32_t kIdPV = mma_idesc_16(BM, D, true, !KV8);
-        const uint32_t qa = smem_addr(smem + L::kQ);
-        auto issue_s = [&](int u) -> bool {
-          const int s = u & 1;
-          const int ks = u % kKSt;
-          // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
-          // point by this thread, and executed in issue order -- has consumed
-          if (!mbar_wait(&bars[KFULL + ks], (u / kKSt) & 1, abort_flag, ds, p.wait_ns)) return false;
-          tc_fence_after();
-          const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-            mma_bf16(tmem + s * BN, sw128_desc(qa + qoff, 16, 1024), sw128_desc(ka + koff, 16, 1024), kIdS,
-                     kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars[SFULL + s]);
-          mma_commit(&bars[KEMPTY + ks]);  // K tile consumed: the producer may refill the stage
-          return true;
-        };
-        // FP8 K/V: the queries once the converters have made them fp16
-        bool ok = mbar_wait(&bars[KV8 ? QCONV : QFULL], 0, abort_flag, ds, p.wait_ns);
-        if (ok) {
-          tc_fence_after();
-          ok = issue_s(0);
-        }
-        if (ok && nt > 1) ok = issue_s(1);
-        // Tile t belongs to softmax group t % 2: its P is in S buffer t % 2 and
-        // P.V accumulates into that group's O.  Issue order S(0) S(1) P.V(0) S(2)
-        // P.V(1) S(3) ...: S(t + 2) reuses the buffer P(t) was read from, so it
-        // follows P.V(t); the other group's softmax runs meanwhile.
-        for (int t = 0; ok && t < nt; ++t) {
-          const int grp = t & 1;
-          if (!mbar_wait(&bars[PFULL + grp], (t >> 1) & 1, abort_flag, ds, p.wait_ns)) break;
-          if (!mbar_wait(&bars[VFULL + t % L::kVSt], (t / L::kVSt) & 1, abort_flag, ds, p.wait_ns)) break;
-          tc_fence_after();
-          const uint32_t va = smem_addr(smem + L::kV + (t % L::kVSt) * L::kKVBytes);
-          const uint32_t pt = tmem + grp * BN;  // P(t): keys 2c, 2c + 1 in column c of the buffer
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t voff = kk * 16 * 128;
-            mma_bf16_ts(tmem + 2 * BN + grp * D, pt + kk * 8, sw128_desc(va + voff, BN * 128, 1024), kIdPV,
-                        (t >= 2 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars[ODONE + grp]);
-          mma_commit(&bars[VEMPTY + t % L::kVSt]);
-          if (t + 2 < nt && !issue_s(t + 2)) break;
-        }
-        mma_commit(&bars[DRAIN]);
-        mbar_drain(&bars[DRAIN], 0, ds);
-      }
-    } else {
-      // ---------------------------------------------------------------- FP8 converters
-      if (KV8 && nt > 0) convert_kv8<D, KV8>(p, tr, nt, smem, bars, abort_flag, kvh);
+      if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
+      for (int u = n > kStgStages ? n - kStgStages : 0; u < n; ++u)
+        mbar_drain(&bars[STG_FULL + u % kStgStages], (u / kStgStages) & 1, ds);
     }
-    // Registers come back only once the softmax warpgroups have returned theirs
-    // (named barrier 1): an earlier setmaxnreg.inc here -- an idle warp's, or
-    // that of a CTA without tiles -- could take the registers the softmax
-    // warpgroups' own inc is still waiting for, and neither would ever go on.
-    __syncwarp();
-    named_sync(1, kAttnThreads);
-    regs_inc<kRegsLaunch>();
-  } else {
-    __syncwarp();
-    regs_inc<kRegsSm>();
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && nt > 0) {
+      // K tile t + 1 needs S of tile t - 2 done (its stage), V tile t needs P.V
+      // of tile t - 2 done; S(t - 2) completes before P.V(t - 3), so issuing in
+      // the order K(t + 1), V(t) never waits behind a later event
+      int nk = nt < 3 ? nt : 3, nv = nt < 2 ? nt : 2;  // tiles issued so far
+      for (int t = 2; t < nt; ++t) {
+        if (t + 1 < nt) {
+          if (!mbar_wait(&bars[KEMPTY + (t + 1) % kKSt], ((t + 1) / kKSt - 1) & 1, abort_flag, ds, p.wait_ns)) break;
+          issue_tile(t + 1, false);
+          nk = t + 2;
+        }
+        if (!mbar_wait(&bars[VEMPTY + t % kVStages], (t / kVStages - 1) & 1, abort_flag, ds, p.wait_ns)) break;
+        issue_tile(t, true);
+        nv = t + 1;
+      }
+      // every copy issued lands before the CTA gives up its shared memory
+      if (p.q_tma) mbar_drain(&bars[QFULL], 0, ds);
+      for (int u = nk > kKSt ? nk - kKSt : 0; u < nk; ++u)
+        mbar_drain(&bars[KFULL + u % kKSt], (u / kKSt) & 1, ds);
+      for (int u = nv > kVStages ? nv - kVStages : 0; u < nv; ++u)
+        mbar_drain(&bars[VFULL + u % kVStages], (u / kVStages) & 1, ds);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t kIdS = mma_idesc_16(BM, BN, false, !KV8);
+      constexpr uint32_t kIdPV = mma_idesc_16(BM, D, true, !KV8);
+      const uint32_t qa = smem_addr(smem + L::kQ);
+      auto issue_s = [&](int u) -> bool {
+        const int s = u & 1;
+        const int ks = u % kKSt;
+        // S buffer s held P(u - 2), which P.V(u - 2) -- issued before this
+        // point by this thread, and executed in issue order -- has consumed
+        if (!mbar_wait(&bars[KFULL + ks], (u / kKSt) & 1, abort_flag, ds, p.wait_ns)) return false;
+        tc_fence_after();
+        const uint32_t ka = smem_addr(smem + L::kK + ks * L::kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+          mma_bf16(tmem + s * BN, sw128_desc(qa + qoff, 16, 1024), sw128_desc(ka + koff, 16, 1024), kIdS,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[SFULL + s]);
+        mma_commit(&bars[KEMPTY + ks]);  // K tile consumed: the producer may refill the stage
+        return true;
+      };
+      // FP8 K/V: the queries once the converters have made them fp16
+      bool ok = mbar_wait(&bars[KV8 ? QCONV : QFULL], 0, abort_flag, ds, p.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+      }
+      for (int t = 0; ok && t < nt; ++t) {
+        if (t + 1 < nt && !issue_s(t + 1)) break;
+        if (!mbar_wait(&bars[PFULL + (t & 1)], (t >> 1) & 1, abort_flag, ds, p.wait_ns)) break;
+        if (!mbar_wait(&bars[VFULL + t % kVStages], (t / kVStages) & 1, abort_flag, ds, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t va = smem_addr(smem + L::kV + (t % kVStages) * L::kKVBytes);
+        const uint32_t pt = tmem + (t & 1) * BN;  // P(t), in the S buffer it was formed from
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // keys [16 kk, 16 kk + 16): the half of the row that holds them, 8 packed columns
+          const uint32_t acol = (kk >> 2) * (BN / 2) + (kk & 3) * 8;
+          const uint32_t voff = kk * 16 * 128;
+          mma_bf16_ts(tmem + 2 * BN, pt + acol, sw128_desc(va + voff, BN * 128, 1024), kIdPV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[ODONE + (t & 1)]);
+        mma_commit(&bars[VEMPTY + t % kVStages]);
+      }
+      mma_commit(&bars[DRAIN]);
+      mbar_drain(&bars[DRAIN], 0, ds);
+    }
+  } else if (KV8 && warp >= 2 + kSmWarps) {
+    // ---------------------------------------------------------------- FP8 converters
+    if (nt > 0) convert_kv8<D, KV8>(p, tr, nt, smem, bars, abort_flag, kvh);
+  } else if (warp < 2 + kSmWarps) {
     // ---------------------------------------------------------------- softmax rows
-    // Two groups of four warps, one warp per TMEM lane quadrant in each: group
-    // grp takes the key tiles t with t % 2 == grp, reading S from buffer grp and
-    // writing P back into it, and P.V of its tiles accumulates into its own O.
-    // A thread holds its packed row's 128 keys of a tile.  The groups run one
-    // tile apart, so one group's softmax overlaps the other's products; at the
-    // end the two partial rows of every packed row are merged.
+    // Two warps per TMEM lane quadrant: warp 2 + 4h + q holds the rows of lanes
+    // [32q, 32q + 32) and key columns [h BN/2, (h+1) BN/2) of each S tile (and
+    // O columns [h D/2, (h+1) D/2)); the halves of a row trade their tile maxima
+    // through shared memory and add their sums at the end.
     const int quad = warp & 3;
-    const int grp = (warp - kSmWarp0) >> 2;
+    const int half = (warp - 2) >> 2;
     const int rl = quad * 32 + lane;  // TMEM lane = packed row within the tile
+    const int c0 = half * (BN / 2);   // first key column of this half
     const int row = m0 + rl;
     const int per_roll = p.n_q * p.G;
     const bool valid = row < p.rows_per_head;
@@ -992,7 +921,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     const int qhead = kvh * p.G + g;
     const size_t orow = (static_cast<size_t>(r_row) * p.n_q + i_row) * p.Hq + qhead;
-    if (!p.q_tma && grp == 0) {  // GQA group that does not divide 128: rows gathered by the threads
+    if (!p.q_tma && half == 0) {  // GQA group that does not divide 128: rows gathered by the threads
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + orow * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
@@ -1008,105 +937,110 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int qpos_row = valid && STREAM ? __ldg(p.q_pos + i_row) : INT_MIN;
     const bool warp_active = __any_sync(0xffffffffu, valid);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t s_tm = lane_base + grp * BN;  // this group's S / P buffer
+    float* xch = reinterpret_cast<float*>(smem + L::kXch);
     bool ok = true;
-    int n_mine = 0;  // tiles of this group so far
-    for (int t = grp; t < nt; t += 2, ++n_mine) {
-      if (ok) ok = all_lanes(mbar_wait(&bars[SFULL + grp], n_mine & 1, abort_flag, ds, p.wait_ns));
-      if (!ok) continue;
-      tc_fence_after();
-      // the row of this tile in registers: one TMEM round trip, then S is free again
-      float sv[BN];
+    float v[32];
+    // Named barrier 2 + quad is reached by the quadrant's two warps the same
+    // number of times (nt + 1), whatever the waits return.
+    for (int t = 0; t < nt; ++t) {
+      const int s = t & 1;
+      if (ok) ok = all_lanes(mbar_wait(&bars[SFULL + s], (t >> 1) & 1, abort_flag, ds, p.wait_ns));
+      // this half of the S row in registers: one TMEM round trip, then S is free again
+      float sv[BN / 2];
       float mx = -INFINITY;
-      bool dead = false;  // streaming mask: no row of this warp sees a key of this tile
-      const TileEntry te = tile_at(p, tr, t);
-      int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
-      if (!valid) lim = 0;
-      const int nv = max(0, min(BN, lim - te.key0));
-      if (warp_active) {
-        if constexpr (STREAM) {
-          // key j is visible iff its re-based position is at most the query's.
-          // The range of the positions of this tile (two 8-byte loads per lane,
-          // warp shuffles) settles most rows at once: every key visible
-          // (nothing to mask) or none (the whole row masked); only when some
-          // row's position falls inside the range are the keys compared one
-          // by one, their positions read 16 bytes at a time
-          const int kb = te.key0;
-          const long long lim_q = static_cast<long long>(qpos_row) + p.kdelta;  // stored positions <= lim_q
-          int kp_lo, kp_hi;
-          if (p.kpos == nullptr) {
-            kp_lo = kb;
-            kp_hi = min(kb + BN, p.C) - 1;
-          } else {
-            kp_lo = INT_MAX;
-            kp_hi = INT_MIN;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int k2 = kb + h2 * (BN / 2) + 2 * lane;
+      int nv = 0;
+      bool dead = false;  // streaming mask: no row of this warp sees a key of this half tile
+      if (ok) {
+        tc_fence_after();
+        const TileEntry te = tile_at(p, tr, t);
+        int lim = te.rollout < 0 ? p.C : (te.rollout == r_row ? lim_priv : 0);
+        if (!valid) lim = 0;
+        nv = max(0, min(BN, lim - te.key0));
+        if (warp_active) {
+          if constexpr (STREAM) {
+            // key j is visible iff its re-based position is at most the query's.
+            // The range of the positions of this half tile (one 8-byte load per
+            // lane, warp shuffles) settles most rows at once: every key visible
+            // (nothing to mask) or none (the whole half masked); only when some
+            // row's position falls inside the range are the keys compared one
+            // by one, their positions read 16 bytes at a time
+            const int kb = te.key0 + c0;
+            const long long lim_q = static_cast<long long>(qpos_row) + p.kdelta;  // stored positions <= lim_q
+            int kp_lo, kp_hi;
+            if (p.kpos == nullptr) {
+              kp_lo = kb;
+              kp_hi = min(kb + BN / 2, p.C) - 1;
+            } else {
+              kp_lo = INT_MAX;
+              kp_hi = INT_MIN;
+              const int k2 = kb + 2 * lane;
               if (k2 + 1 < p.C) {
                 const int2 kv = __ldg(reinterpret_cast<const int2*>(p.kpos + k2));
-                kp_lo = min(kp_lo, min(kv.x, kv.y));
-                kp_hi = max(kp_hi, max(kv.x, kv.y));
+                kp_lo = min(kv.x, kv.y);
+                kp_hi = max(kv.x, kv.y);
               } else if (k2 < p.C) {
-                const int kv = __ldg(p.kpos + k2);
-                kp_lo = min(kp_lo, kv);
-                kp_hi = max(kp_hi, kv);
+                kp_lo = kp_hi = __ldg(p.kpos + k2);
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                kp_lo = min(kp_lo, __shfl_xor_sync(0xffffffffu, kp_lo, o));
+                kp_hi = max(kp_hi, __shfl_xor_sync(0xffffffffu, kp_hi, o));
               }
             }
+            const bool all_vis = kb + BN / 2 <= p.C && static_cast<long long>(kp_hi) <= lim_q;
+            const bool none_vis = static_cast<long long>(kp_lo) > lim_q;
+            dead = __all_sync(0xffffffffu, none_vis);  // S is then not even loaded
+            if (!dead) tmem_ld64(lane_base + s * BN + c0, sv);
+            if (!dead && !__all_sync(0xffffffffu, all_vis)) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              kp_lo = min(kp_lo, __shfl_xor_sync(0xffffffffu, kp_lo, o));
-              kp_hi = max(kp_hi, __shfl_xor_sync(0xffffffffu, kp_hi, o));
-            }
-          }
-          const bool all_vis = kb + BN <= p.C && static_cast<long long>(kp_hi) <= lim_q;
-          const bool none_vis = static_cast<long long>(kp_lo) > lim_q;
-          dead = __all_sync(0xffffffffu, none_vis);  // S is then not even loaded
-          if (!dead) tmem_ld128(s_tm, sv);
-          if (!dead && !__all_sync(0xffffffffu, all_vis)) {
+              for (int b = 0; b < BN / 64; ++b) {
+                const int k0 = kb + 32 * b;
+                if (p.kpos != nullptr && k0 + 32 <= p.C) {
+                  int4 kp4[8];
 #pragma unroll
-            for (int b = 0; b < BN / 32; ++b) {
-              const int k0 = kb + 32 * b;
-              if (p.kpos != nullptr && k0 + 32 <= p.C) {
-                int4 kp4[8];
+                  for (int j4 = 0; j4 < 8; ++j4) kp4[j4] = __ldg(reinterpret_cast<const int4*>(p.kpos + k0) + j4);
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) kp4[j4] = __ldg(reinterpret_cast<const int4*>(p.kpos + k0) + j4);
+                  for (int j4 = 0; j4 < 8; ++j4) {
+                    if (kp4[j4].x > lim_q) sv[32 * b + 4 * j4 + 0] = -INFINITY;
+                    if (kp4[j4].y > lim_q) sv[32 * b + 4 * j4 + 1] = -INFINITY;
+                    if (kp4[j4].z > lim_q) sv[32 * b + 4 * j4 + 2] = -INFINITY;
+                    if (kp4[j4].w > lim_q) sv[32 * b + 4 * j4 + 3] = -INFINITY;
+                  }
+                } else {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                  if (kp4[j4].x > lim_q) sv[32 * b + 4 * j4 + 0] = -INFINITY;
-                  if (kp4[j4].y > lim_q) sv[32 * b + 4 * j4 + 1] = -INFINITY;
-                  if (kp4[j4].z > lim_q) sv[32 * b + 4 * j4 + 2] = -INFINITY;
-                  if (kp4[j4].w > lim_q) sv[32 * b + 4 * j4 + 3] = -INFINITY;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  const int key = k0 + j;
-                  const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) : INT_MAX;
-                  if (key >= p.C || kp > lim_q) sv[32 * b + j] = -INFINITY;
+                  for (int j = 0; j < 32; ++j) {
+                    const int key = k0 + j;
+                    const int kp = key < p.C ? (p.kpos ? __ldg(p.kpos + key) : key) : INT_MAX;
+                    if (key >= p.C || kp > lim_q) sv[32 * b + j] = -INFINITY;
+                  }
                 }
               }
             }
+          } else {
+            tmem_ld64(lane_base + s * BN + c0, sv);
+            if (!__all_sync(0xffffffffu, nv >= c0 + BN / 2)) {
+#pragma unroll
+              for (int j = 0; j < BN / 2; ++j)
+                if (c0 + j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+            }
           }
-        } else {
-          tmem_ld128(s_tm, sv);
-          if (!__all_sync(0xffffffffu, nv >= BN)) {
+          if (!dead) {
+            // eight independent chains of three-input maxima
+            float m8[8];
 #pragma unroll
-            for (int j = 0; j < BN; ++j)
-              if (j >= nv) sv[j] = -INFINITY;  // out of the max; exp2 gives 0
+            for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+#pragma unroll
+            for (int j = 8; j < BN / 2; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], sv[j], sv[j + 1]);
+            mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
           }
-        }
-        if (!dead) {
-          // eight independent chains of three-input maxima
-          float m8[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) m8[q] = sv[q];
-#pragma unroll
-          for (int j = 8; j < BN; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], sv[j], sv[j + 1]);
-          mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
         }
       }
+      xch[(s * 2 + half) * BM + rl] = mx;
+      named_sync(2 + quad, 64);  // the two halves of these 32 rows
+      mx = fmaxf(mx, xch[(s * 2 + (half ^ 1)) * BM + rl]);
+      if (!ok) continue;
       const float m_tile = nv > 0 ? mx * p.scale_log2 : -INFINITY;
+      // both halves see the same m_tile and m_run, so they take the same decision
       const bool grow = m_tile > -INFINITY && (m_run == -INFINITY || m_tile > m_run + kRescaleLog2);
       float alpha = 1.f;
       if (grow) {
@@ -1114,22 +1048,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_run = m_tile;
         l_run *= alpha;
       }
-      // P of this tile, rounded to 16 bits, goes into the first half of the
-      // group's S buffer (keys 2c, 2c + 1 in column c)
+      // O must be rescaled (rare once the running max has settled): that needs
+      // the previous tile's P.V to have finished first
+      const bool rescale = warp_active && t > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (rescale) {  // P.V(t - 1) must have finished updating O
+        ok = all_lanes(mbar_wait(&bars[ODONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag, ds, p.wait_ns));
+        if (!ok) continue;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t oa = lane_base + 2 * BN + half * (D / 2) + c * 32;
+          tmem_ld32(oa, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+          tmem_st32(oa, v);
+        }
+      }
+      // P of this tile, rounded to bf16, goes into the first half of this
+      // half's S columns (S buffer s), while the previous tile's P.V -- which
+      // reads the other buffer -- is still running on the tensor pipe
       if (warp_active && dead) {
-        // the tile is hidden from every row of this warp: P = 0
+        // the half tile is hidden from every row of this warp: P = 0
         uint32_t zero[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) zero[j] = 0u;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_st16(s_tm + 16 * c, zero);
+        for (int c = 0; c < BN / 64; ++c) tmem_st16(lane_base + s * BN + c0 + 16 * c, zero);
         tmem_wait_st();
       } else if (warp_active) {
         // masked entries are -inf; a row that has seen no key yet keeps m_run = -inf
         const float mneg = m_run == -INFINITY ? 0.f : -m_run;
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -1140,77 +1091,59 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             add2(ls[2 * (j & 3)], ls[2 * (j & 3) + 1], a, b);
             pk[j] = KV8 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
           }
-          tmem_st16(s_tm + 16 * c, pk);
+          tmem_st16(lane_base + s * BN + c0 + 16 * c, pk);
         }
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
       }
-      // O is rescaled (rare once the running max has settled), after P so that
-      // S is no longer held in registers.  P.V of this group's previous tile
-      // has finished: S(t) was issued after it, and the commit that signalled
-      // S(t) covers every earlier product of the issuer
-      if (warp_active && n_mine > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        float v[32];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint32_t oa = lane_base + 2 * BN + grp * D + c * 32;
-          tmem_ld32(oa, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= alpha;
-          tmem_st32(oa, v);
-        }
+      // P(t) does not wait for P.V(t - 1): it goes into the other S buffer.
+      // The wait on P.V(t - 2) -- already done, since S(t) was issued after it
+      // and tcgen05.mma runs in issue order -- only keeps this thread's view of
+      // each ODONE barrier within one phase (no parity aliasing later).
+      if (t >= 2) {
+        ok = all_lanes(mbar_wait(&bars[ODONE + (t & 1)], ((t - 2) >> 1) & 1, abort_flag, ds, p.wait_ns));
+        if (!ok) continue;
       }
       tc_fence_before();
-      mbar_arrive(&bars[PFULL + grp]);
+      mbar_arrive(&bars[PFULL + (t & 1)]);
     }
-    if (ok && n_mine > 0) {  // this group's last P.V (and, by the commit, every earlier one)
-      ok = all_lanes(mbar_wait(&bars[ODONE + grp], (n_mine - 1) & 1, abort_flag, ds, p.wait_ns));
+    if (ok && nt > 0) {  // the last P.V (and, in issue order, every earlier one)
+      ok = all_lanes(mbar_wait(&bars[ODONE + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag, ds, p.wait_ns));
       tc_fence_after();
     }
-    // Merge of the two groups' partial rows: the weights 2^(m_g - M) of each
-    // group's (max, sum, O) and the row's (M, L), the same in both threads of the row
-    const bool mine = ok && n_mine > 0;
-    float* xch = reinterpret_cast<float*>(smem + L::kXch);
-    xch[grp * BM + rl] = mine ? m_run : -INFINITY;
-    xch[(2 + grp) * BM + rl] = mine ? l_run : 0.f;
-    xch[(4 + grp) * BM + rl] = mine ? 1.f : 0.f;
-    named_sync(2 + quad, 64);  // the row's two threads
-    const float m_g[2] = {xch[rl], xch[BM + rl]};
-    const float l_g[2] = {xch[2 * BM + rl], xch[3 * BM + rl]};
-    have0 = xch[4 * BM + rl] != 0.f;
-    have1 = xch[5 * BM + rl] != 0.f;
-    mrg_M = fmaxf(m_g[0], m_g[1]);
-    w0 = have0 && m_g[0] != -INFINITY ? fast_exp2(m_g[0] - mrg_M) : 0.f;
-    w1 = have1 && m_g[1] != -INFINITY ? fast_exp2(m_g[1] - mrg_M) : 0.f;
-    mrg_L = l_g[0] * w0 + l_g[1] * w1;
+    have_o = ok && nt > 0;
+    xch[(4 + half) * BM + rl] = l_run;
+    named_sync(2 + quad, 64);
+    l_run += xch[(4 + (half ^ 1)) * BM + rl];  // the row's sum over both halves
     if (p.num_splits == 1) {
-      const float inv_l = mrg_L > 0.f ? 1.f / mrg_L : 0.f;
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       if (warp_active) {
-        // this thread stores columns [grp D/2, (grp + 1) D/2) of its row
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          const int col = grp * (D / 2) + c * 32;
-          float v[32];
-          merged_o_chunk<D>(lane_base + 2 * BN + col, have0, have1, w0 * inv_l, w1 * inv_l, v);
+          const int col = half * (D / 2) + c * 32;
+          if (have_o) {
+            tmem_ld32(lane_base + 2 * BN + col, v);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          }
           if (!valid) continue;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
-            dst[qq] = make_uint4(pack_bf16x2(v[8 * qq + 0], v[8 * qq + 1]), pack_bf16x2(v[8 * qq + 2], v[8 * qq + 3]),
-                                 pack_bf16x2(v[8 * qq + 4], v[8 * qq + 5]), pack_bf16x2(v[8 * qq + 6], v[8 * qq + 7]));
+            dst[qq] = make_uint4(pack_bf16x2(v[8 * qq + 0] * inv_l, v[8 * qq + 1] * inv_l),
+                                 pack_bf16x2(v[8 * qq + 2] * inv_l, v[8 * qq + 3] * inv_l),
+                                 pack_bf16x2(v[8 * qq + 4] * inv_l, v[8 * qq + 5] * inv_l),
+                                 pack_bf16x2(v[8 * qq + 6] * inv_l, v[8 * qq + 7] * inv_l));
         }
       }
-      if (valid && grp == 0 && p.lse)
+      if (valid && half == 0 && p.lse)
         p.lse[(static_cast<size_t>(r_row) * p.Hq + qhead) * p.n_q + i_row] =
-            mrg_L > 0.f ? (mrg_M + log2f(mrg_L)) * kLn2 : -INFINITY;
+            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
-    __syncwarp();
-    regs_dec<kRegsLaunch>();
-    named_sync(1, kAttnThreads);
   }
 
-  if (p.num_splits > 1)
-    cluster_merge<D, KV8>(p, smem, tmem, m0, mrg_M, mrg_L, w0, w1, have0, have1, bars, abort_flag);
+  if (p.num_splits > 1) cluster_merge<D, KV8>(p, smem, tmem, m0, have_o, m_run, l_run, bars, abort_flag);
 
   tc_fence_before();
   __syncthreads();
@@ -1228,17 +1161,12 @@ cudaError_t launch_attn_t(AttnParams p, const AttnMaps& maps, int m_tiles, cudaS
   cudaError_t ce = configured.run([&] {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    // the softmax warpgroups' setmaxnreg.inc is only satisfiable if the kernel
-    // was built with the registers per thread the split assumes
-    cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
-    if (e == cudaSuccess && fa.numRegs < kRegsLaunch) e = cudaErrorInvalidConfiguration;
     return e;
   });
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(threads_of<KV8>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   for (;;) {
@@ -1418,7 +1346,7 @@ int attn_max_clusters(int S, int D) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(S, 1, 1);
-    cfg.blockDim = dim3(kAttnThreads);
+    cfg.blockDim = dim3(threads_of<false>());
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -198,18 +198,6 @@ __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* t) {
   return old;
 }
 
-// Per-thread register count of the executing warpgroup (all four warps execute
-// it): dec hands registers back to the CTA's pool, inc waits until the pool
-// holds enough.  N is a multiple of 8 in [24, 256].
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Named barrier over `count` threads (ids 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
