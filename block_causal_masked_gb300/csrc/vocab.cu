@@ -317,9 +317,16 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
       #pragma unroll 1
       for (int j = plo + tid; j < lo; j += kThreads) prev_done += st0[j] != BD_MASKED;
     }
-    if (masked) atomicAdd(&cnt[0], masked);
-    if (cand) atomicAdd(&cnt[1], cand);
-    if (prev_done) atomicAdd(&cnt[2], prev_done);
+    // one shared-memory atomic per warp: every thread adding its own count to
+    // the same word serialises them
+    masked = __reduce_add_sync(0xffffffffu, masked);
+    cand = __reduce_add_sync(0xffffffffu, cand);
+    prev_done = __reduce_add_sync(0xffffffffu, prev_done);
+    if ((tid & 31) == 0) {
+      if (masked) atomicAdd(&cnt[0], masked);
+      if (cand) atomicAdd(&cnt[1], cand);
+      if (prev_done) atomicAdd(&cnt[2], prev_done);
+    }
     __syncthreads();
     int status;
     if (cnt[0] == 0) {
@@ -369,7 +376,8 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
       for (int j = lo + tid; j < hi; j += kThreads)
         if (pred_s[j] >= 0) p.tokens[j] = pred_s[j];
     }
-    if (ncom) atomicAdd(&cnt[3], ncom);
+    ncom = __reduce_add_sync(0xffffffffu, ncom);
+    if ((tid & 31) == 0 && ncom) atomicAdd(&cnt[3], ncom);
     __syncthreads();
     if (tid == 0) {
       p.n_committed[b] = cnt[3];
