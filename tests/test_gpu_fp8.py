@@ -1,8 +1,9 @@
 """GPU parity of the FP8 (E4M3) KV-cache attention against the float64 oracle
 over the dequantised cache (oracle/kvquant.py), through the C ABI: plain
 block-causal attention (head dims 64 / 128, ragged prefixes, block size 1, 92
-positions over 6 row tiles, fixed and planned KV splits), the shared-prefix
-fork, closed forms that pin the dequantised values (Q = 0: the mean of exactly
+positions over 6 row tiles, fixed and planned KV splits; the decode shapes
+the benchmark times; a call of more row tiles than one wave of SMs, run as two
+launches), the shared-prefix fork, closed forms that pin the dequantised values (Q = 0: the mean of exactly
 the visible dequantised values), an exponent outside [-15, 7] reported as
 BD_ERR_DEVICE_INPUT, and RoPE refused.  Tolerances as for bf16 K/V."""
 import zlib
@@ -56,6 +57,38 @@ def test_fp8_attention_matches_oracle(name, C, bs, Hq, Hkv, D, splits):
     o, lse = _run8(case.q, k8, ke, v8, ve, C, bs, splits)
     o_ref, lse_ref = oracle.block_causal_attention(case.q, kd, vd, C, bs)
     assert_attn_close(o, lse, o_ref, lse_ref, name)
+
+
+BENCH_SHAPES = [
+    # the decode shapes bench.py times for the E4M3 cache, one block of n_q positions, planned splits:
+    # (name, Hq, Hkv, C, n_q)
+    ("wam_diff2_B32", 16, 8, 2048 + 128, 32),
+    ("wam_diff2_B1", 16, 8, 2048 + 128, 1),
+    ("fast_ddrive", 16, 2, 3124, 33),
+]
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,C,n_q", BENCH_SHAPES, ids=[c[0] for c in BENCH_SHAPES])
+def test_fp8_bench_shapes_match_oracle(name, Hq, Hkv, C, n_q):
+    bs = [0, n_q]
+    case = synth.attn_case(75, zlib.crc32(name.encode()) % 1000, C=C, block_start=bs, Hq=Hq, Hkv=Hkv, D=128)
+    k8, ke, v8, ve, kd, vd = _quantised(case)
+    o, lse = _run8(case.q, k8, ke, v8, ve, C, bs)
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, kd, vd, C, bs)
+    assert_attn_close(o, lse, o_ref, lse_ref, name)
+
+
+def test_fp8_two_launch_plan_matches_oracle():
+    """More (row tile, KV head) groups than one wave of SMs with the E4M3 cache:
+    2,500 positions x 8 query heads on one KV head = 157 row tiles, a bulk
+    launch of unsplit row tiles and a tail split wide; block size 100."""
+    n_q, C = 2500, 200
+    bs = list(range(0, n_q, 100)) + [n_q]
+    case = synth.attn_case(76, 0, C=C, block_start=bs, Hq=8, Hkv=1, D=128)
+    k8, ke, v8, ve, kd, vd = _quantised(case)
+    o, lse = _run8(case.q, k8, ke, v8, ve, C, bs)
+    o_ref, lse_ref = oracle.block_causal_attention(case.q, kd, vd, C, bs)
+    assert_attn_close(o, lse, o_ref, lse_ref, "fp8 two-launch")
 
 
 def test_fp8_zero_queries_give_the_mean_of_the_dequantised_values():
