@@ -23,7 +23,11 @@
 namespace bd {
 namespace {
 
-constexpr int kThreads = 256;
+// Threads of a CTA: 128, or 256 where every element costs more (sampled
+// scores: two logarithms per element).  Launched with blockDim.x of either;
+// per-CTA arrays are sized for the larger.
+constexpr int kMaxThreads = 256;
+constexpr int kLightThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxBlock = 1024;   // positions of one block
@@ -97,7 +101,7 @@ __device__ Acc block_reduce(Acc a, Acc* sh) {
   if (lane == 0) sh[warp] = a;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kThreads / 32; ++w) acc_merge(a, sh[w]);
+    for (int w = 1; w < static_cast<int>(blockDim.x) / 32; ++w) acc_merge(a, sh[w]);
   }
   return a;
 }
@@ -153,7 +157,7 @@ __device__ Acc reduce_chunk(const Stream& st, const void* logits, int dtype, lon
     if (ok) ok = mbar_wait_bounded(&st.bars[b], (k / kPieceStages) & 1, st.dev_status, st.wait_ns);
     if (ok) {
       const uint8_t* piece = st.buf + b * stage_bytes;
-      for (int v = threadIdx.x; v < nv; v += kThreads) {
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
         float x[8];
         if (dtype == BD_BF16) {
           const uint4 w = *reinterpret_cast<const uint4*>(piece + 16 * v);
@@ -190,7 +194,7 @@ __device__ Acc reduce_chunk(const Stream& st, const void* logits, int dtype, lon
       mbar_wait_bounded(&st.bars[k % kPieceStages], (k / kPieceStages) & 1, nullptr);
   }
   // ragged tail of the row (only when the row length is not a multiple of 8)
-  for (int i = vend + threadIdx.x; i < hi; i += kThreads) {
+  for (int i = vend + threadIdx.x; i < hi; i += blockDim.x) {
     float x[1] = {load_one(logits, dtype, row_off + i)};
     if (noise) x[0] = gumbel_score(x[0], __ldg(noise + noise_off + i), inv_temp);
     acc_vec<1>(a, x, i, need_sum);
@@ -257,7 +261,7 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
     // size (instruction fetch) costs more than its instruction count.
     const int n_items = max(max(p.n_pos, p.n_blocks + 1), n_res);
 #pragma unroll 1
-    for (int j = tid; j < n_items; j += kThreads) {
+    for (int j = tid; j < n_items; j += blockDim.x) {
       const uint8_t sv = j < p.n_pos ? p.state[j] : 0;
       const int rv = j < p.n_pos ? __ldg(p.logit_row + j) : -1;
       const int bv = j <= p.n_blocks ? __ldg(p.block_start + j) : 0;
@@ -273,7 +277,7 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
   __syncthreads();
   // every masked position with a logits row: prediction, confidence, LSE
 #pragma unroll 1
-  for (int j = tid; j < p.n_pos; j += kThreads) {
+  for (int j = tid; j < p.n_pos; j += blockDim.x) {
     const int row = row_s[j];
     int pred = -1;
     float conf = 0.f, lse = 0.f;
@@ -292,7 +296,7 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
   }
   int ok_local = 1;
   #pragma unroll 1
-  for (int b = tid; b < p.n_blocks; b += kThreads) {
+  for (int b = tid; b < p.n_blocks; b += blockDim.x) {
     const int lo = bs_s[b], hi = bs_s[b + 1];
     ok_local &= lo < hi && hi - lo <= kMaxBlock;
   }
@@ -308,14 +312,14 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
     __syncthreads();
     int masked = 0, cand = 0, prev_done = 0;
     #pragma unroll 1
-    for (int j = lo + tid; j < hi; j += kThreads) {
+    for (int j = lo + tid; j < hi; j += blockDim.x) {
       masked += st0[j] == BD_MASKED;
       cand += pred_s[j] >= 0;
     }
     if (b > 0) {
       const int plo = bs_s[b - 1];
       #pragma unroll 1
-      for (int j = plo + tid; j < lo; j += kThreads) prev_done += st0[j] != BD_MASKED;
+      for (int j = plo + tid; j < lo; j += blockDim.x) prev_done += st0[j] != BD_MASKED;
     }
     // one shared-memory atomic per warp: every thread adding its own count to
     // the same word serialises them
@@ -346,7 +350,7 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
     int ncom = 0;
     if (status == BD_FULL || status == BD_HALF) {
       #pragma unroll 1
-      for (int j = lo + tid; j < hi; j += kThreads) {
+      for (int j = lo + tid; j < hi; j += blockDim.x) {
         if (pred_s[j] < 0) continue;
         const float c = conf_s[j];
         bool take;
@@ -373,7 +377,7 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
       }
     } else if (p.write_draft) {
       #pragma unroll 1
-      for (int j = lo + tid; j < hi; j += kThreads)
+      for (int j = lo + tid; j < hi; j += blockDim.x)
         if (pred_s[j] >= 0) p.tokens[j] = pred_s[j];
     }
     ncom = __reduce_add_sync(0xffffffffu, ncom);
@@ -387,8 +391,8 @@ __device__ void unmask_select(const UnmaskParams& p, uint8_t* dyn) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
-  __shared__ Acc red[kThreads / 32];
+__global__ void __launch_bounds__(kMaxThreads) unmask_kernel(const __grid_constant__ UnmaskParams p) {
+  __shared__ Acc red[kMaxThreads / 32];
   __shared__ __align__(16) float4 parts[kMaxChunks];
   __shared__ int last;
   __shared__ __align__(8) uint64_t bars[kPieceStages];
@@ -434,7 +438,7 @@ __device__ void verify_match(const VerifyParams& p, int s) {
     // one memory round trip: the sequence's state, tokens and row results
     const float4* res = p.row_res + static_cast<size_t>(s) * p.n_rows;
 #pragma unroll 1
-    for (int j = threadIdx.x; j < max(L, p.n_rows); j += kThreads) {
+    for (int j = threadIdx.x; j < max(L, p.n_rows); j += blockDim.x) {
       const uint8_t sv = j < L ? p.state[static_cast<size_t>(s) * L + j] : 0;
       const int tv = j < L ? p.tokens[static_cast<size_t>(s) * L + j] : 0;
       const float4 q = j < p.n_rows ? __ldcg(res + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -482,14 +486,14 @@ __device__ void verify_match(const VerifyParams& p, int s) {
   }
   __syncthreads();
   #pragma unroll 1
-  for (int j = threadIdx.x; j < L; j += kThreads) {
+  for (int j = threadIdx.x; j < L; j += blockDim.x) {
     p.state[static_cast<size_t>(s) * L + j] = st[j];
     p.tokens[static_cast<size_t>(s) * L + j] = tok[j];
   }
 }
 
-__global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
-  __shared__ Acc red[kThreads / 32];
+__global__ void __launch_bounds__(kMaxThreads) verify_kernel(const __grid_constant__ VerifyParams p) {
+  __shared__ Acc red[kMaxThreads / 32];
   __shared__ __align__(16) float4 parts[kMaxChunks];
   __shared__ int last;
   __shared__ __align__(8) uint64_t bars[kPieceStages];
@@ -562,7 +566,7 @@ size_t verify_workspace_bytes(int n_seq, int n_rows) {
 // that many CTAs' room in one GPC; if the device has none, the rows are cut
 // into 8 chunks instead.
 template <typename P>
-static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem, cudaStream_t stream) {
+static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem, int threads, cudaStream_t stream) {
   static PerDeviceOnce configured;  // one instantiation per kernel
   const cudaError_t ce = configured.run([&] {
     cudaError_t e =
@@ -573,7 +577,7 @@ static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.dynamicSmemBytes = smem;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -600,12 +604,14 @@ static cudaError_t launch_rows(void (*kernel)(P), int rows, P p, int V, int smem
 }
 
 cudaError_t launch_unmask(const UnmaskParams& p, cudaStream_t stream) {
-  return launch_rows(unmask_kernel, p.R, p, p.V, stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, false), stream);
+  return launch_rows(unmask_kernel, p.R, p, p.V, stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, false), kLightThreads,
+                     stream);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
   return launch_rows(verify_kernel, p.n_seq * p.n_rows, p, p.V,
-                     stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, p.noise != nullptr), stream);
+                     stream_smem_bytes(p.dtype == BD_BF16 ? 2 : 4, p.noise != nullptr),
+                     p.noise != nullptr ? kMaxThreads : kLightThreads, stream);
 }
 
 }  // namespace bd
